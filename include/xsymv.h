@@ -1,0 +1,147 @@
+/*
+ * xsymv — symmetric / Hermitian matrix-vector product on NVIDIA GB300 (sm_103a)
+ *
+ *     y := alpha * A * x + beta * y
+ *
+ * with A an n-by-n symmetric (xSYMV) or Hermitian (xHEMV) matrix of which only
+ * the upper (uplo = 'U') or lower (uplo = 'L') triangle is stored and read.
+ * This is equation (1) of "CUDA-xSYMV の実装と評価" (Implementation and
+ * evaluation of CUDA-xSYMV; Imamura, Mukunoki, Yamada, Machida, IPSJ SIG
+ * Technical Report 2014-HPC-146), §1.  Its figure "x-symv API" (§2.2) gives
+ * the five entry points and their BLAS-style argument list, reproduced here
+ * with an int status instead of void.  Every stored element leaves HBM once
+ * and serves both A(i,j)*x(j) and A(j,i)*x(i) (§2.1), half the traffic of
+ * GEMV; cross-block partial sums are combined in a fixed order, so results
+ * are bit-identical from run to run (the report's abstract and §2.1,
+ * figure "Atomic").
+ *
+ * Arguments (all entry points; Fortran-BLAS semantics, 0-based in memory):
+ *   uplo   'U'/'u': upper triangle stored; 'L'/'l': lower triangle stored.
+ *   n      order of A, n >= 0.
+ *   alpha  scalar, passed by value.
+ *   A      DEVICE pointer to the matrix, column-major: A(i,j) at A[i + j*lda].
+ *          Only the uplo triangle (diagonal included) is read; for Hermitian
+ *          A the imaginary parts of the diagonal are not read either.
+ *   lda    leading dimension, lda >= max(1, n).
+ *   x      DEVICE pointer; element i at x[kx + i*incx], kx = 0 if incx > 0,
+ *          else (1-n)*incx (negative strides run backwards, as in BLAS).
+ *   incx   stride of x, non-zero.
+ *   beta   scalar.  beta == 0: y is written without being read.
+ *   y      DEVICE pointer, same addressing as x with incy.  Only the n
+ *          elements y(0..n-1) are written.
+ *   incy   stride of y, non-zero.
+ *   alpha == 0 means A and x are not read; alpha == 0 and beta == 1 returns
+ *   at once without touching anything.
+ *
+ * Layout of the element types: xsymv_c32 / xsymv_c64 are (re, im) pairs,
+ * layout-compatible with cuFloatComplex / cuDoubleComplex (float2 / double2);
+ * xsymv_dd is a double-double (hi, lo), the value hi + lo (the report's
+ * cuddreal, a double2).
+ *
+ * Ownership: the caller owns A, x and y (device memory, not freed or kept).
+ * The library owns a workspace per (device, stream), allocated with
+ * cudaMalloc on first use and grown on demand; it lives until the process
+ * exits.  Work is enqueued on the stream set by xsymv_set_stream (default:
+ * the legacy default stream) and runs asynchronously: when a call returns
+ * XSYMV_OK the result is ready once that stream has reached it.  Two calls
+ * on the same stream are ordered; calls on different streams use different
+ * workspaces.
+ *
+ * Status (return value):
+ *   0                 success.
+ *   1, 2, 5, 7, 10    the argument at that position is invalid (BLAS xerbla
+ *                     convention: 1 uplo, 2 n, 5 lda, 7 incx, 10 incy).
+ *                     Arguments are checked before anything is enqueued;
+ *                     nothing is read or written.
+ *   negative          XSYMV_ERR_* below; a CUDA error is recorded and can be
+ *                     read with xsymv_last_cuda_error().
+ */
+#ifndef XSYMV_H
+#define XSYMV_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define XSYMV_API __attribute__((visibility("default")))
+
+typedef struct { float re, im; } xsymv_c32;
+typedef struct { double re, im; } xsymv_c64;
+typedef struct { double hi, lo; } xsymv_dd;
+
+#define XSYMV_OK 0
+#define XSYMV_ERR_CUDA (-1)       /* a CUDA call or kernel launch failed        */
+#define XSYMV_ERR_ALLOC (-2)      /* the workspace could not be allocated       */
+#define XSYMV_ERR_DEVICE (-3)     /* no usable device, or not compute cap. 10.3 */
+#define XSYMV_ERR_VALUE (-4)      /* invalid argument to a non-BLAS entry point */
+
+/* SSYMV: float data, float arithmetic. */
+XSYMV_API int xsymv_s(char uplo, int n, float alpha, const float *A, int lda,
+                      const float *x, int incx, float beta, float *y, int incy);
+
+/* DSYMV: double data, double arithmetic. */
+XSYMV_API int xsymv_d(char uplo, int n, double alpha, const double *A, int lda,
+                      const double *x, int incx, double beta, double *y, int incy);
+
+/* CHEMV: single-complex Hermitian, A(j,i) = conj(A(i,j)). */
+XSYMV_API int xhemv_c(char uplo, int n, xsymv_c32 alpha, const xsymv_c32 *A, int lda,
+                      const xsymv_c32 *x, int incx, xsymv_c32 beta, xsymv_c32 *y, int incy);
+
+/* ZHEMV: double-complex Hermitian. */
+XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_c64 *A, int lda,
+                      const xsymv_c64 *x, int incx, xsymv_c64 beta, xsymv_c64 *y, int incy);
+
+/* WSYMV: double-double data and arithmetic (TwoSum / TwoProd-FMA, after
+ * Hida, Li and Bailey, the report's reference [14] in §2.2).  Input pairs
+ * are renormalised as they are read; results are renormalised pairs. */
+XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int lda,
+                      const xsymv_dd *x, int incx, xsymv_dd beta, xsymv_dd *y, int incy);
+
+/* Stream for subsequent calls from any thread (a cudaStream_t; NULL = the
+ * legacy default stream).  Returns 0. */
+XSYMV_API int xsymv_set_stream(void *stream);
+XSYMV_API void *xsymv_get_stream(void);
+
+/* Human-readable text for a status code (static storage). */
+XSYMV_API const char *xsymv_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call (0 if none). */
+XSYMV_API int xsymv_last_cuda_error(void);
+
+/* ---- measurement hooks (used by the benchmark; off by default) ---------- */
+
+/* Record CUDA events around each call's main kernel and whole call on the
+ * call's stream.  on = 0 disables and discards what was recorded. */
+XSYMV_API int xsymv_timing_enable(int on);
+
+/* Wait for the recorded events, then report the number of timed calls and
+ * the summed device time of their main kernels and of the whole calls (ms).
+ * Clears the record.  Returns 0, or XSYMV_ERR_CUDA. */
+XSYMV_API int xsymv_timing_read(int *calls, double *main_ms, double *call_ms);
+
+/* Number of kernels this library has launched since it was loaded. */
+XSYMV_API long long xsymv_launch_count(void);
+
+/* ---- kernel variants: the tuner's parameter space ----------------------- */
+
+/* kind: 's', 'd', 'c', 'z' or 'w'.  Number of compiled variants (0 for an
+ * unknown kind) and the name of variant index ("vr<VR>_u<U>_w<WARPS>":
+ * 16-byte vectors per lane, columns in flight per warp, warps per block). */
+XSYMV_API int xsymv_variant_count(char kind);
+XSYMV_API const char *xsymv_variant_name(char kind, int index);
+
+/* Force variant index for kind (-1: the built-in tuned choice).
+ * Returns 0 or XSYMV_ERR_VALUE. */
+XSYMV_API int xsymv_set_variant(char kind, int index);
+
+/* The variant index a call of this kind, uplo and n would use. */
+XSYMV_API int xsymv_selected_variant(char kind, char uplo, int n);
+
+/* Workspace bytes a call of this kind, uplo and n needs on the current
+ * device (< 0: XSYMV_ERR_*). */
+XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XSYMV_H */

@@ -1,1 +1,240 @@
-"""GB300-native xSYMV / xHEMV (placeholder; binding added with the CUDA library)."""
+"""xSYMV / xHEMV on NVIDIA GB300: y := alpha*A*x + beta*y for a symmetric or
+Hermitian A of which only one triangle is stored and read.
+
+A thin ctypes binding over the C ABI of ``include/xsymv.h`` (libxsymv.so,
+built in-tree by ``_build.build()``).  The functions keep the C names and
+argument order; they only marshal arguments: device pointers may be given as
+integers or as CUDA tensors (anything with ``data_ptr()``), scalars as Python
+numbers (complex for c/z, a (hi, lo) pair for w).  Every computation runs in
+the library's CUDA kernels; there is no CPU path.  Each call is enqueued on
+``stream`` (default: torch's current CUDA stream when torch is loaded, else
+the legacy default stream).
+
+Status codes are returned as ints (0 = success); ``check()`` turns a
+non-zero status into an ``XsymvError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import sys
+import threading
+
+from . import _build
+
+__all__ = [
+    "xsymv_s", "xsymv_d", "xhemv_c", "xhemv_z", "xsymv_w", "symv",
+    "xsymv_set_stream", "xsymv_get_stream", "xsymv_status_string", "xsymv_last_cuda_error",
+    "xsymv_timing_enable", "xsymv_timing_read", "xsymv_launch_count",
+    "xsymv_variant_count", "xsymv_variant_name", "xsymv_set_variant", "xsymv_selected_variant",
+    "xsymv_workspace_bytes", "XsymvError", "check", "load", "library_path", "ENTRY_POINTS",
+]
+
+ENTRY_POINTS = {"s": "xsymv_s", "d": "xsymv_d", "c": "xhemv_c", "z": "xhemv_z", "w": "xsymv_w"}
+
+
+class C32(ctypes.Structure):
+    _fields_ = [("re", ctypes.c_float), ("im", ctypes.c_float)]
+
+
+class C64(ctypes.Structure):
+    _fields_ = [("re", ctypes.c_double), ("im", ctypes.c_double)]
+
+
+class DD(ctypes.Structure):
+    _fields_ = [("hi", ctypes.c_double), ("lo", ctypes.c_double)]
+
+
+class XsymvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("xsymv status %d: %s" % (status, message))
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBPATH
+
+
+def load():
+    """The loaded libxsymv.so.  Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIBPATH
+        if not os.path.exists(path):
+            raise RuntimeError("libxsymv.so is not built (run __graft_entry__.build() or "
+                               "python -m symmetric_matrix_vector_gb300._build)")
+        lib = ctypes.CDLL(path)
+        c_char, c_int, vp = ctypes.c_char, ctypes.c_int, ctypes.c_void_p
+        scal = {"s": ctypes.c_float, "d": ctypes.c_double, "c": C32, "z": C64, "w": DD}
+        for k, name in ENTRY_POINTS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = [c_char, c_int, scal[k], vp, c_int, vp, c_int, scal[k], vp, c_int]
+            fn.restype = c_int
+        lib.xsymv_set_stream.argtypes = [vp]
+        lib.xsymv_set_stream.restype = c_int
+        lib.xsymv_get_stream.restype = vp
+        lib.xsymv_status_string.argtypes = [c_int]
+        lib.xsymv_status_string.restype = ctypes.c_char_p
+        lib.xsymv_last_cuda_error.restype = c_int
+        lib.xsymv_timing_enable.argtypes = [c_int]
+        lib.xsymv_timing_enable.restype = c_int
+        lib.xsymv_timing_read.argtypes = [ctypes.POINTER(c_int), ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_double)]
+        lib.xsymv_timing_read.restype = c_int
+        lib.xsymv_launch_count.restype = ctypes.c_longlong
+        lib.xsymv_variant_count.argtypes = [c_char]
+        lib.xsymv_variant_count.restype = c_int
+        lib.xsymv_variant_name.argtypes = [c_char, c_int]
+        lib.xsymv_variant_name.restype = ctypes.c_char_p
+        lib.xsymv_set_variant.argtypes = [c_char, c_int]
+        lib.xsymv_set_variant.restype = c_int
+        lib.xsymv_selected_variant.argtypes = [c_char, c_char, c_int]
+        lib.xsymv_selected_variant.restype = c_int
+        lib.xsymv_workspace_bytes.argtypes = [c_char, c_char, c_int]
+        lib.xsymv_workspace_bytes.restype = ctypes.c_longlong
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------- marshalling --
+
+def _ptr(a) -> int:
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        if hasattr(a, "is_cuda") and not a.is_cuda:
+            raise ValueError("xsymv needs device memory; got a CPU tensor")
+        return a.data_ptr()
+    raise TypeError("expected a device pointer (int) or a CUDA tensor, got %r" % type(a))
+
+
+def _scalar(kind: str, v):
+    if kind == "s":
+        return ctypes.c_float(float(v))
+    if kind == "d":
+        return ctypes.c_double(float(v))
+    if kind == "c":
+        v = complex(v)
+        return C32(v.real, v.imag)
+    if kind == "z":
+        v = complex(v)
+        return C64(v.real, v.imag)
+    if isinstance(v, (tuple, list)):
+        return DD(float(v[0]), float(v[1]))
+    return DD(float(v), 0.0)
+
+
+def _uplo(u) -> bytes:
+    if isinstance(u, bytes):
+        return u
+    return str(u).encode()[:1] or b"?"
+
+
+def _torch_stream():
+    torch = sys.modules.get("torch")
+    if torch is None or not torch.cuda.is_available():
+        return None
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _call(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream):
+    lib = load()
+    s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
+                                                getattr(stream, "cuda_stream", stream))
+    lib.xsymv_set_stream(ctypes.c_void_p(s or 0))
+    fn = getattr(lib, ENTRY_POINTS[kind])
+    return fn(_uplo(uplo), int(n), _scalar(kind, alpha), ctypes.c_void_p(_ptr(A)), int(lda),
+              ctypes.c_void_p(_ptr(x)), int(incx), _scalar(kind, beta), ctypes.c_void_p(_ptr(y)),
+              int(incy))
+
+
+def xsymv_s(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("s", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xsymv_d(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("d", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xhemv_c(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("c", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xhemv_z(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("z", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xsymv_w(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("w", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def symv(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    """Dispatch on kind ('s', 'd', 'c', 'z', 'w') to the matching entry point."""
+    return _call(kind.lower(), uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xsymv_set_stream(stream) -> int:
+    return load().xsymv_set_stream(ctypes.c_void_p(int(stream or 0)))
+
+
+def xsymv_get_stream() -> int:
+    return load().xsymv_get_stream() or 0
+
+
+def xsymv_status_string(status: int) -> str:
+    return load().xsymv_status_string(int(status)).decode()
+
+
+def xsymv_last_cuda_error() -> int:
+    return load().xsymv_last_cuda_error()
+
+
+def check(status: int) -> None:
+    if status != 0:
+        raise XsymvError(status, xsymv_status_string(status))
+
+
+def xsymv_timing_enable(on: bool) -> int:
+    return load().xsymv_timing_enable(1 if on else 0)
+
+
+def xsymv_timing_read():
+    """(calls, main-kernel ms summed, whole-call ms summed); clears the record."""
+    calls, m, c = ctypes.c_int(0), ctypes.c_double(0), ctypes.c_double(0)
+    st = load().xsymv_timing_read(ctypes.byref(calls), ctypes.byref(m), ctypes.byref(c))
+    check(st)
+    return calls.value, m.value, c.value
+
+
+def xsymv_launch_count() -> int:
+    return load().xsymv_launch_count()
+
+
+def xsymv_variant_count(kind: str) -> int:
+    return load().xsymv_variant_count(kind.encode())
+
+
+def xsymv_variant_name(kind: str, index: int):
+    r = load().xsymv_variant_name(kind.encode(), int(index))
+    return r.decode() if r else None
+
+
+def xsymv_set_variant(kind: str, index: int) -> int:
+    return load().xsymv_set_variant(kind.encode(), int(index))
+
+
+def xsymv_selected_variant(kind: str, uplo: str, n: int) -> int:
+    return load().xsymv_selected_variant(kind.encode(), _uplo(uplo), int(n))
+
+
+def xsymv_workspace_bytes(kind: str, uplo: str, n: int) -> int:
+    return load().xsymv_workspace_bytes(kind.encode(), _uplo(uplo), int(n))

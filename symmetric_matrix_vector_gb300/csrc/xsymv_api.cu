@@ -1,0 +1,300 @@
+// Host runtime of the xsymv library: stream selection, workspace cache,
+// launch counter, event timing, status strings and variant overrides.
+// The five compute entry points live in xsymv_{s,d,c,z,w}.cu.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/xsymv.h"
+#include "xsymv_runtime.h"
+
+namespace xsymv {
+
+namespace {
+
+std::atomic<cudaStream_t> g_stream{nullptr};
+std::atomic<long long> g_launches{0};
+std::atomic<int> g_last_error{0};
+
+std::mutex g_mu;
+
+struct WsEntry {
+  int device;
+  cudaStream_t stream;
+  void* ptr;
+  size_t bytes;
+};
+std::vector<WsEntry> g_ws;
+
+struct DevInfo {
+  int device;
+  int sms;
+};
+std::vector<DevInfo> g_dev;
+
+struct TimedCall {
+  cudaEvent_t ev[3];
+};
+bool g_timing = false;
+std::vector<TimedCall> g_timed;      // calls recorded since the last read
+TimedCall g_cur{};                   // call being recorded
+std::vector<cudaEvent_t> g_free_ev;  // event pool
+
+int g_forced[5] = {-1, -1, -1, -1, -1};
+
+int kind_index(char k) {
+  switch (k) {
+    case 's': case 'S': return 0;
+    case 'd': case 'D': return 1;
+    case 'c': case 'C': return 2;
+    case 'z': case 'Z': return 3;
+    case 'w': case 'W': return 4;
+  }
+  return -1;
+}
+
+cudaEvent_t take_event() {
+  if (!g_free_ev.empty()) {
+    cudaEvent_t e = g_free_ev.back();
+    g_free_ev.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+cudaStream_t current_stream() { return g_stream.load(); }
+
+void record_cuda_error(cudaError_t e) {
+  if (e != cudaSuccess) g_last_error.store((int)e);
+}
+
+bool current_device(int* dev, int* sm_count) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const DevInfo& di : g_dev)
+    if (di.device == d) {
+      *dev = d;
+      *sm_count = di.sms;
+      return true;
+    }
+  int major = 0, minor = 0, sms = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d)) != cudaSuccess) {
+    record_cuda_error(e);
+    return false;
+  }
+  if (major != 10 || minor != 3) return false;  // built for sm_103a only
+  g_dev.push_back(DevInfo{d, sms});
+  *dev = d;
+  *sm_count = sms;
+  return true;
+}
+
+void* workspace(size_t bytes, cudaStream_t stream, int* status) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    *status = XSYMV_ERR_CUDA;
+    return nullptr;
+  }
+  if (bytes == 0) bytes = 256;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (WsEntry& w : g_ws) {
+    if (w.device != d || w.stream != stream) continue;
+    if (w.bytes >= bytes) return w.ptr;
+    // grow: the old buffer may still be in use by work queued on `stream`
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      *status = XSYMV_ERR_CUDA;
+      return nullptr;
+    }
+    size_t want = bytes + bytes / 8;
+    e = cudaMalloc(&w.ptr, want);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      cudaGetLastError();
+      w.ptr = nullptr;
+      *status = XSYMV_ERR_ALLOC;
+      return nullptr;
+    }
+    w.bytes = want;
+    return w.ptr;
+  }
+  void* p = nullptr;
+  e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    cudaGetLastError();
+    *status = XSYMV_ERR_ALLOC;
+    return nullptr;
+  }
+  g_ws.push_back(WsEntry{d, stream, p, bytes});
+  return p;
+}
+
+void note_launches(int k) { g_launches.fetch_add(k); }
+
+void timing_begin(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_timing) return;
+  for (int i = 0; i < 3; ++i) g_cur.ev[i] = take_event();
+  if (g_cur.ev[0]) cudaEventRecord(g_cur.ev[0], s);
+}
+void timing_mid(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_timing && g_cur.ev[1]) cudaEventRecord(g_cur.ev[1], s);
+}
+void timing_end(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_timing) return;
+  if (g_cur.ev[2]) cudaEventRecord(g_cur.ev[2], s);
+  if (g_cur.ev[0] && g_cur.ev[1] && g_cur.ev[2]) {
+    g_timed.push_back(g_cur);
+  } else {
+    for (int i = 0; i < 3; ++i)
+      if (g_cur.ev[i]) g_free_ev.push_back(g_cur.ev[i]);
+  }
+  g_cur = TimedCall{};
+}
+
+int forced_variant(char kind) {
+  int k = kind_index(kind);
+  return k < 0 ? -1 : g_forced[k];
+}
+
+}  // namespace xsymv
+
+using namespace xsymv;
+
+extern "C" {
+
+XSYMV_API int xsymv_set_stream(void* stream) {
+  g_stream.store(reinterpret_cast<cudaStream_t>(stream));
+  return XSYMV_OK;
+}
+
+XSYMV_API void* xsymv_get_stream(void) { return reinterpret_cast<void*>(g_stream.load()); }
+
+XSYMV_API const char* xsymv_status_string(int status) {
+  switch (status) {
+    case 0: return "success";
+    case 1: return "invalid argument 1 (uplo): must be 'U', 'u', 'L' or 'l'";
+    case 2: return "invalid argument 2 (n): must be >= 0";
+    case 5: return "invalid argument 5 (lda): must be >= max(1, n)";
+    case 7: return "invalid argument 7 (incx): must be non-zero";
+    case 10: return "invalid argument 10 (incy): must be non-zero";
+    case XSYMV_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case XSYMV_ERR_ALLOC: return "workspace allocation failed";
+    case XSYMV_ERR_DEVICE: return "no usable device (compute capability 10.3 required)";
+    case XSYMV_ERR_VALUE: return "invalid value";
+  }
+  return "unknown status";
+}
+
+XSYMV_API int xsymv_last_cuda_error(void) { return g_last_error.load(); }
+
+XSYMV_API int xsymv_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing = on != 0;
+  if (!g_timing) {
+    for (TimedCall& t : g_timed)
+      for (int i = 0; i < 3; ++i) g_free_ev.push_back(t.ev[i]);
+    g_timed.clear();
+  }
+  return XSYMV_OK;
+}
+
+XSYMV_API int xsymv_timing_read(int* calls, double* main_ms, double* call_ms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  double m = 0.0, c = 0.0;
+  int status = XSYMV_OK;
+  for (TimedCall& t : g_timed) {
+    cudaError_t e = cudaEventSynchronize(t.ev[2]);
+    float a = 0.f, b = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&a, t.ev[0], t.ev[1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&b, t.ev[0], t.ev[2]);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      status = XSYMV_ERR_CUDA;
+    }
+    m += a;
+    c += b;
+  }
+  if (calls) *calls = (int)g_timed.size();
+  if (main_ms) *main_ms = m;
+  if (call_ms) *call_ms = c;
+  for (TimedCall& t : g_timed)
+    for (int i = 0; i < 3; ++i) g_free_ev.push_back(t.ev[i]);
+  g_timed.clear();
+  return status;
+}
+
+XSYMV_API long long xsymv_launch_count(void) { return g_launches.load(); }
+
+XSYMV_API int xsymv_variant_count(char kind) {
+  switch (kind_index(kind)) {
+    case 0: return variant_count_s();
+    case 1: return variant_count_d();
+    case 2: return variant_count_c();
+    case 3: return variant_count_z();
+    case 4: return variant_count_w();
+  }
+  return 0;
+}
+
+XSYMV_API const char* xsymv_variant_name(char kind, int index) {
+  switch (kind_index(kind)) {
+    case 0: return variant_name_s(index);
+    case 1: return variant_name_d(index);
+    case 2: return variant_name_c(index);
+    case 3: return variant_name_z(index);
+    case 4: return variant_name_w(index);
+  }
+  return nullptr;
+}
+
+XSYMV_API int xsymv_selected_variant(char kind, char uplo, int n) {
+  switch (kind_index(kind)) {
+    case 0: return selected_variant_s(uplo, n);
+    case 1: return selected_variant_d(uplo, n);
+    case 2: return selected_variant_c(uplo, n);
+    case 3: return selected_variant_z(uplo, n);
+    case 4: return selected_variant_w(uplo, n);
+  }
+  return XSYMV_ERR_VALUE;
+}
+
+XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n) {
+  switch (kind_index(kind)) {
+    case 0: return workspace_bytes_s(uplo, n);
+    case 1: return workspace_bytes_d(uplo, n);
+    case 2: return workspace_bytes_c(uplo, n);
+    case 3: return workspace_bytes_z(uplo, n);
+    case 4: return workspace_bytes_w(uplo, n);
+  }
+  return XSYMV_ERR_VALUE;
+}
+
+XSYMV_API int xsymv_set_variant(char kind, int index) {
+  int k = kind_index(kind);
+  if (k < 0 || index < -1 || index >= xsymv_variant_count(kind)) return XSYMV_ERR_VALUE;
+  g_forced[k] = index;
+  return XSYMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,25 @@
+// Entry point xhemv_c of the xsymv C ABI and its compiled kernel variants.
+#include "xsymv_entry.cuh"
+
+namespace xsymv {
+static const Variant<c32> kVariants_c[] = {
+    XSYMV_VARIANT(c32, 2, 4, 8),
+    XSYMV_VARIANT(c32, 1, 8, 8),
+};
+static_assert(sizeof(c32) == sizeof(xsymv_c32), "C-ABI type layout");
+}  // namespace xsymv
+
+XSYMV_DEFINE_INTROSPECTION(c, xsymv::c32, kVariants_c)
+
+extern "C" XSYMV_API int xhemv_c(char uplo, int n, xsymv_c32 alpha, const xsymv_c32* A, int lda, const xsymv_c32* x,
+                                int incx, xsymv_c32 beta, xsymv_c32* y, int incy) {
+  using T = xsymv::c32;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_entry<T>(xsymv::kVariants_c,
+                              (int)(sizeof(xsymv::kVariants_c) / sizeof(xsymv::kVariants_c[0])),
+                              'c', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                              reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                              incy);
+}

@@ -1,0 +1,26 @@
+// Entry point xsymv_d of the xsymv C ABI and its compiled kernel variants.
+#include "xsymv_entry.cuh"
+
+namespace xsymv {
+static const Variant<double> kVariants_d[] = {
+    XSYMV_VARIANT(double, 2, 4, 8),
+    XSYMV_VARIANT(double, 1, 8, 8),
+    XSYMV_VARIANT(double, 2, 8, 4),
+};
+static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");
+}  // namespace xsymv
+
+XSYMV_DEFINE_INTROSPECTION(d, double, kVariants_d)
+
+extern "C" XSYMV_API int xsymv_d(char uplo, int n, double alpha, const double* A, int lda, const double* x,
+                                int incx, double beta, double* y, int incy) {
+  using T = double;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_entry<T>(xsymv::kVariants_d,
+                              (int)(sizeof(xsymv::kVariants_d) / sizeof(xsymv::kVariants_d[0])),
+                              'd', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                              reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                              incy);
+}

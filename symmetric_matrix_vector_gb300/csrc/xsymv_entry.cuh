@@ -1,0 +1,196 @@
+// Host dispatch shared by the five entry points: BLAS argument checks, quick
+// returns, variant choice, work partition, workspace and the two launches.
+#pragma once
+
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/xsymv.h"
+#include "xsymv_kernels.cuh"
+#include "xsymv_runtime.h"
+#include "xsymv_tuned.h"
+
+namespace xsymv {
+
+// One compiled configuration of the main kernel.
+template <class T>
+struct Variant {
+  const char* name;
+  int NB;     // tile edge = 32 lanes * elements per 16 bytes * VR
+  int warps;  // warps per block
+  cudaError_t (*launch)(const Plan&, const T*, long long, const T*, long long, T*, T*, bool,
+                        cudaStream_t);
+  int (*ctas_per_sm)();
+};
+
+template <class T, int VR, int U, int WARPS>
+cudaError_t launch_main(const Plan& p, const T* A, long long lda, const T* x, long long incx,
+                        T* Wc, T* Wr, bool aligned, cudaStream_t st) {
+  const unsigned grid = (unsigned)((p.W + WARPS - 1) / WARPS);
+  if (aligned)
+    symv_main<T, VR, U, WARPS, true><<<grid, WARPS * 32, 0, st>>>(p, A, lda, x, incx, Wc, Wr);
+  else
+    symv_main<T, VR, U, WARPS, false><<<grid, WARPS * 32, 0, st>>>(p, A, lda, x, incx, Wc, Wr);
+  return cudaGetLastError();
+}
+
+template <class T, int VR, int U, int WARPS>
+int ctas_per_sm() {
+  static int cached = 0;
+  if (!cached) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, WARPS, true>,
+                                                      WARPS * 32, 0) != cudaSuccess || b < 1) {
+      cudaGetLastError();
+      b = 1;
+    }
+    cached = b;
+  }
+  return cached;
+}
+
+#define XSYMV_VARIANT(T, VR, U, W)                                                      \
+  Variant<T> {                                                                          \
+    "vr" #VR "_u" #U "_w" #W, 32 * Ops<T>::VPL * (VR), (W), &launch_main<T, VR, U, W>, \
+        &ctas_per_sm<T, VR, U, W>                                                       \
+  }
+
+// ---------------------------------------------------------------- checks --
+inline int check_args(char uplo, int n, int lda, int incx, int incy) {
+  if (uplo != 'U' && uplo != 'u' && uplo != 'L' && uplo != 'l') return 1;
+  if (n < 0) return 2;
+  if (lda < (n > 1 ? n : 1)) return 5;
+  if (incx == 0) return 7;
+  if (incy == 0) return 10;
+  return 0;
+}
+
+inline bool is_zero(float a) { return a == 0.f; }
+inline bool is_zero(double a) { return a == 0.0; }
+inline bool is_zero(c32 a) { return a.re == 0.f && a.im == 0.f; }
+inline bool is_zero(c64 a) { return a.re == 0.0 && a.im == 0.0; }
+inline bool is_zero(dd a) { return a.hi == 0.0 && a.lo == 0.0; }
+inline bool is_one(float a) { return a == 1.f; }
+inline bool is_one(double a) { return a == 1.0; }
+inline bool is_one(c32 a) { return a.re == 1.f && a.im == 0.f; }
+inline bool is_one(c64 a) { return a.re == 1.0 && a.im == 0.0; }
+inline bool is_one(dd a) { return a.hi == 1.0 && a.lo == 0.0; }
+
+inline long long align_up(long long v, long long a) { return (v + a - 1) / a * a; }
+
+template <class T>
+struct Workload {
+  Plan plan;
+  const Variant<T>* variant;
+  long long wc_bytes;   // offset of Wr inside the workspace
+  long long bytes;      // total workspace bytes
+};
+
+template <class T>
+int pick_variant(const Variant<T>* table, int count, char kind, int upper, int n) {
+  int f = forced_variant(kind);
+  if (f >= 0 && f < count) return f;
+  int t = tuned_variant(kind, upper, n);
+  return (t >= 0 && t < count) ? t : 0;
+}
+
+template <class T>
+int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, Workload<T>* out) {
+  int dev = 0, sms = 0;
+  if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
+  const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n)];
+  const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps;
+  out->plan = plan_make(n, v->NB, upper, wmax);
+  out->variant = v;
+  out->wc_bytes = align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
+  out->bytes = out->wc_bytes + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
+  return XSYMV_OK;
+}
+
+// -------------------------------------------------------------- the call --
+template <class T>
+int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, T alpha,
+               const T* A, int lda, const T* x, int incx, T beta, T* y, int incy) {
+  int info = check_args(uplo, n, lda, incx, incy);
+  if (info) return info;
+  if (n == 0) return XSYMV_OK;
+  const bool az = is_zero(alpha), bz = is_zero(beta);
+  if (az && is_one(beta)) return XSYMV_OK;
+
+  const int upper = (uplo == 'U' || uplo == 'u');
+  cudaStream_t st = current_stream();
+  // pointers to logical element 0 (BLAS: negative strides start at the end)
+  T* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
+  const T* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
+  const unsigned fgrid = (unsigned)((n + 255) / 256);
+
+  if (az) {  // y := beta*y: neither A nor x is read
+    int dev = 0, sms = 0;
+    if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
+    Plan p = plan_make(n, 32, upper, 1);
+    timing_begin(st);
+    timing_mid(st);
+    symv_finalize<T><<<fgrid, 256, 0, st>>>(p, nullptr, nullptr, alpha, beta,
+                                             bz ? kZero : kAlphaZero, y0, incy);
+    cudaError_t e = cudaGetLastError();
+    timing_end(st);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+    return XSYMV_OK;
+  }
+
+  Workload<T> wl;
+  int status = plan_call(table, count, kind, upper, n, &wl);
+  if (status) return status;
+  char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status));
+  if (!ws) return status;
+  T* Wc = reinterpret_cast<T*>(ws);
+  T* Wr = reinterpret_cast<T*>(ws + wl.wc_bytes);
+
+  const bool aligned = (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
+                       (((long long)lda * (long long)sizeof(T)) % 16 == 0);
+  timing_begin(st);
+  cudaError_t e = wl.variant->launch(wl.plan, A, lda, x0, incx, Wc, Wr, aligned, st);
+  if (e == cudaSuccess) {
+    timing_mid(st);
+    symv_finalize<T><<<fgrid, 256, 0, st>>>(wl.plan, Wc, Wr, alpha, beta, bz ? kBetaZero : kFull,
+                                             y0, incy);
+    e = cudaGetLastError();
+  }
+  timing_end(st);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_launches(2);
+  return XSYMV_OK;
+}
+
+template <class T>
+long long workspace_bytes(const Variant<T>* table, int count, char kind, char uplo, int n) {
+  if (check_args(uplo, n, n > 1 ? n : 1, 1, 1)) return XSYMV_ERR_VALUE;
+  if (n == 0) return 0;
+  Workload<T> wl;
+  int status = plan_call(table, count, kind, uplo == 'U' || uplo == 'u', n, &wl);
+  return status ? status : wl.bytes;
+}
+
+}  // namespace xsymv
+
+// Per-kind tables and introspection functions (defined in each xsymv_<k>.cu).
+#define XSYMV_DEFINE_INTROSPECTION(KIND, T, TABLE)                                          \
+  namespace xsymv {                                                                         \
+  int variant_count_##KIND() { return (int)(sizeof(TABLE) / sizeof(TABLE[0])); }            \
+  const char* variant_name_##KIND(int i) {                                                  \
+    return (i >= 0 && i < variant_count_##KIND()) ? TABLE[i].name : nullptr;                \
+  }                                                                                         \
+  int selected_variant_##KIND(char uplo, int n) {                                           \
+    return pick_variant<T>(TABLE, variant_count_##KIND(), #KIND[0], uplo == 'U' || uplo == 'u', n); \
+  }                                                                                         \
+  long long workspace_bytes_##KIND(char uplo, int n) {                                      \
+    return workspace_bytes<T>(TABLE, variant_count_##KIND(), #KIND[0], uplo, n);            \
+  }                                                                                         \
+  }

@@ -1,0 +1,46 @@
+// Host-side services shared by the five entry points: stream, device
+// properties, per-(device, stream) workspace, launch counting, event timing
+// and variant overrides.  Implemented in xsymv_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace xsymv {
+
+cudaStream_t current_stream();
+
+// current device and its multiprocessor count; false if there is no usable
+// device (records the CUDA error)
+bool current_device(int* dev, int* sm_count);
+
+// workspace of at least `bytes` for (current device, stream); nullptr and
+// *status set on failure
+void* workspace(size_t bytes, cudaStream_t stream, int* status);
+
+void note_launches(int k);
+void record_cuda_error(cudaError_t e);
+
+// event timing around one call: begin() before the main kernel, mid() after
+// it, end() after the last kernel.  Does nothing unless timing is enabled.
+void timing_begin(cudaStream_t s);
+void timing_mid(cudaStream_t s);
+void timing_end(cudaStream_t s);
+
+// -1 unless a variant was forced for this kind
+int forced_variant(char kind);
+
+// per-kind introspection, defined next to each kind's variant table
+#define XSYMV_DECLARE_INTROSPECTION(KIND)            \
+  int variant_count_##KIND();                        \
+  const char* variant_name_##KIND(int i);            \
+  int selected_variant_##KIND(char uplo, int n);     \
+  long long workspace_bytes_##KIND(char uplo, int n);
+XSYMV_DECLARE_INTROSPECTION(s)
+XSYMV_DECLARE_INTROSPECTION(d)
+XSYMV_DECLARE_INTROSPECTION(c)
+XSYMV_DECLARE_INTROSPECTION(z)
+XSYMV_DECLARE_INTROSPECTION(w)
+#undef XSYMV_DECLARE_INTROSPECTION
+
+}  // namespace xsymv

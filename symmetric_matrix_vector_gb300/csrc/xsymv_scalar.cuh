@@ -1,0 +1,229 @@
+// Scalar types of the five xSYMV / xHEMV variants and the few operations the
+// kernels need on them: zero, add, the two multiply-adds of a stored element
+// (row term A(i,j)*x(j) and column term conj(A(i,j))*x(i)), warp shuffles and
+// 16-byte streaming loads.
+//
+// Types (as listed in §2.2 and figure "x-symv API" of "CUDA-xSYMV の実装と
+// 評価", IPSJ 2014-HPC-146): float, double, single and double complex
+// (float2 / double2 layout) and double-double (a double2 holding hi + lo).
+//
+// Double-double follows Hida, Li and Bailey's quad-double paper (the report's
+// reference for its DD format): TwoSum, QuickTwoSum, TwoProd through FMA, and
+// the accurate ("IEEE") addition.  Every DD step uses the explicitly rounded
+// intrinsics so the compiler can neither contract nor reassociate it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace xsymv {
+
+struct c32 { float re, im; };
+struct c64 { double re, im; };
+struct dd { double hi, lo; };
+
+// ---------------------------------------------------------------- DD core --
+__device__ __forceinline__ void two_sum(double a, double b, double& s, double& e) {
+  s = __dadd_rn(a, b);
+  double bb = __dsub_rn(s, a);
+  e = __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb));
+}
+__device__ __forceinline__ void quick_two_sum(double a, double b, double& s, double& e) {
+  s = __dadd_rn(a, b);
+  e = __dsub_rn(b, __dsub_rn(s, a));
+}
+__device__ __forceinline__ dd dd_add(dd a, dd b) {
+  double s1, s2, t1, t2;
+  two_sum(a.hi, b.hi, s1, s2);
+  two_sum(a.lo, b.lo, t1, t2);
+  s2 = __dadd_rn(s2, t1);
+  quick_two_sum(s1, s2, s1, s2);
+  s2 = __dadd_rn(s2, t2);
+  quick_two_sum(s1, s2, s1, s2);
+  return dd{s1, s2};
+}
+__device__ __forceinline__ dd dd_mul(dd a, dd b) {
+  double p = __dmul_rn(a.hi, b.hi);
+  double e = __fma_rn(a.hi, b.hi, -p);
+  e = __fma_rn(a.hi, b.lo, e);
+  e = __fma_rn(a.lo, b.hi, e);
+  double s, t;
+  quick_two_sum(p, e, s, t);
+  return dd{s, t};
+}
+__device__ __forceinline__ dd dd_renorm(dd a) {
+  dd r;
+  quick_two_sum(a.hi, a.lo, r.hi, r.lo);
+  return r;
+}
+
+// --------------------------------------------------------------- traits ----
+// VPL: elements per 16-byte vector load.  HERM: complex Hermitian variant.
+template <class T> struct Ops;
+
+template <> struct Ops<float> {
+  static constexpr int VPL = 4;
+  static constexpr bool HERM = false;
+  __device__ __forceinline__ static float zero() { return 0.f; }
+  __device__ __forceinline__ static float add(float a, float b) { return a + b; }
+  __device__ __forceinline__ static float mul(float a, float b) { return a * b; }
+  // acc + a*b and acc + conj(a)*b
+  __device__ __forceinline__ static float madd(float acc, float a, float b) { return fmaf(a, b, acc); }
+  __device__ __forceinline__ static float maddc(float acc, float a, float b) { return fmaf(a, b, acc); }
+  __device__ __forceinline__ static float diag(float a) { return a; }
+  __device__ __forceinline__ static float load(const float* p) { return __ldg(p); }
+  __device__ __forceinline__ static float shfl_xor(float v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+  __device__ __forceinline__ static float shfl(float v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+};
+
+template <> struct Ops<double> {
+  static constexpr int VPL = 2;
+  static constexpr bool HERM = false;
+  __device__ __forceinline__ static double zero() { return 0.0; }
+  __device__ __forceinline__ static double add(double a, double b) { return a + b; }
+  __device__ __forceinline__ static double mul(double a, double b) { return a * b; }
+  __device__ __forceinline__ static double madd(double acc, double a, double b) { return fma(a, b, acc); }
+  __device__ __forceinline__ static double maddc(double acc, double a, double b) { return fma(a, b, acc); }
+  __device__ __forceinline__ static double diag(double a) { return a; }
+  __device__ __forceinline__ static double load(const double* p) { return __ldg(p); }
+  __device__ __forceinline__ static double shfl_xor(double v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+  __device__ __forceinline__ static double shfl(double v, int src) { return __shfl_sync(0xffffffffu, v, src); }
+};
+
+template <> struct Ops<c32> {
+  static constexpr int VPL = 2;
+  static constexpr bool HERM = true;
+  __device__ __forceinline__ static c32 zero() { return c32{0.f, 0.f}; }
+  __device__ __forceinline__ static c32 add(c32 a, c32 b) { return c32{a.re + b.re, a.im + b.im}; }
+  __device__ __forceinline__ static c32 mul(c32 a, c32 b) {
+    return c32{a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
+  }
+  __device__ __forceinline__ static c32 madd(c32 acc, c32 a, c32 b) {
+    acc.re = fmaf(a.re, b.re, acc.re);
+    acc.re = fmaf(-a.im, b.im, acc.re);
+    acc.im = fmaf(a.re, b.im, acc.im);
+    acc.im = fmaf(a.im, b.re, acc.im);
+    return acc;
+  }
+  __device__ __forceinline__ static c32 maddc(c32 acc, c32 a, c32 b) {
+    acc.re = fmaf(a.re, b.re, acc.re);
+    acc.re = fmaf(a.im, b.im, acc.re);
+    acc.im = fmaf(a.re, b.im, acc.im);
+    acc.im = fmaf(-a.im, b.re, acc.im);
+    return acc;
+  }
+  // the imaginary part of a Hermitian diagonal is never referenced
+  __device__ __forceinline__ static c32 diag(c32 a) { return c32{a.re, 0.f}; }
+  // element loads need only the alignment of the component type
+  __device__ __forceinline__ static c32 load(const c32* p) {
+    const float* f = reinterpret_cast<const float*>(p);
+    return c32{__ldg(f), __ldg(f + 1)};
+  }
+  __device__ __forceinline__ static c32 shfl_xor(c32 v, int m) {
+    return c32{__shfl_xor_sync(0xffffffffu, v.re, m), __shfl_xor_sync(0xffffffffu, v.im, m)};
+  }
+  __device__ __forceinline__ static c32 shfl(c32 v, int s) {
+    return c32{__shfl_sync(0xffffffffu, v.re, s), __shfl_sync(0xffffffffu, v.im, s)};
+  }
+};
+
+template <> struct Ops<c64> {
+  static constexpr int VPL = 1;
+  static constexpr bool HERM = true;
+  __device__ __forceinline__ static c64 zero() { return c64{0.0, 0.0}; }
+  __device__ __forceinline__ static c64 add(c64 a, c64 b) { return c64{a.re + b.re, a.im + b.im}; }
+  __device__ __forceinline__ static c64 mul(c64 a, c64 b) {
+    return c64{a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
+  }
+  __device__ __forceinline__ static c64 madd(c64 acc, c64 a, c64 b) {
+    acc.re = fma(a.re, b.re, acc.re);
+    acc.re = fma(-a.im, b.im, acc.re);
+    acc.im = fma(a.re, b.im, acc.im);
+    acc.im = fma(a.im, b.re, acc.im);
+    return acc;
+  }
+  __device__ __forceinline__ static c64 maddc(c64 acc, c64 a, c64 b) {
+    acc.re = fma(a.re, b.re, acc.re);
+    acc.re = fma(a.im, b.im, acc.re);
+    acc.im = fma(a.re, b.im, acc.im);
+    acc.im = fma(-a.im, b.re, acc.im);
+    return acc;
+  }
+  __device__ __forceinline__ static c64 diag(c64 a) { return c64{a.re, 0.0}; }
+  __device__ __forceinline__ static c64 load(const c64* p) {
+    const double* f = reinterpret_cast<const double*>(p);
+    return c64{__ldg(f), __ldg(f + 1)};
+  }
+  __device__ __forceinline__ static c64 shfl_xor(c64 v, int m) {
+    return c64{__shfl_xor_sync(0xffffffffu, v.re, m), __shfl_xor_sync(0xffffffffu, v.im, m)};
+  }
+  __device__ __forceinline__ static c64 shfl(c64 v, int s) {
+    return c64{__shfl_sync(0xffffffffu, v.re, s), __shfl_sync(0xffffffffu, v.im, s)};
+  }
+};
+
+template <> struct Ops<dd> {
+  static constexpr int VPL = 1;
+  static constexpr bool HERM = false;
+  __device__ __forceinline__ static dd zero() { return dd{0.0, 0.0}; }
+  __device__ __forceinline__ static dd add(dd a, dd b) { return dd_add(a, b); }
+  __device__ __forceinline__ static dd mul(dd a, dd b) { return dd_mul(a, b); }
+  __device__ __forceinline__ static dd madd(dd acc, dd a, dd b) { return dd_add(acc, dd_mul(a, b)); }
+  __device__ __forceinline__ static dd maddc(dd acc, dd a, dd b) { return dd_add(acc, dd_mul(a, b)); }
+  __device__ __forceinline__ static dd diag(dd a) { return a; }
+  // inputs are renormalised (QuickTwoSum) as they are read
+  __device__ __forceinline__ static dd load(const dd* p) {
+    const double* f = reinterpret_cast<const double*>(p);
+    return dd_renorm(dd{__ldg(f), __ldg(f + 1)});
+  }
+  __device__ __forceinline__ static dd shfl_xor(dd v, int m) {
+    return dd{__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
+  }
+  __device__ __forceinline__ static dd shfl(dd v, int s) {
+    return dd{__shfl_sync(0xffffffffu, v.hi, s), __shfl_sync(0xffffffffu, v.lo, s)};
+  }
+};
+
+// ------------------------------------------------ 16-byte streaming loads --
+// The stored triangle is read exactly once: bypass L1 and use the read-only
+// path.  The address must be 16-byte aligned.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// unpack one 16-byte vector into VPL elements of T
+template <class T> struct Unpack;
+template <> struct Unpack<float> {
+  __device__ __forceinline__ static void run(uint4 v, float* o) {
+    o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+  }
+};
+template <> struct Unpack<double> {
+  __device__ __forceinline__ static void run(uint4 v, double* o) {
+    o[0] = __hiloint2double((int)v.y, (int)v.x);
+    o[1] = __hiloint2double((int)v.w, (int)v.z);
+  }
+};
+template <> struct Unpack<c32> {
+  __device__ __forceinline__ static void run(uint4 v, c32* o) {
+    o[0] = c32{__uint_as_float(v.x), __uint_as_float(v.y)};
+    o[1] = c32{__uint_as_float(v.z), __uint_as_float(v.w)};
+  }
+};
+template <> struct Unpack<c64> {
+  __device__ __forceinline__ static void run(uint4 v, c64* o) {
+    o[0] = c64{__hiloint2double((int)v.y, (int)v.x), __hiloint2double((int)v.w, (int)v.z)};
+  }
+};
+template <> struct Unpack<dd> {
+  __device__ __forceinline__ static void run(uint4 v, dd* o) {
+    o[0] = dd_renorm(dd{__hiloint2double((int)v.y, (int)v.x), __hiloint2double((int)v.w, (int)v.z)});
+  }
+};
+
+}  // namespace xsymv

@@ -1,0 +1,25 @@
+// Entry point xsymv_w of the xsymv C ABI and its compiled kernel variants.
+#include "xsymv_entry.cuh"
+
+namespace xsymv {
+static const Variant<dd> kVariants_w[] = {
+    XSYMV_VARIANT(dd, 4, 2, 8),
+    XSYMV_VARIANT(dd, 2, 4, 8),
+};
+static_assert(sizeof(dd) == sizeof(xsymv_dd), "C-ABI type layout");
+}  // namespace xsymv
+
+XSYMV_DEFINE_INTROSPECTION(w, xsymv::dd, kVariants_w)
+
+extern "C" XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd* A, int lda, const xsymv_dd* x,
+                                int incx, xsymv_dd beta, xsymv_dd* y, int incy) {
+  using T = xsymv::dd;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_entry<T>(xsymv::kVariants_w,
+                              (int)(sizeof(xsymv::kVariants_w) / sizeof(xsymv::kVariants_w[0])),
+                              'w', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                              reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                              incy);
+}

@@ -1,0 +1,25 @@
+// Entry point xhemv_z of the xsymv C ABI and its compiled kernel variants.
+#include "xsymv_entry.cuh"
+
+namespace xsymv {
+static const Variant<c64> kVariants_z[] = {
+    XSYMV_VARIANT(c64, 4, 2, 8),
+    XSYMV_VARIANT(c64, 2, 4, 8),
+};
+static_assert(sizeof(c64) == sizeof(xsymv_c64), "C-ABI type layout");
+}  // namespace xsymv
+
+XSYMV_DEFINE_INTROSPECTION(z, xsymv::c64, kVariants_z)
+
+extern "C" XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_c64* A, int lda, const xsymv_c64* x,
+                                int incx, xsymv_c64 beta, xsymv_c64* y, int incy) {
+  using T = xsymv::c64;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_entry<T>(xsymv::kVariants_z,
+                              (int)(sizeof(xsymv::kVariants_z) / sizeof(xsymv::kVariants_z[0])),
+                              'z', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                              reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                              incy);
+}

@@ -1,0 +1,100 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/xsymv.h declares, and rejects bad BLAS arguments (checked on the host
+before any CUDA call) with the xerbla positions."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import symmetric_matrix_vector_gb300 as xs
+from symmetric_matrix_vector_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xsymv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return xs.load()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return re.findall(r"XSYMV_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_symbols()
+    for n in ("xsymv_s", "xsymv_d", "xhemv_c", "xhemv_z", "xsymv_w"):
+        assert n in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(xs.library_path())
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", xs.library_path()], check=True,
+                         capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.split() and l.split()[-2] in "TDBR"}
+    exported = {e for e in exported if not e.startswith("_")}
+    assert exported == set(declared_symbols()), exported ^ set(declared_symbols())
+
+
+@pytest.mark.parametrize("kind", ["s", "d", "c", "z", "w"])
+def test_argument_errors_on_host(lib, kind):
+    one = (1.0, 0.0) if kind == "w" else 1.0
+    zero = (0.0, 0.0) if kind == "w" else 0.0
+    f = getattr(xs, xs.ENTRY_POINTS[kind])
+    # pointers are never dereferenced: the checks come first
+    bogus = 0x1000
+    assert f("X", 4, one, bogus, 4, bogus, 1, zero, bogus, 1, stream=0) == 1
+    assert f("U", -1, one, bogus, 4, bogus, 1, zero, bogus, 1, stream=0) == 2
+    assert f("L", 4, one, bogus, 3, bogus, 1, zero, bogus, 1, stream=0) == 5
+    assert f("U", 4, one, bogus, 4, bogus, 0, zero, bogus, 1, stream=0) == 7
+    assert f("u", 4, one, bogus, 4, bogus, 1, zero, bogus, 0, stream=0) == 10
+    # first bad argument wins, as in xerbla
+    assert f("X", -1, one, bogus, 0, bogus, 0, zero, bogus, 0, stream=0) == 1
+    assert f("U", 5, one, bogus, 1, bogus, 0, zero, bogus, 1, stream=0) == 5
+    # quick returns touch nothing
+    assert f("U", 0, one, bogus, 1, bogus, 1, zero, bogus, 1, stream=0) == 0
+    assert f("l", 7, zero, bogus, 7, bogus, 1, one, bogus, 1, stream=0) == 0
+
+
+def test_status_strings(lib):
+    for st in (0, 1, 2, 5, 7, 10, -1, -2, -3, -4):
+        assert xs.xsymv_status_string(st) != "unknown status"
+    assert xs.xsymv_status_string(12345) == "unknown status"
+
+
+def test_variants_introspection(lib):
+    for kind in "sdczw":
+        cnt = xs.xsymv_variant_count(kind)
+        assert cnt >= 1
+        for i in range(cnt):
+            assert re.fullmatch(r"vr\d+_u\d+_w\d+", xs.xsymv_variant_name(kind, i))
+        assert xs.xsymv_variant_name(kind, cnt) is None
+        assert xs.xsymv_set_variant(kind, cnt) == -4
+        assert xs.xsymv_set_variant(kind, -1) == 0
+    assert xs.xsymv_variant_count("q") == 0
+
+
+def test_stream_round_trip(lib):
+    assert xs.xsymv_set_stream(0x1234) == 0
+    assert xs.xsymv_get_stream() == 0x1234
+    assert xs.xsymv_set_stream(0) == 0
+
+
+def test_cpu_tensor_is_refused(lib):
+    import torch
+
+    a = torch.zeros(4)
+    with pytest.raises(ValueError):
+        xs.xsymv_s("U", 2, 1.0, a, 2, a, 1, 0.0, a, 1, stream=0)

@@ -1,0 +1,270 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle,
+element by element on seeded inputs (componentwise error normalised by
+|alpha||A||x| + |beta||y|), plus bitwise run-to-run identity and the BLAS
+edge cases.  The operation is equation (1) of "CUDA-xSYMV の実装と評価"
+(IPSJ 2014-HPC-146): y := alpha*A*x + beta*y, one triangle of A stored."""
+import numpy as np
+import pytest
+
+import oracle
+from symmetric_matrix_vector_gb300 import inputs
+from tests.gpu_helpers import TOL, DeviceProblem, errors, from_device, logical, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+KINDS = ("s", "d", "c", "z", "w")
+SCAL = {
+    "s": (1.25, 0.5), "d": (-0.75, 2.0), "c": (complex(1.0, 0.5), complex(0.5, -0.25)),
+    "z": (complex(1.0, 0.5), complex(0.5, -0.25)), "w": ((1.0, 2.0 ** -60), (0.5, 0.0)),
+}
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    import symmetric_matrix_vector_gb300 as xs
+
+    assert torch.cuda.is_available()
+    xs.load()
+    for k in KINDS:
+        xs.xsymv_set_variant(k, -1)
+    yield xs
+    for k in KINDS:
+        xs.xsymv_set_variant(k, -1)
+
+
+def run_and_check(o, p, rows=None, **kw):
+    dp = DeviceProblem(p)
+    st, yd = dp.run(**kw)
+    assert st == 0, st
+    y = from_device(yd, p.y)
+    err, _ = errors(o, p, y, rows=rows, alpha=kw.get("alpha"), beta=kw.get("beta"))
+    assert np.max(err) <= TOL[p.kind], (p.kind, p.uplo, p.n, float(np.max(err)))
+    return y
+
+
+# ---------------------------------------------------------------- sizes ----
+SIZES = [1, 2, 3, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 513]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("uplo", ["U", "L"])
+def test_sizes_and_ragged_tails(o, kind, uplo):
+    al, be = SCAL[kind]
+    for n in SIZES:
+        p = inputs.make_problem(kind, uplo, n, lda=n + (n % 3), alpha=al, beta=be, seed=n)
+        run_and_check(o, p)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("uplo", ["U", "L"])
+@pytest.mark.parametrize("incx,incy", [(2, -1), (-3, 2), (-1, -1)])
+def test_strides(o, kind, uplo, incx, incy):
+    al, be = SCAL[kind]
+    for n in (45, 200):
+        p = inputs.make_problem(kind, uplo, n, lda=n + 1, alpha=al, beta=be, incx=incx,
+                                incy=incy, seed=7 + n)
+        y = run_and_check(o, p)
+        # gap elements of y are never written (they stay NaN)
+        idx = set((np.arange(n) * abs(incy)).tolist())
+        gaps = [k for k in range(len(y)) if k not in idx]
+        assert all(np.all(np.isnan(y[k])) for k in gaps)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_every_variant(o, lib, kind):
+    """each compiled kernel variant (the tuner's space) is correct"""
+    al, be = SCAL[kind]
+    try:
+        for v in range(lib.xsymv_variant_count(kind)):
+            assert lib.xsymv_set_variant(kind, v) == 0
+            for uplo in ("U", "L"):
+                for n in (97, 700):
+                    p = inputs.make_problem(kind, uplo, n, lda=n + 2, alpha=al, beta=be,
+                                            seed=100 + v)
+                    run_and_check(o, p)
+    finally:
+        lib.xsymv_set_variant(kind, -1)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_unaligned_matrix(o, kind):
+    """lda and base address off the 16-byte grid take the element-load path"""
+    import torch
+
+    al, be = SCAL[kind]
+    n = 301
+    p = inputs.make_problem(kind, "U", n, lda=n, alpha=al, beta=be, seed=3)
+    dp = DeviceProblem(p)
+    esz = p.A.itemsize * (2 if kind == "w" else 1)
+    # shift A off the 16-byte grid (by one element, or half of a 16-byte one)
+    off = esz if esz < 16 else 8
+    buf = torch.zeros(dp.A.numel() + 64, dtype=torch.uint8, device="cuda")
+    buf[off:off + dp.A.numel()] = dp.A
+    st, yd = dp.run(A=buf[off:])
+    assert st == 0
+    err, _ = errors(o, p, from_device(yd, p.y))
+    assert np.max(err) <= TOL[kind]
+
+
+# ------------------------------------------------------------ workloads ----
+@pytest.mark.parametrize("name", ["ssymv_small", "dsymv", "chemv", "zhemv", "wsymv"])
+def test_workloads_small_n(o, name):
+    """the five named workloads' recipes (uplo, lda, scalars, NaN sentinels)
+    at sizes the oracle checks row by row in seconds"""
+    n = {"ssymv_small": 1024, "dsymv": 1100, "chemv": 900, "zhemv": 700, "wsymv": 520}[name]
+    p = inputs.workload(name, n=n)
+    run_and_check(o, p)
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+def test_sweep_points_all_rows(o, n):
+    p = inputs.workload("ssymv_sweep", n=n)
+    run_and_check(o, p, rows=sample_rows(n, count=512, seed=n))
+
+
+FULL = [("ssymv_sweep", 16384), ("ssymv_sweep", 32768), ("dsymv", None), ("chemv", None),
+        ("zhemv", None), ("wsymv", None)]
+
+
+@pytest.mark.parametrize("name,n", FULL, ids=["%s_%s" % (a, b or "full") for a, b in FULL])
+def test_workloads_full_size_sampled(o, name, n):
+    """full sizes, in the benchmark's launch configuration, checked on
+    sampled rows (each recomputed by the oracle from the definition), and
+    bitwise identical across repeated calls"""
+    p = inputs.workload(name, n=n)
+    dp = DeviceProblem(p)
+    st, y1 = dp.run()
+    assert st == 0
+    y = from_device(y1, p.y)
+    assert np.all(np.isfinite(logical(p.kind, y, p.n, p.incy)))
+    rows = sample_rows(p.n, count=160, seed=p.n)
+    err, _ = errors(o, p, y, rows=rows)
+    assert np.max(err) <= TOL[p.kind], (name, float(np.max(err)))
+    for _ in range(3):
+        st, y2 = dp.run()
+        assert st == 0
+        assert bool((y1 == y2).all()), "results differ between runs"
+
+
+# --------------------------------------------------------- determinism -----
+@pytest.mark.parametrize("kind", KINDS)
+def test_bitwise_repeatable(kind):
+    """ten repeats give identical bytes, also with other work running
+    concurrently on a second stream"""
+    import torch
+
+    al, be = SCAL[kind]
+    n = {"s": 6000, "d": 4000, "c": 3000, "z": 2500, "w": 1500}[kind]
+    p = inputs.make_problem(kind, "U", n, lda=n + 8, alpha=al, beta=be, seed=21)
+    dp = DeviceProblem(p)
+    st, first = dp.run()
+    assert st == 0
+    noise_stream = torch.cuda.Stream()
+    big = torch.randn(1 << 24, device="cuda")
+    for r in range(10):
+        if r % 2:
+            with torch.cuda.stream(noise_stream):
+                for _ in range(4):
+                    big.mul_(1.0001)
+        st, again = dp.run()
+        assert st == 0
+        assert bool((first == again).all()), ("repeat", r)
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------- edge cases -----
+@pytest.mark.parametrize("kind", KINDS)
+def test_special_scalars(o, kind):
+    import torch
+
+    n = 150
+    p = inputs.make_problem(kind, "L", n, lda=n, alpha=SCAL[kind][0], beta=SCAL[kind][1],
+                            seed=5)
+    dp = DeviceProblem(p)
+    zero = (0.0, 0.0) if kind == "w" else 0.0
+    one = (1.0, 0.0) if kind == "w" else 1.0
+    nanA = torch.full_like(dp.A, 0xFF)          # all-ones bytes: NaN in every type
+    # alpha = 0: y := beta*y, A and x not read
+    st, yd = dp.run(alpha=zero, A=nanA)
+    assert st == 0
+    err, _ = errors(o, p, from_device(yd, p.y), alpha=zero)
+    assert np.max(err) <= TOL[kind]
+    # alpha = 0, beta = 1: nothing is touched
+    st, yd = dp.run(alpha=zero, beta=one, A=nanA)
+    assert st == 0 and bool((yd == dp.y0).all())
+    # beta = 0: y is not read (NaN input does not propagate)
+    ynan = torch.full_like(dp.y0, 0xFF)
+    st, yd = dp.run(beta=zero, y=ynan)
+    assert st == 0
+    err, _ = errors(o, p, from_device(yd, p.y), beta=zero)
+    assert np.max(err) <= TOL[kind]
+
+
+def test_n_zero_and_errors(lib):
+    import torch
+
+    y = torch.full((16,), 7.0, device="cuda")
+    assert lib.xsymv_s("U", 0, 1.0, 0, 1, 0, 1, 0.0, y, 1) == 0
+    assert lib.xsymv_s("Q", 4, 1.0, y, 4, y, 1, 0.0, y, 1) == 1
+    assert lib.xsymv_s("U", -2, 1.0, y, 4, y, 1, 0.0, y, 1) == 2
+    assert lib.xsymv_s("U", 4, 1.0, y, 3, y, 1, 0.0, y, 1) == 5
+    assert lib.xsymv_s("U", 4, 1.0, y, 4, y, 0, 0.0, y, 1) == 7
+    assert lib.xsymv_s("U", 4, 1.0, y, 4, y, 1, 0.0, y, 0) == 10
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_y_guard_words(o, kind):
+    """elements just before and after y are never written"""
+    import torch
+
+    n = 333
+    p = inputs.make_problem(kind, "U", n, lda=n, alpha=SCAL[kind][0], beta=SCAL[kind][1],
+                            seed=9)
+    dp = DeviceProblem(p)
+    guard = 64
+    buf = torch.full((dp.y0.numel() + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    buf[guard:guard + dp.y0.numel()] = dp.y0
+    st, _ = dp.run(y=buf[guard:guard + dp.y0.numel()])
+    assert st == 0
+    torch.cuda.synchronize()
+    assert bool((buf[:guard] == 0x5A).all()) and bool((buf[-guard:] == 0x5A).all())
+    err, _ = errors(o, p, from_device(buf[guard:guard + dp.y0.numel()], p.y))
+    assert np.max(err) <= TOL[kind]
+
+
+def test_non_default_stream(o):
+    import torch
+
+    p = inputs.make_problem("s", "U", 2000, lda=2000, alpha=1.0, beta=0.0, seed=11)
+    dp = DeviceProblem(p)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        st, yd = dp.run()
+    assert st == 0
+    s.synchronize()
+    err, _ = errors(o, p, from_device(yd, p.y))
+    assert np.max(err) <= TOL["s"]
+
+
+def test_launch_count_and_timing(lib):
+    """every call launches exactly the main kernel and the finaliser"""
+    p = inputs.make_problem("s", "U", 1000, alpha=1.0, beta=0.5, seed=1)
+    dp = DeviceProblem(p)
+    c0 = lib.xsymv_launch_count()
+    lib.xsymv_timing_enable(True)
+    for _ in range(5):
+        st, _ = dp.run()
+        assert st == 0
+    calls, main_ms, call_ms = lib.xsymv_timing_read()
+    lib.xsymv_timing_enable(False)
+    assert lib.xsymv_launch_count() - c0 == 10
+    assert calls == 5 and 0 < main_ms <= call_ms
