@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the xSYMV hot path on GB300.
+
+Workload: SSYMV, n = 32768, upper triangle stored, lda = n + 32, alpha = 1,
+beta = 0 (the largest point of the single-precision size sweep n = 4096 ..
+32768), synthetic U(-1, 1) data drawn on the device, NaN outside the stored
+triangle.  One step = one call of the library's C ABI (main kernel + fixed-
+order finaliser).  The stored triangle is 2.15 GB, far larger than the 129 MB
+L2, so no flush is needed between steps.
+
+Prints one JSON line: GFLOP/s (2 n^2 flops per call) over the timed steps,
+the main kernel's achieved HBM bandwidth against the measured copy bandwidth
+(roofline), the end-to-end rate through the host-buffer entry point with the
+host<->device copies inside the timed region, SM clocks sampled during the
+timed region, the number of kernels launched, and the CPU oracle timed on a
+bounded sample (cpu_baseline).  ``--impl reference`` times the CPU oracle
+alone on a sample of the same workload.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
+the problem (the call does not shard); ``value`` is the total over ranks
+divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "xSYMV GFLOP/s & achieved HBM GB/s (% of GB300 peak) at n=8K–32K, 1 GPU"
+UNIT = "GFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL = "symv_main"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--n", type=int, default=32768)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the n = 8K..32K sweep")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def flops(n: int) -> float:
+    return 2.0 * n * n
+
+
+def triangle_bytes(n: int, es: int = 4) -> float:
+    return n * (n + 1) / 2.0 * es
+
+
+def workload_config(n: int) -> dict:
+    return {"workload": "ssymv n=%d uplo=U lda=n+32 alpha=1 beta=0 U(-1,1) seed=%d" % (n, n),
+            "kernel_variant": None, "l2": "inputs larger than L2 (triangle %.2f GB vs 129 MB L2), "
+            "no flush" % (triangle_bytes(n) / 1e9)}
+
+
+# ----------------------------------------------------------------- helpers --
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    csrc = os.path.join(ROOT, "symmetric_matrix_vector_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")) and f != "xsymv_tuned.h":
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(n: int, variant: str):
+    """DRAM bytes per launch of the main kernel from the committed ncu
+    summary, scaled to n by stored elements; None when the kernel sources
+    changed since the capture or no capture matches."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_digest") != kernel_source_digest() or rec.get("variant") != variant:
+        return None
+    n0 = rec["n"]
+    per_elem = rec["dram_bytes_per_launch"] / (n0 * (n0 + 1) / 2.0)
+    return per_elem * n * (n + 1) / 2.0
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_stop(self):
+        self.t_stop = time.perf_counter()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        inside = [s for t, s in self.samples
+                  if self.t_start is not None and self.t_start <= t <= (self.t_stop or t)]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], None, set()
+        for s in inside:
+            parts = [p.strip() for p in s.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def cpu_oracle_rate(n: int, seconds: float):
+    """Run the CPU oracle's SSYMV on an n-by-n instance of the workload's
+    recipe until ``seconds`` have passed; returns (GFLOP/s, calls, seconds)."""
+    import oracle
+    from symmetric_matrix_vector_gb300 import inputs
+
+    p = inputs.workload("ssymv_sweep", n=n)
+    o = oracle.get()
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        info, _, _, _ = o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+        assert info == 0
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return flops(n) * calls / el / 1e9, calls, el
+
+
+def run_reference(args):
+    """The CPU oracle, timed step by step on a sample of the workload."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from symmetric_matrix_vector_gb300 import inputs
+
+    o = oracle.get()
+    # size the per-step sample so the whole run stays within ~90 s
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    p0 = inputs.workload("ssymv_sweep", n=1024)
+    t0 = time.perf_counter()
+    o.symv("s", p0.uplo, p0.n, p0.alpha, p0.A, p0.lda, p0.x, 1, p0.beta, p0.y, 1)
+    rate = flops(1024) / max(time.perf_counter() - t0, 1e-6)
+    ns = int((budget * rate / 2.0) ** 0.5) // 256 * 256
+    ns = max(256, min(ns, 8192))
+    p = inputs.workload("ssymv_sweep", n=ns)
+    for _ in range(args.warmup):
+        o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+    el = time.perf_counter() - t0
+    value = flops(ns) * args.steps / el / 1e9
+    sample = ("each step: the oracle's three-part SSYMV (binary64 accumulator) on n=%d of the "
+              "same recipe (uplo=U, lda=n+32, alpha=1, beta=0), single-threaded" % ns)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(args.n),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- our arm ----
+
+def run_ours(args):
+    import torch
+
+    import symmetric_matrix_vector_gb300 as xs
+    from symmetric_matrix_vector_gb300 import _build, inputs
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    _build.build()
+    xs.load()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    n = args.n
+    prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
+    A, x, y = prob["A"], prob["x"], prob["y"]
+    lda = prob["lda"]
+    stream = torch.cuda.current_stream()
+    variant = xs.xsymv_variant_name("s", xs.xsymv_selected_variant("s", "U", n))
+
+    def step():
+        xs.check(xs.xsymv_s("U", n, 1.0, A, lda, x, 1, 0.0, y, 1))
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region 1: the value (no hooks inside the library)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = xs.xsymv_launch_count()
+    clocks.mark_start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    barrier()
+    launches = xs.xsymv_launch_count() - l0
+    clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * flops(n) / (ms_per_step * 1e-3) / 1e9
+
+    # ---- timed region 2: per-kernel durations via the library's events
+    xs.xsymv_timing_enable(True)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    calls, main_ms, call_ms = xs.xsymv_timing_read()
+    xs.xsymv_timing_enable(False)
+    main_avg = main_ms / max(calls, 1)
+    peak, peak_src = measured_peak()
+    alg = triangle_bytes(n)
+    achieved = alg / (main_avg * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(n, variant),
+                "peak_source": peak_src, "kernel": KERNEL, "main_kernel_ms": main_avg,
+                "call_ms": call_ms / max(calls, 1),
+                "algorithmic_bytes": alg}
+
+    # ---- size sweep (n = 8K..32K), beside the headline
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        del prob
+        for m in (8192, 16384, 24576, 32768):
+            if m == n:
+                sweep.append({"n": m, "gflops": flops(m) / (ms_per_step * 1e-3) / 1e9,
+                              "gbs": triangle_bytes(m) / (ms_per_step * 1e-3) / 1e9})
+                continue
+            pm = inputs.device_problem("s", "U", m, lda=m + 32, alpha=1.0, beta=0.0, seed=m)
+            reps = max(10, min(200, int(4e10 / triangle_bytes(m))))
+            for _ in range(5):
+                xs.check(xs.xsymv_s("U", m, 1.0, pm["A"], m + 32, pm["x"], 1, 0.0, pm["y"], 1))
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                xs.check(xs.xsymv_s("U", m, 1.0, pm["A"], m + 32, pm["x"], 1, 0.0, pm["y"], 1))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / reps
+            sweep.append({"n": m, "gflops": flops(m) / (t * 1e-3) / 1e9,
+                          "gbs": triangle_bytes(m) / (t * 1e-3) / 1e9,
+                          "frac": triangle_bytes(m) / (t * 1e-3) / 1e9 / peak})
+            del pm
+        torch.cuda.empty_cache()
+        prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
+        A, x, y = prob["A"], prob["x"], prob["y"]
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
+        hA.copy_(A)
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        del prob, A, x, y
+        torch.cuda.empty_cache()
+
+        def hstep():
+            xs.check(xs.xsymv_s_host("U", n, 1.0, hA, lda, hx, 1, 0.0, hy, 1))
+
+        for _ in range(3):
+            hstep()
+        esteps = max(3, min(args.steps, 50))
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(esteps):
+            hstep()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1) / esteps
+        if dist is not None:
+            t = torch.tensor([ems], device="cuda", dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d, d2h = xs.xsymv_host_traffic()
+        e2e = {"value": world * flops(n) / (ems * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "steps": esteps, "api": "xsymv_s_host (pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, calls_c, el = cpu_oracle_rate(8192, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "the oracle's three-part SSYMV (binary64 accumulator), single-threaded, "
+                         "on n=8192 of the same recipe (uplo=U, lda=n+32, alpha=1, beta=0): "
+                         "%d calls in %.1f s" % (calls_c, el)}
+
+    if rank == 0:
+        cfg = workload_config(n)
+        cfg["kernel_variant"] = variant
+        cfg["parallelism"] = "replicas" if world > 1 else "single-gpu"
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": cfg,
+            "hbm_gbs": triangle_bytes(n) / (ms_per_step * 1e-3) / 1e9,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks.summary(), "gpu_launches": launches, "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

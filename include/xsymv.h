@@ -97,6 +97,30 @@ XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_c64 *A, int
 XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int lda,
                       const xsymv_dd *x, int incx, xsymv_dd beta, xsymv_dd *y, int incy);
 
+/* ---- host-buffer variants ----------------------------------------------
+ * Same arguments, semantics and status codes as the five calls above, but A,
+ * x and y are HOST pointers (pageable or, for full link bandwidth, pinned;
+ * device pointers also work).  Each call copies the stored triangle (in
+ * column panels, so at most a few percent of the other triangle travels
+ * too), x and, when beta != 0, y into library-owned device buffers on the
+ * current stream, runs the same kernels, copies the n elements of y back
+ * and waits for the stream: y holds the result when the call returns.  The
+ * device buffers are kept per (device, stream) for reuse, like the
+ * workspace.  On a CUDA error y may be partly written. */
+XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float *A, int lda,
+                           const float *x, int incx, float beta, float *y, int incy);
+XSYMV_API int xsymv_d_host(char uplo, int n, double alpha, const double *A, int lda,
+                           const double *x, int incx, double beta, double *y, int incy);
+XSYMV_API int xhemv_c_host(char uplo, int n, xsymv_c32 alpha, const xsymv_c32 *A, int lda,
+                           const xsymv_c32 *x, int incx, xsymv_c32 beta, xsymv_c32 *y, int incy);
+XSYMV_API int xhemv_z_host(char uplo, int n, xsymv_c64 alpha, const xsymv_c64 *A, int lda,
+                           const xsymv_c64 *x, int incx, xsymv_c64 beta, xsymv_c64 *y, int incy);
+XSYMV_API int xsymv_w_host(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int lda,
+                           const xsymv_dd *x, int incx, xsymv_dd beta, xsymv_dd *y, int incy);
+
+/* Bytes the last host-buffer call copied host-to-device and back. */
+XSYMV_API int xsymv_host_traffic(long long *h2d_bytes, long long *d2h_bytes);
+
 /* Stream for subsequent calls from any thread (a cudaStream_t; NULL = the
  * legacy default stream).  Returns 0. */
 XSYMV_API int xsymv_set_stream(void *stream);

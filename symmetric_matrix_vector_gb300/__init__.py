@@ -28,6 +28,8 @@ __all__ = [
     "xsymv_timing_enable", "xsymv_timing_read", "xsymv_launch_count",
     "xsymv_variant_count", "xsymv_variant_name", "xsymv_set_variant", "xsymv_selected_variant",
     "xsymv_workspace_bytes", "XsymvError", "check", "load", "library_path", "ENTRY_POINTS",
+    "xsymv_s_host", "xsymv_d_host", "xhemv_c_host", "xhemv_z_host", "xsymv_w_host", "symv_host",
+    "xsymv_host_traffic",
 ]
 
 ENTRY_POINTS = {"s": "xsymv_s", "d": "xsymv_d", "c": "xhemv_c", "z": "xhemv_z", "w": "xsymv_w"}
@@ -74,9 +76,12 @@ def load():
         c_char, c_int, vp = ctypes.c_char, ctypes.c_int, ctypes.c_void_p
         scal = {"s": ctypes.c_float, "d": ctypes.c_double, "c": C32, "z": C64, "w": DD}
         for k, name in ENTRY_POINTS.items():
-            fn = getattr(lib, name)
-            fn.argtypes = [c_char, c_int, scal[k], vp, c_int, vp, c_int, scal[k], vp, c_int]
-            fn.restype = c_int
+            for nm in (name, name + "_host"):
+                fn = getattr(lib, nm)
+                fn.argtypes = [c_char, c_int, scal[k], vp, c_int, vp, c_int, scal[k], vp, c_int]
+                fn.restype = c_int
+        lib.xsymv_host_traffic.argtypes = [ctypes.POINTER(ctypes.c_longlong)] * 2
+        lib.xsymv_host_traffic.restype = c_int
         lib.xsymv_set_stream.argtypes = [vp]
         lib.xsymv_set_stream.restype = c_int
         lib.xsymv_get_stream.restype = vp
@@ -146,14 +151,27 @@ def _torch_stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def _call(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream):
+def _host_ptr(a) -> int:
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        return a.data_ptr()
+    if hasattr(a, "ctypes"):                      # numpy array
+        return a.ctypes.data
+    raise TypeError("expected a host pointer, a numpy array or a tensor, got %r" % type(a))
+
+
+def _call(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=False):
     lib = load()
     s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
                                                 getattr(stream, "cuda_stream", stream))
     lib.xsymv_set_stream(ctypes.c_void_p(s or 0))
-    fn = getattr(lib, ENTRY_POINTS[kind])
-    return fn(_uplo(uplo), int(n), _scalar(kind, alpha), ctypes.c_void_p(_ptr(A)), int(lda),
-              ctypes.c_void_p(_ptr(x)), int(incx), _scalar(kind, beta), ctypes.c_void_p(_ptr(y)),
+    fn = getattr(lib, ENTRY_POINTS[kind] + ("_host" if host else ""))
+    cv = _host_ptr if host else _ptr
+    return fn(_uplo(uplo), int(n), _scalar(kind, alpha), ctypes.c_void_p(cv(A)), int(lda),
+              ctypes.c_void_p(cv(x)), int(incx), _scalar(kind, beta), ctypes.c_void_p(cv(y)),
               int(incy))
 
 
@@ -180,6 +198,39 @@ def xsymv_w(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
 def symv(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
     """Dispatch on kind ('s', 'd', 'c', 'z', 'w') to the matching entry point."""
     return _call(kind.lower(), uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xsymv_s_host(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("s", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def xsymv_d_host(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("d", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def xhemv_c_host(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("c", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def xhemv_z_host(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("z", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def xsymv_w_host(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return _call("w", uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def symv_host(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    """Host-buffer variant of ``symv``: A, x, y are host arrays (numpy arrays,
+    CPU tensors or raw addresses); y holds the result on return."""
+    return _call(kind.lower(), uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+def xsymv_host_traffic():
+    """(host-to-device bytes, device-to-host bytes) of the last host call"""
+    h, d = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    check(load().xsymv_host_traffic(ctypes.byref(h), ctypes.byref(d)))
+    return h.value, d.value
 
 
 def xsymv_set_stream(stream) -> int:

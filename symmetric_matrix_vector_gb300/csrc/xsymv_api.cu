@@ -21,6 +21,7 @@ std::mutex g_mu;
 struct WsEntry {
   int device;
   cudaStream_t stream;
+  int slot;
   void* ptr;
   size_t bytes;
 };
@@ -100,7 +101,9 @@ bool current_device(int* dev, int* sm_count) {
   return true;
 }
 
-void* workspace(size_t bytes, cudaStream_t stream, int* status) {
+std::atomic<long long> g_h2d{0}, g_d2h{0};
+
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) {
@@ -111,7 +114,7 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status) {
   if (bytes == 0) bytes = 256;
   std::lock_guard<std::mutex> lk(g_mu);
   for (WsEntry& w : g_ws) {
-    if (w.device != d || w.stream != stream) continue;
+    if (w.device != d || w.stream != stream || w.slot != slot) continue;
     if (w.bytes >= bytes) return w.ptr;
     // grow: the old buffer may still be in use by work queued on `stream`
     e = cudaStreamSynchronize(stream);
@@ -143,11 +146,16 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status) {
     *status = XSYMV_ERR_ALLOC;
     return nullptr;
   }
-  g_ws.push_back(WsEntry{d, stream, p, bytes});
+  g_ws.push_back(WsEntry{d, stream, slot, p, bytes});
   return p;
 }
 
 void note_launches(int k) { g_launches.fetch_add(k); }
+
+void note_host_traffic(long long h2d, long long d2h) {
+  g_h2d.store(h2d);
+  g_d2h.store(d2h);
+}
 
 void timing_begin(cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -245,6 +253,12 @@ XSYMV_API int xsymv_timing_read(int* calls, double* main_ms, double* call_ms) {
 }
 
 XSYMV_API long long xsymv_launch_count(void) { return g_launches.load(); }
+
+XSYMV_API int xsymv_host_traffic(long long* h2d_bytes, long long* d2h_bytes) {
+  if (h2d_bytes) *h2d_bytes = g_h2d.load();
+  if (d2h_bytes) *d2h_bytes = g_d2h.load();
+  return XSYMV_OK;
+}
 
 XSYMV_API int xsymv_variant_count(char kind) {
   switch (kind_index(kind)) {

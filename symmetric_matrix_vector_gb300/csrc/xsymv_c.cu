@@ -23,3 +23,16 @@ extern "C" XSYMV_API int xhemv_c(char uplo, int n, xsymv_c32 alpha, const xsymv_
                               reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                               incy);
 }
+
+extern "C" XSYMV_API int xhemv_c_host(char uplo, int n, xsymv_c32 alpha, const xsymv_c32* A, int lda, const xsymv_c32* x,
+                                   int incx, xsymv_c32 beta, xsymv_c32* y, int incy) {
+  using T = xsymv::c32;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_host_entry<T>(xsymv::kVariants_c,
+                                   (int)(sizeof(xsymv::kVariants_c) / sizeof(xsymv::kVariants_c[0])),
+                                   'c', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                                   reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                                   incy);
+}

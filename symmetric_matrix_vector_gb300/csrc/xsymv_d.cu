@@ -24,3 +24,16 @@ extern "C" XSYMV_API int xsymv_d(char uplo, int n, double alpha, const double* A
                               reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                               incy);
 }
+
+extern "C" XSYMV_API int xsymv_d_host(char uplo, int n, double alpha, const double* A, int lda, const double* x,
+                                   int incx, double beta, double* y, int incy) {
+  using T = double;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_host_entry<T>(xsymv::kVariants_d,
+                                   (int)(sizeof(xsymv::kVariants_d) / sizeof(xsymv::kVariants_d[0])),
+                                   'd', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                                   reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                                   incy);
+}

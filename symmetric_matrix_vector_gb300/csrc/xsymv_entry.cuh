@@ -169,6 +169,79 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   return XSYMV_OK;
 }
 
+// -------------------------------------------------- host-buffer variant --
+// Copies the stored triangle (in column panels), x and, when beta != 0, y to
+// library-owned device memory on the call's stream, runs symv_entry there,
+// copies y back and waits for the stream.
+template <class T>
+int symv_host_entry(const Variant<T>* table, int count, char kind, char uplo, int n, T alpha,
+                    const T* hA, int lda, const T* hx, int incx, T beta, T* hy, int incy) {
+  int info = check_args(uplo, n, lda, incx, incy);
+  if (info) return info;
+  note_host_traffic(0, 0);
+  if (n == 0) return XSYMV_OK;
+  const bool az = is_zero(alpha), bz = is_zero(beta);
+  if (az && is_one(beta)) return XSYMV_OK;
+  int dev = 0, sms = 0;
+  if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
+
+  const int upper = (uplo == 'U' || uplo == 'u');
+  const long long es = (long long)sizeof(T);
+  const long long per16 = 16 / es > 0 ? 16 / es : 1;
+  const long long ldd = align_up(n, per16);          // 16-byte aligned columns
+  const long long a_bytes = align_up(ldd * n * es, 256);
+  const long long v_bytes = align_up((long long)n * es, 256);
+  cudaStream_t st = current_stream();
+  int status = XSYMV_OK;
+  char* buf = static_cast<char*>(workspace((size_t)(a_bytes + 2 * v_bytes), st, &status, 1));
+  if (!buf) return status;
+  T* dA = reinterpret_cast<T*>(buf);
+  T* dx = reinterpret_cast<T*>(buf + a_bytes);
+  T* dy = reinterpret_cast<T*>(buf + a_bytes + v_bytes);
+
+  long long h2d = 0, d2h = 0;
+  cudaError_t e = cudaSuccess;
+  // strided vector -> contiguous device copy in memory order; a negative
+  // stride keeps its sign (stride -1 on the device)
+  auto vec_in = [&](const T* h, int inc, T* d) {
+    const long long ai = inc < 0 ? -(long long)inc : inc;
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(d, es, h, ai * es, es, n, cudaMemcpyDefault, st);
+    h2d += (long long)n * es;
+  };
+  if (!az) {
+    // the triangle in panels of P columns: upper rows [0, j1), lower [j0, n)
+    const long long P = align_up((n + 63) / 64, 64);   // at most 64 panels
+    for (long long j0 = 0; j0 < n && e == cudaSuccess; j0 += P) {
+      const long long j1 = j0 + P < n ? j0 + P : n;
+      const long long r0 = upper ? 0 : j0;
+      const long long r1 = upper ? j1 : n;
+      e = cudaMemcpy2DAsync(dA + j0 * ldd + r0, ldd * es, hA + j0 * (long long)lda + r0,
+                            (long long)lda * es, (r1 - r0) * es, j1 - j0, cudaMemcpyDefault, st);
+      h2d += (r1 - r0) * es * (j1 - j0);
+    }
+    vec_in(hx, incx, dx);
+  }
+  if (!bz) vec_in(hy, incy, dy);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  status = symv_entry<T>(table, count, kind, uplo, n, alpha, dA, (int)ldd, dx, incx < 0 ? -1 : 1,
+                         beta, dy, incy < 0 ? -1 : 1);
+  if (status) return status;
+  const long long ai = incy < 0 ? -(long long)incy : incy;
+  e = cudaMemcpy2DAsync(hy, ai * es, dy, es, es, n, cudaMemcpyDefault, st);
+  d2h += (long long)n * es;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_host_traffic(h2d, d2h);
+  return XSYMV_OK;
+}
+
 template <class T>
 long long workspace_bytes(const Variant<T>* table, int count, char kind, char uplo, int n) {
   if (check_args(uplo, n, n > 1 ? n : 1, 1, 1)) return XSYMV_ERR_VALUE;

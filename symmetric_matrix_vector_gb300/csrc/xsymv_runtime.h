@@ -14,9 +14,13 @@ cudaStream_t current_stream();
 // device (records the CUDA error)
 bool current_device(int* dev, int* sm_count);
 
-// workspace of at least `bytes` for (current device, stream); nullptr and
-// *status set on failure
-void* workspace(size_t bytes, cudaStream_t stream, int* status);
+// buffer of at least `bytes` for (current device, stream, slot); nullptr and
+// *status set on failure.  Slot 0: the kernels' workspace; slot 1: device
+// copies of host operands for the host-buffer entry points.
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot = 0);
+
+// bytes moved by the last host-buffer call
+void note_host_traffic(long long h2d, long long d2h);
 
 void note_launches(int k);
 void record_cuda_error(cudaError_t e);

@@ -25,3 +25,16 @@ extern "C" XSYMV_API int xsymv_s(char uplo, int n, float alpha, const float* A, 
                               reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                               incy);
 }
+
+extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float* A, int lda, const float* x,
+                                   int incx, float beta, float* y, int incy) {
+  using T = float;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_host_entry<T>(xsymv::kVariants_s,
+                                   (int)(sizeof(xsymv::kVariants_s) / sizeof(xsymv::kVariants_s[0])),
+                                   's', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                                   reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                                   incy);
+}

@@ -23,3 +23,16 @@ extern "C" XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_d
                               reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                               incy);
 }
+
+extern "C" XSYMV_API int xsymv_w_host(char uplo, int n, xsymv_dd alpha, const xsymv_dd* A, int lda, const xsymv_dd* x,
+                                   int incx, xsymv_dd beta, xsymv_dd* y, int incy) {
+  using T = xsymv::dd;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_host_entry<T>(xsymv::kVariants_w,
+                                   (int)(sizeof(xsymv::kVariants_w) / sizeof(xsymv::kVariants_w[0])),
+                                   'w', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                                   reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                                   incy);
+}

@@ -23,3 +23,16 @@ extern "C" XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_
                               reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                               incy);
 }
+
+extern "C" XSYMV_API int xhemv_z_host(char uplo, int n, xsymv_c64 alpha, const xsymv_c64* A, int lda, const xsymv_c64* x,
+                                   int incx, xsymv_c64 beta, xsymv_c64* y, int incy) {
+  using T = xsymv::c64;
+  T a, b;
+  memcpy(&a, &alpha, sizeof(T));
+  memcpy(&b, &beta, sizeof(T));
+  return xsymv::symv_host_entry<T>(xsymv::kVariants_z,
+                                   (int)(sizeof(xsymv::kVariants_z) / sizeof(xsymv::kVariants_z[0])),
+                                   'z', uplo, n, a, reinterpret_cast<const T*>(A), lda,
+                                   reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
+                                   incy);
+}

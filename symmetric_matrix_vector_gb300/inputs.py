@@ -192,3 +192,64 @@ def workload(name: str, n: int | None = None, **over) -> Problem:
 
 
 WORKLOADS = ("ssymv_small", "ssymv_sweep", "dsymv", "chemv", "zhemv", "wsymv")
+
+
+# ---------------------------------------------------------------------------
+# the same recipe drawn on the GPU (torch's Philox generator), for benchmarks
+# ---------------------------------------------------------------------------
+
+def device_problem(kind: str, uplo: str, n: int, *, lda: int | None = None, alpha=1.0, beta=0.0,
+                   dist: str = "uniform", diag_shift: float = 0.0, seed: int = 0,
+                   device: str = "cuda"):
+    """Dense random problem on the device, contiguous x and y (inc = 1).
+
+    Same layout and sentinels as ``make_problem`` (NaN outside the stored
+    triangle, in the padding rows and in Hermitian diagonal imaginary parts);
+    the random stream is torch's CUDA generator seeded with ``seed``, so the
+    values differ from the host recipe's.  Returns a dict with tensors ``A``
+    (shape (n, lda), or (n, lda, 2) for w), ``x``, ``y`` and the scalars.
+    """
+    import torch
+
+    kind = kind.lower()
+    uplo = uplo.upper()
+    lda = max(1, n) if lda is None else lda
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    rdt = {"s": torch.float32, "d": torch.float64, "c": torch.float32, "z": torch.float64,
+           "w": torch.float64}[kind]
+    width = {"s": 1, "d": 1, "c": 2, "z": 2, "w": 2}[kind]
+
+    def draw(shape):
+        if dist == "uniform":
+            return torch.rand(shape, generator=g, device=device, dtype=rdt).mul_(2).sub_(1)
+        return torch.randn(shape, generator=g, device=device, dtype=rdt)
+
+    def values(count):
+        if kind in ("s", "d"):
+            return draw((count,))
+        if kind in ("c", "z"):
+            return draw((count, 2))
+        hi = draw((count,))
+        lo = hi * (2.0 ** -53) * (torch.rand((count,), generator=g, device=device,
+                                             dtype=rdt) * 2 - 1)
+        return torch.stack([hi, lo], dim=-1)
+
+    A = values(n * lda).reshape(n, lda, *(() if width == 1 else (2,)))
+    rows = torch.arange(lda, device=device)[None, :]
+    cols = torch.arange(n, device=device)[:, None]
+    unused = (rows > cols) if uplo == "U" else ((rows < cols) | (rows >= n))
+    if width == 1:
+        A.masked_fill_(unused, float("nan"))
+    else:
+        A.masked_fill_(unused[..., None], float("nan"))
+    idx = torch.arange(n, device=device)
+    if diag_shift:
+        if width == 1:
+            A[idx, idx] += diag_shift
+        else:
+            A[idx, idx, 0] += diag_shift
+    if kind in ("c", "z"):
+        A[idx, idx, 1] = float("nan")
+    return dict(kind=kind, uplo=uplo, n=n, lda=lda, alpha=alpha, beta=beta, A=A.contiguous(),
+                x=values(n).contiguous(), y=values(n).contiguous())

@@ -268,3 +268,26 @@ def test_launch_count_and_timing(lib):
     lib.xsymv_timing_enable(False)
     assert lib.xsymv_launch_count() - c0 == 10
     assert calls == 5 and 0 < main_ms <= call_ms
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("uplo", ["U", "L"])
+def test_host_buffer_entry(o, lib, kind, uplo):
+    """the *_host entry points take host arrays, copy the triangle in panels
+    and return with y written"""
+    al, be = SCAL[kind]
+    for n, incx, incy in ((1, 1, 1), (129, 1, 1), (300, -2, 3), (5000, 1, -1)):
+        if kind in ("z", "w") and n == 5000:
+            n = 2100
+        p = inputs.make_problem(kind, uplo, n, lda=n + 3, alpha=al, beta=be, incx=incx, incy=incy,
+                                seed=31 + n)
+        y = p.y.copy()
+        st = lib.symv_host(kind, uplo, n, al, p.A, p.lda, p.x, incx, be, y, incy)
+        assert st == 0
+        err, _ = errors(o, p, y)
+        assert np.max(err) <= TOL[kind], (kind, uplo, n, float(np.max(err)))
+        h2d, d2h = lib.xsymv_host_traffic()
+        es = p.A.itemsize * (2 if kind == "w" else 1)
+        assert d2h == n * es
+        # only the triangle (plus a few percent in panel corners) travels
+        assert h2d <= (n * (n + 1) / 2 * 1.05 + 2 * n + 64 * n) * es
