@@ -74,6 +74,7 @@ typedef struct { double hi, lo; } xsymv_dd;
 #define XSYMV_ERR_ALLOC (-2)      /* the workspace could not be allocated       */
 #define XSYMV_ERR_DEVICE (-3)     /* no usable device, or not compute cap. 10.3 */
 #define XSYMV_ERR_VALUE (-4)      /* invalid argument to a non-BLAS entry point */
+#define XSYMV_ERR_TOO_LARGE (-5)  /* problem exceeds xsymv_s_noalloc's scratch  */
 
 /* SSYMV: float data, float arithmetic. */
 XSYMV_API int xsymv_s(char uplo, int n, float alpha, const float *A, int lda,
@@ -96,6 +97,24 @@ XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_c64 *A, int
  * are renormalised as they are read; results are renormalised pairs. */
 XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int lda,
                       const xsymv_dd *x, int incx, xsymv_dd beta, xsymv_dd *y, int incy);
+
+/* ---- allocation-free SSYMV ----------------------------------------------
+ * The report has no counterpart to this entry point.  It is xsymv_s for
+ * callers that cannot let a library allocate device memory during a call:
+ * a plug-in whose host application owns all device memory and forbids
+ * allocating inside the plug-in, or latency-critical code where cudaMalloc /
+ * cudaFree would block or synchronise the device.  Same arguments, results
+ * and status codes as xsymv_s; it never allocates.  Its workspace is one
+ * fixed 16 MiB device array in the library, held on every GPU that loads the
+ * library until the process exits; a problem whose workspace does not fit
+ * (roughly n > 19000) returns XSYMV_ERR_TOO_LARGE with nothing enqueued.
+ * The first call on a device looks up the array's address on that device;
+ * make that call before any stream capture.  All calls share the array and
+ * it keeps the last call's contents (nothing in it needs to start at zero):
+ * calls that overlap on the GPU, on different streams or from different
+ * threads, race on it and corrupt each other's results. */
+XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float *A, int lda,
+                              const float *x, int incx, float beta, float *y, int incy);
 
 /* ---- host-buffer variants ----------------------------------------------
  * Same arguments, semantics and status codes as the five calls above, but A,

@@ -210,6 +210,8 @@ XSYMV_API const char* xsymv_status_string(int status) {
     case XSYMV_ERR_ALLOC: return "workspace allocation failed";
     case XSYMV_ERR_DEVICE: return "no usable device (compute capability 10.3 required)";
     case XSYMV_ERR_VALUE: return "invalid value";
+    case XSYMV_ERR_TOO_LARGE:
+      return "problem too large for xsymv_s_noalloc's fixed 16 MiB workspace (use xsymv_s)";
   }
   return "unknown status";
 }

@@ -1,4 +1,7 @@
 // Entry point xsymv_s of the xsymv C ABI and its compiled kernel variants.
+#include <mutex>
+#include <vector>
+
 #include "xsymv_entry.cuh"
 
 namespace xsymv {
@@ -37,4 +40,120 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
                                    's', uplo, n, a, reinterpret_cast<const T*>(A), lda,
                                    reinterpret_cast<const T*>(x), incx, b, reinterpret_cast<T*>(y),
                                    incy);
+}
+
+// ---------------------------------------------------------------------------
+// xsymv_s_noalloc: SSYMV that never allocates device memory.
+//
+// Some callers cannot let a library allocate device memory during a call:
+// a plug-in whose host application owns all device memory and forbids
+// allocations inside the plug-in, or latency-critical code where cudaMalloc /
+// cudaFree would block or synchronise the device.  For them this entry point
+// runs the same two kernels as xsymv_s, with the partial-sum workspace taken
+// from the fixed device array below instead of a cudaMalloc'd buffer.
+//
+// * The array holds kNoallocScratchBytes (16 MiB) on every GPU that loads
+//   this library, until the process exits.  Problems whose workspace does
+//   not fit (roughly n > 19000 for single precision on GB300) are rejected
+//   with XSYMV_ERR_TOO_LARGE before anything is enqueued.
+// * The first call on a device looks up the array's device address
+//   (cudaGetSymbolAddress, with that device current) and caches it; make
+//   that first call before any stream capture.
+// * Nothing in the array has to start at zero: the main kernel writes every
+//   workspace slot the finaliser then reads.  The array keeps the last
+//   call's contents.
+// * All calls share the one array: calls that overlap on the GPU (on
+//   different streams, or from different host threads) race and corrupt
+//   each other's results.  Order them, e.g. on one stream.
+static constexpr long long kNoallocScratchBytes = 16ll << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+struct NoallocDevice {
+  int device;
+  void* scratch;
+};
+std::mutex g_noalloc_mu;
+std::vector<NoallocDevice> g_noalloc_devices;
+
+// device address of g_noalloc_scratch on the current device
+int noalloc_scratch(void** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    xsymv::record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  for (const NoallocDevice& s : g_noalloc_devices)
+    if (s.device == d) {
+      *out = s.scratch;
+      return XSYMV_OK;
+    }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    xsymv::record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  g_noalloc_devices.push_back(NoallocDevice{d, p});
+  *out = p;
+  return XSYMV_OK;
+}
+}  // namespace
+
+extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float* A, int lda,
+                                         const float* x, int incx, float beta, float* y,
+                                         int incy) {
+  using namespace xsymv;
+  int info = check_args(uplo, n, lda, incx, incy);
+  if (info) return info;
+  if (n == 0) return XSYMV_OK;
+  const bool az = alpha == 0.f, bz = beta == 0.f;
+  if (az && beta == 1.f) return XSYMV_OK;
+
+  const int upper = (uplo == 'U' || uplo == 'u');
+  cudaStream_t st = current_stream();
+  float* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
+  const float* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
+  const unsigned fgrid = (unsigned)((n + 255) / 256);
+
+  void* scratch = nullptr;
+  int status = noalloc_scratch(&scratch);
+  if (status) return status;
+
+  if (az) {  // y := beta*y, no workspace needed
+    Plan p = plan_make(n, 32, upper, 1);
+    symv_finalize<float><<<fgrid, 256, 0, st>>>(p, nullptr, nullptr, alpha, beta,
+                                                 bz ? kZero : kAlphaZero, y0, incy);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+    return XSYMV_OK;
+  }
+
+  const int count = (int)(sizeof(kVariants_s) / sizeof(kVariants_s[0]));
+  Workload<float> wl;
+  status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
+  if (status) return status;
+  if (wl.bytes > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
+  float* Wc = static_cast<float*>(scratch);
+  float* Wr = reinterpret_cast<float*>(static_cast<char*>(scratch) + wl.wc_bytes);
+  const bool aligned =
+      (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (((long long)lda * 4) % 16 == 0);
+  cudaError_t e = wl.variant->launch(wl.plan, A, lda, x0, incx, Wc, Wr, aligned, st);
+  if (e == cudaSuccess) {
+    symv_finalize<float><<<fgrid, 256, 0, st>>>(wl.plan, Wc, Wr, alpha, beta,
+                                                 bz ? kBetaZero : kFull, y0, incy);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_launches(2);
+  return XSYMV_OK;
 }
