@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "xSYMV GFLOP/s & achieved HBM GB/s (% of GB300 peak) at n=8K–32K, 1 GPU"
 UNIT = "GFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
 KERNEL = "symv_main"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -320,11 +321,16 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     alg = triangle_bytes(n)
     achieved = alg / (main_avg * 1e-3) / 1e9
+    probes = xs.xsymv_probe_peaks() if rank == 0 else {}
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": recorded_traffic(n, variant),
                 "peak_source": peak_src, "kernel": KERNEL, "main_kernel_ms": main_avg,
-                "call_ms": call_ms / max(calls, 1),
-                "algorithmic_bytes": alg}
+                "call_ms": call_ms / max(calls, 1), "algorithmic_bytes": alg,
+                "nominal_gbs": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS}
+    if probes:
+        roofline["same_run"] = {k: round(v, 2) for k, v in probes.items()}
+        roofline["frac_same_run_copy"] = achieved / probes["copy_gbs"]
+        roofline["frac_same_run_read"] = achieved / probes["read_gbs"]
 
     # ---- size sweep (n = 8K..32K), beside the headline
     sweep = []

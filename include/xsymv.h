@@ -75,6 +75,7 @@ typedef struct { double hi, lo; } xsymv_dd;
 #define XSYMV_ERR_DEVICE (-3)     /* no usable device, or not compute cap. 10.3 */
 #define XSYMV_ERR_VALUE (-4)      /* invalid argument to a non-BLAS entry point */
 #define XSYMV_ERR_TOO_LARGE (-5)  /* problem exceeds xsymv_s_noalloc's scratch  */
+#define XSYMV_ERR_TIMEOUT (-6)    /* a kernel gave up waiting; y was set to NaN */
 
 /* SSYMV: float data, float arithmetic. */
 XSYMV_API int xsymv_s(char uplo, int n, float alpha, const float *A, int lda,
@@ -109,10 +110,11 @@ XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int l
  * library until the process exits; a problem whose workspace does not fit
  * (roughly n > 19000) returns XSYMV_ERR_TOO_LARGE with nothing enqueued.
  * The first call on a device looks up the array's address on that device;
- * make that call before any stream capture.  All calls share the array and
- * it keeps the last call's contents (nothing in it needs to start at zero):
- * calls that overlap on the GPU, on different streams or from different
- * threads, race on it and corrupt each other's results. */
+ * make that call before any stream capture.  It also clears the array's
+ * 256-byte status header, the only part that must start at zero.  All calls
+ * share the array and it keeps the last call's contents: calls that overlap
+ * on the GPU, on different streams or from different threads, race on it
+ * and corrupt each other's results. */
 XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float *A, int lda,
                               const float *x, int incx, float beta, float *y, int incy);
 
@@ -145,6 +147,22 @@ XSYMV_API int xsymv_host_traffic(long long *h2d_bytes, long long *d2h_bytes);
 XSYMV_API int xsymv_set_stream(void *stream);
 XSYMV_API void *xsymv_get_stream(void);
 
+/* ---- failure detection -------------------------------------------------
+ * Every wait inside the kernels (for bulk copies landing in shared memory)
+ * has a time limit, 2 s by default.  If one runs out, the kernel records
+ * the failure in the workspace, waits (again with the limit) for its copies
+ * in flight and returns; the call's y is then filled with NaN.
+ * xsymv_sync_status waits for the current stream and returns
+ * XSYMV_ERR_TIMEOUT if the latest call on it (device, stream) failed that
+ * way, else 0 (or XSYMV_ERR_CUDA). */
+XSYMV_API int xsymv_sync_status(void);
+/* Time limit of those waits in ns (0: back to 2 s). */
+XSYMV_API int xsymv_set_wait_limit(unsigned long long ns);
+/* Test hook: on != 0 makes every bulk-copy barrier expect 16 bytes that
+ * never arrive, so the next calls' waits run out (nothing faults; the
+ * kernels return after the time limit).  0 restores normal operation. */
+XSYMV_API int xsymv_test_stall(int on);
+
 /* Human-readable text for a status code (static storage). */
 XSYMV_API const char *xsymv_status_string(int status);
 
@@ -162,14 +180,26 @@ XSYMV_API int xsymv_timing_enable(int on);
  * Clears the record.  Returns 0, or XSYMV_ERR_CUDA. */
 XSYMV_API int xsymv_timing_read(int *calls, double *main_ms, double *call_ms);
 
+/* Roofline denominators measured now on the current device and stream:
+ * HBM copy bandwidth (bytes read + written per second, 1 GiB buffers), HBM
+ * read bandwidth, and FP64 / FP32 FMA throughput (2 flops per FMA), each the
+ * best of a few timed runs.  Allocates and frees two 1 GiB buffers;
+ * synchronises the stream.  Any output pointer may be NULL. */
+XSYMV_API int xsymv_probe_peaks(double *copy_gbs, double *read_gbs, double *fp64_tflops,
+                                double *fp32_tflops);
+
 /* Number of kernels this library has launched since it was loaded. */
 XSYMV_API long long xsymv_launch_count(void);
 
 /* ---- kernel variants: the tuner's parameter space ----------------------- */
 
 /* kind: 's', 'd', 'c', 'z' or 'w'.  Number of compiled variants (0 for an
- * unknown kind) and the name of variant index ("vr<VR>_u<U>_w<WARPS>":
- * 16-byte vectors per lane, columns in flight per warp, warps per block). */
+ * unknown kind) and the name of variant index: "vr<VR>_u<U>_<p><S>_w<W>" =
+ * 16-byte vectors per lane (the tile edge is 32 lanes x VR vectors), columns
+ * per chunk, how off-diagonal columns reach the arithmetic (p = r: loads
+ * into registers; t: a per-warp shared-memory ring of S chunks filled by
+ * bulk (TMA) copies; a: the same ring filled by per-lane cp.async copies)
+ * and warps per block. */
 XSYMV_API int xsymv_variant_count(char kind);
 XSYMV_API const char *xsymv_variant_name(char kind, int index);
 

@@ -29,7 +29,8 @@ __all__ = [
     "xsymv_variant_count", "xsymv_variant_name", "xsymv_set_variant", "xsymv_selected_variant",
     "xsymv_workspace_bytes", "XsymvError", "check", "load", "library_path", "ENTRY_POINTS",
     "xsymv_s_host", "xsymv_d_host", "xhemv_c_host", "xhemv_z_host", "xsymv_w_host", "symv_host",
-    "xsymv_host_traffic",
+    "xsymv_host_traffic", "xsymv_sync_status", "xsymv_set_wait_limit", "xsymv_test_stall",
+    "xsymv_probe_peaks",
 ]
 
 ENTRY_POINTS = {"s": "xsymv_s", "d": "xsymv_d", "c": "xhemv_c", "z": "xhemv_z", "w": "xsymv_w"}
@@ -82,6 +83,13 @@ def load():
                 fn.restype = c_int
         lib.xsymv_host_traffic.argtypes = [ctypes.POINTER(ctypes.c_longlong)] * 2
         lib.xsymv_host_traffic.restype = c_int
+        lib.xsymv_sync_status.restype = c_int
+        lib.xsymv_probe_peaks.argtypes = [ctypes.POINTER(ctypes.c_double)] * 4
+        lib.xsymv_probe_peaks.restype = c_int
+        lib.xsymv_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+        lib.xsymv_set_wait_limit.restype = c_int
+        lib.xsymv_test_stall.argtypes = [c_int]
+        lib.xsymv_test_stall.restype = c_int
         lib.xsymv_set_stream.argtypes = [vp]
         lib.xsymv_set_stream.restype = c_int
         lib.xsymv_get_stream.restype = vp
@@ -231,6 +239,27 @@ def xsymv_host_traffic():
     h, d = ctypes.c_longlong(0), ctypes.c_longlong(0)
     check(load().xsymv_host_traffic(ctypes.byref(h), ctypes.byref(d)))
     return h.value, d.value
+
+
+def xsymv_sync_status() -> int:
+    """Wait for the current stream; XSYMV_ERR_TIMEOUT (-6) if its latest call
+    gave up on a bounded wait (its y was set to NaN), else 0."""
+    return load().xsymv_sync_status()
+
+
+def xsymv_set_wait_limit(ns: int) -> int:
+    return load().xsymv_set_wait_limit(int(ns))
+
+
+def xsymv_test_stall(on: bool) -> int:
+    return load().xsymv_test_stall(1 if on else 0)
+
+
+def xsymv_probe_peaks():
+    """Measured now: dict of copy_gbs, read_gbs, fp64_tflops, fp32_tflops."""
+    v = [ctypes.c_double(0) for _ in range(4)]
+    check(load().xsymv_probe_peaks(*[ctypes.byref(x) for x in v]))
+    return dict(zip(("copy_gbs", "read_gbs", "fp64_tflops", "fp32_tflops"), (x.value for x in v)))
 
 
 def xsymv_set_stream(stream) -> int:

@@ -24,6 +24,7 @@ struct WsEntry {
   int slot;
   void* ptr;
   size_t bytes;
+  int epoch;     // last call number handed out (slot 0)
 };
 std::vector<WsEntry> g_ws;
 
@@ -102,8 +103,10 @@ bool current_device(int* dev, int* sm_count) {
 }
 
 std::atomic<long long> g_h2d{0}, g_d2h{0};
+std::atomic<unsigned long long> g_wait_limit{2000000000ull};
+std::atomic<uint32_t> g_extra_tx{0};
 
-void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot) {
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) {
@@ -111,44 +114,57 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot) {
     *status = XSYMV_ERR_CUDA;
     return nullptr;
   }
-  if (bytes == 0) bytes = 256;
+  if (bytes < 256) bytes = 256;
   std::lock_guard<std::mutex> lk(g_mu);
-  for (WsEntry& w : g_ws) {
-    if (w.device != d || w.stream != stream || w.slot != slot) continue;
-    if (w.bytes >= bytes) return w.ptr;
-    // grow: the old buffer may still be in use by work queued on `stream`
-    e = cudaStreamSynchronize(stream);
-    if (e == cudaSuccess) e = cudaFree(w.ptr);
-    w.ptr = nullptr;
-    w.bytes = 0;
-    if (e != cudaSuccess) {
-      record_cuda_error(e);
-      *status = XSYMV_ERR_CUDA;
-      return nullptr;
+  WsEntry* w = nullptr;
+  for (WsEntry& c : g_ws)
+    if (c.device == d && c.stream == stream && c.slot == slot) w = &c;
+  if (w == nullptr) {
+    g_ws.push_back(WsEntry{d, stream, slot, nullptr, 0, 0});
+    w = &g_ws.back();
+  }
+  if (w->bytes < bytes) {
+    if (w->ptr != nullptr) {
+      // the old buffer may still be in use by work queued on `stream`
+      e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess) e = cudaFree(w->ptr);
+      w->ptr = nullptr;
+      w->bytes = 0;
+      if (e != cudaSuccess) {
+        record_cuda_error(e);
+        *status = XSYMV_ERR_CUDA;
+        return nullptr;
+      }
+      bytes += bytes / 8;
     }
-    size_t want = bytes + bytes / 8;
-    e = cudaMalloc(&w.ptr, want);
+    e = cudaMalloc(&w->ptr, bytes);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       cudaGetLastError();
-      w.ptr = nullptr;
+      w->ptr = nullptr;
       *status = XSYMV_ERR_ALLOC;
       return nullptr;
     }
-    w.bytes = want;
-    return w.ptr;
+    w->bytes = bytes;
+    if (slot == 0) {
+      e = cudaMemsetAsync(w->ptr, 0, 256, stream);   // status header
+      if (e != cudaSuccess) {
+        record_cuda_error(e);
+        *status = XSYMV_ERR_CUDA;
+        return nullptr;
+      }
+      w->epoch = 0;
+    }
   }
-  void* p = nullptr;
-  e = cudaMalloc(&p, bytes);
-  if (e != cudaSuccess) {
-    record_cuda_error(e);
-    cudaGetLastError();
-    *status = XSYMV_ERR_ALLOC;
-    return nullptr;
+  if (epoch != nullptr) {
+    w->epoch = (w->epoch >= 0x7ffffffe) ? 1 : w->epoch + 1;
+    *epoch = w->epoch;
   }
-  g_ws.push_back(WsEntry{d, stream, slot, p, bytes});
-  return p;
+  return w->ptr;
 }
+
+unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
+uint32_t test_extra_tx() { return g_extra_tx.load(); }
 
 void note_launches(int k) { g_launches.fetch_add(k); }
 
@@ -210,6 +226,8 @@ XSYMV_API const char* xsymv_status_string(int status) {
     case XSYMV_ERR_ALLOC: return "workspace allocation failed";
     case XSYMV_ERR_DEVICE: return "no usable device (compute capability 10.3 required)";
     case XSYMV_ERR_VALUE: return "invalid value";
+    case XSYMV_ERR_TIMEOUT:
+      return "a bounded wait in the main kernel ran out; the call's y was set to NaN";
     case XSYMV_ERR_TOO_LARGE:
       return "problem too large for xsymv_s_noalloc's fixed 16 MiB workspace (use xsymv_s)";
   }
@@ -255,6 +273,45 @@ XSYMV_API int xsymv_timing_read(int* calls, double* main_ms, double* call_ms) {
 }
 
 XSYMV_API long long xsymv_launch_count(void) { return g_launches.load(); }
+
+XSYMV_API int xsymv_sync_status(void) {
+  cudaStream_t s = g_stream.load();
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  void* ptr = nullptr;
+  int epoch = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (WsEntry& w : g_ws)
+      if (w.device == d && w.stream == s && w.slot == 0) {
+        ptr = w.ptr;
+        epoch = w.epoch;
+      }
+  }
+  if (ptr == nullptr || epoch == 0) return XSYMV_OK;
+  int word = 0;
+  e = cudaMemcpy(&word, ptr, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  return word == epoch ? XSYMV_ERR_TIMEOUT : XSYMV_OK;
+}
+
+XSYMV_API int xsymv_set_wait_limit(unsigned long long ns) {
+  g_wait_limit.store(ns == 0 ? 2000000000ull : ns);
+  return XSYMV_OK;
+}
+
+XSYMV_API int xsymv_test_stall(int on) {
+  g_extra_tx.store(on ? 16u : 0u);
+  return XSYMV_OK;
+}
 
 XSYMV_API int xsymv_host_traffic(long long* h2d_bytes, long long* d2h_bytes) {
   if (h2d_bytes) *h2d_bytes = g_h2d.load();

@@ -12,35 +12,80 @@
 
 namespace xsymv {
 
+// Workspace layout: a 256-byte header (word 0: the status word the main
+// kernel sets to the call's epoch when a bounded wait runs out), then the
+// column partials Wc, then the row partials Wr.
+constexpr long long kHeaderBytes = 256;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // 2 s
+
+// Everything one launch of the main kernel needs.
+template <class T>
+struct MainArgs {
+  Plan plan;
+  const T* A;
+  long long lda;
+  const T* x;      // logical element 0
+  long long incx;
+  T* Wc;
+  T* Wr;
+  int* status;
+  int epoch;
+  bool aligned;    // A and lda*sizeof(T) on the 16-byte grid
+  cudaStream_t stream;
+};
+
 // One compiled configuration of the main kernel.
 template <class T>
 struct Variant {
   const char* name;
-  int NB;     // tile edge = 32 lanes * elements per 16 bytes * VR
-  int warps;  // warps per block
-  cudaError_t (*launch)(const Plan&, const T*, long long, const T*, long long, T*, T*, bool,
-                        cudaStream_t);
+  int NB;      // tile edge = 32 lanes * elements per 16 bytes * VR
+  int warps;   // warps per block
+  int stages;  // shared-memory ring depth
+  int pipe;    // enum Pipe
+  cudaError_t (*launch)(const MainArgs<T>&);
   int (*ctas_per_sm)();
 };
 
-template <class T, int VR, int U, int WARPS>
-cudaError_t launch_main(const Plan& p, const T* A, long long lda, const T* x, long long incx,
-                        T* Wc, T* Wr, bool aligned, cudaStream_t st) {
-  const unsigned grid = (unsigned)((p.W + WARPS - 1) / WARPS);
-  if (aligned)
-    symv_main<T, VR, U, WARPS, true><<<grid, WARPS * 32, 0, st>>>(p, A, lda, x, incx, Wc, Wr);
+template <class T, int VR, int U, int S, int P, int WARPS>
+constexpr int ring_smem_bytes() {
+  return WARPS * RingLayout<T, VR, U, S, P>::WARP_BYTES;
+}
+
+template <class T, int VR, int U, int S, int P, int WARPS>
+cudaError_t launch_main(const MainArgs<T>& a) {
+  constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
+  static bool configured = false;
+  if (!configured) {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    configured = true;
+  }
+  const unsigned grid = (unsigned)((a.plan.W + WARPS - 1) / WARPS);
+  const unsigned long long limit = wait_limit_ns();
+  const uint32_t extra = test_extra_tx();
+  if (a.aligned)
+    symv_main<T, VR, U, S, P, WARPS, true><<<grid, WARPS * 32, smem, a.stream>>>(
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   else
-    symv_main<T, VR, U, WARPS, false><<<grid, WARPS * 32, 0, st>>>(p, A, lda, x, incx, Wc, Wr);
+    symv_main<T, VR, U, S, P, WARPS, false><<<grid, WARPS * 32, 0, a.stream>>>(
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   return cudaGetLastError();
 }
 
-template <class T, int VR, int U, int WARPS>
+template <class T, int VR, int U, int S, int P, int WARPS>
 int ctas_per_sm() {
   static int cached = 0;
   if (!cached) {
+    constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, WARPS, true>,
-                                                      WARPS * 32, 0) != cudaSuccess || b < 1) {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true>,
+                                                      WARPS * 32, smem) != cudaSuccess || b < 1) {
       cudaGetLastError();
       b = 1;
     }
@@ -49,11 +94,36 @@ int ctas_per_sm() {
   return cached;
 }
 
-#define XSYMV_VARIANT(T, VR, U, W)                                                      \
-  Variant<T> {                                                                          \
-    "vr" #VR "_u" #U "_w" #W, 32 * Ops<T>::VPL * (VR), (W), &launch_main<T, VR, U, W>, \
-        &ctas_per_sm<T, VR, U, W>                                                       \
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>, pipe r = registers,
+// t = bulk-copy (TMA) ring, a = cp.async ring.
+#define XSYMV_VARIANT_P(T, VR, U, S, P, L, W)                                             \
+  Variant<T> {                                                                            \
+    "vr" #VR "_u" #U "_" L #S "_w" #W, 32 * Ops<T>::VPL * (VR), (W), (S), (P),           \
+        &launch_main<T, VR, U, S, P, W>, &ctas_per_sm<T, VR, U, S, P, W>                  \
   }
+#define XSYMV_REG(T, VR, U, W) XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W)
+#define XSYMV_TMA(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeBulk, "t", W)
+#define XSYMV_ASYNC(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeLdgsts, "a", W)
+
+template <class T>
+cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, T alpha, T beta, int mode,
+                            T* y0, long long incy, const int* status, int epoch,
+                            cudaStream_t st) {
+  // programmatic dependent launch: the launch overlaps the tail of the main
+  // kernel, whose completion the finaliser awaits with griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.n + kFinCols - 1) / kFinCols));
+  cfg.blockDim = dim3(kFinParts * kFinCols);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, symv_finalize<T>, p, Wc, Wr, alpha, beta, mode, y0, incy,
+                            status, epoch);
+}
 
 // ---------------------------------------------------------------- checks --
 inline int check_args(char uplo, int n, int lda, int incx, int incy) {
@@ -82,7 +152,8 @@ template <class T>
 struct Workload {
   Plan plan;
   const Variant<T>* variant;
-  long long wc_bytes;   // offset of Wr inside the workspace
+  long long wc_off;     // byte offset of Wc in the workspace
+  long long wr_off;     // byte offset of Wr
   long long bytes;      // total workspace bytes
 };
 
@@ -102,8 +173,9 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps;
   out->plan = plan_make(n, v->NB, upper, wmax);
   out->variant = v;
-  out->wc_bytes = align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
-  out->bytes = out->wc_bytes + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
+  out->wc_off = kHeaderBytes;
+  out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
+  out->bytes = out->wr_off + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
   return XSYMV_OK;
 }
 
@@ -122,7 +194,6 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   // pointers to logical element 0 (BLAS: negative strides start at the end)
   T* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
   const T* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
-  const unsigned fgrid = (unsigned)((n + 255) / 256);
 
   if (az) {  // y := beta*y: neither A nor x is read
     int dev = 0, sms = 0;
@@ -130,9 +201,8 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     Plan p = plan_make(n, 32, upper, 1);
     timing_begin(st);
     timing_mid(st);
-    symv_finalize<T><<<fgrid, 256, 0, st>>>(p, nullptr, nullptr, alpha, beta,
-                                             bz ? kZero : kAlphaZero, y0, incy);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, alpha, beta, bz ? kZero : kAlphaZero,
+                                       y0, incy, nullptr, 0, st);
     timing_end(st);
     if (e != cudaSuccess) {
       record_cuda_error(e);
@@ -145,20 +215,20 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   Workload<T> wl;
   int status = plan_call(table, count, kind, upper, n, &wl);
   if (status) return status;
-  char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status));
+  int epoch = 0;
+  char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status, 0, &epoch));
   if (!ws) return status;
-  T* Wc = reinterpret_cast<T*>(ws);
-  T* Wr = reinterpret_cast<T*>(ws + wl.wc_bytes);
-
-  const bool aligned = (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
-                       (((long long)lda * (long long)sizeof(T)) % 16 == 0);
+  MainArgs<T> m{wl.plan, A, lda, x0, incx, reinterpret_cast<T*>(ws + wl.wc_off),
+                reinterpret_cast<T*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
+                (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
+                    (((long long)lda * (long long)sizeof(T)) % 16 == 0),
+                st};
   timing_begin(st);
-  cudaError_t e = wl.variant->launch(wl.plan, A, lda, x0, incx, Wc, Wr, aligned, st);
+  cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {
     timing_mid(st);
-    symv_finalize<T><<<fgrid, 256, 0, st>>>(wl.plan, Wc, Wr, alpha, beta, bz ? kBetaZero : kFull,
-                                             y0, incy);
-    e = cudaGetLastError();
+    e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, alpha, beta, bz ? kBetaZero : kFull, y0, incy,
+                           m.status, epoch, st);
   }
   timing_end(st);
   if (e != cudaSuccess) {
@@ -193,7 +263,7 @@ int symv_host_entry(const Variant<T>* table, int count, char kind, char uplo, in
   const long long v_bytes = align_up((long long)n * es, 256);
   cudaStream_t st = current_stream();
   int status = XSYMV_OK;
-  char* buf = static_cast<char*>(workspace((size_t)(a_bytes + 2 * v_bytes), st, &status, 1));
+  char* buf = static_cast<char*>(workspace((size_t)(a_bytes + 2 * v_bytes), st, &status, 1, nullptr));
   if (!buf) return status;
   T* dA = reinterpret_cast<T*>(buf);
   T* dx = reinterpret_cast<T*>(buf + a_bytes);

@@ -13,21 +13,31 @@
 //   symv_main      Each warp streams an equal share of the triangle's column
 //                  segments (see xsymv_plan.h).  A column segment is the
 //                  NB-row piece of one matrix column inside one block row:
-//                  the 32 lanes cover its NB rows with 16-byte loads
-//                  (VR vectors per lane), U columns in flight at a time.
-//                  Row terms stay in the lane's registers for the whole block
-//                  row (no reduction needed: each lane owns its rows); column
-//                  terms are summed across the 32 lanes with a butterfly
-//                  reduce-scatter of the U columns and written to the
-//                  workspace.  The diagonal tile is handled by the same loop
-//                  with a triangle mask: its stored part is read once and
-//                  contributes to both sides, which is what the report's
-//                  mirrored copy in shared memory (part two) achieves.
-//   symv_finalize  One thread per output element sums the workspace slots of
-//                  its row in a fixed order and applies y = alpha*s + beta*y
-//                  (the report's parts three and the beta scaling).  No atomic
+//                  the 32 lanes cover its NB rows (VR 16-byte vectors per
+//                  lane), U columns at a time.  Off-diagonal columns travel
+//                  HBM -> shared memory by bulk asynchronous copies
+//                  (cp.async.bulk, the TMA engine) into a ring of STAGES
+//                  chunks per warp, completed on mbarriers, so several chunks
+//                  are in flight while the warp computes; without 16-byte
+//                  alignment they are read with element loads instead.  Row
+//                  terms stay in the lane's registers for the whole block row
+//                  (each lane owns its rows); column terms are summed across
+//                  the 32 lanes with a butterfly reduce-scatter of the U
+//                  columns and written to the workspace.  The diagonal tile
+//                  goes through the same arithmetic with a triangle mask: its
+//                  stored part is read once and contributes to both sides,
+//                  which is what the report's mirrored copy in shared memory
+//                  (part two) achieves.
+//   symv_finalize  For every output element, sums the workspace slots of its
+//                  row in a fixed order and applies y = alpha*s + beta*y (the
+//                  report's part three and beta scaling).  No atomic
 //                  operation touches data, so results are bit-identical from
 //                  run to run.
+//
+// Every wait on an mbarrier has a time limit.  A wait that runs out marks the
+// call failed (status word := the call's epoch), waits (again with a limit)
+// for the warp's copies still in flight and leaves the kernel; the finaliser
+// then writes NaN to y and the host can read the status.
 #pragma once
 
 #include "xsymv_plan.h"
@@ -42,6 +52,76 @@ template <> struct Log2<4> { static constexpr int v = 2; };
 template <> struct Log2<8> { static constexpr int v = 3; };
 template <> struct Log2<16> { static constexpr int v = 4; };
 template <> struct Log2<32> { static constexpr int v = 5; };
+
+// -------------------------------------------------- async-copy primitives --
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// one arrival that also announces `bytes` of asynchronous transfers
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// HBM -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// per-thread asynchronous 16-byte copy HBM -> shared (LDGSTS, L2 only)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's committed groups are still pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+// Wait for phase `parity` of the mbarrier, giving up after about limit_ns.
+// The limit is counted in SM clock cycles (at most 2 per ns, i.e. a clock of
+// up to 2 GHz; a slower clock only lengthens the wait), read every 256 tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  const long long limit = (long long)(limit_ns < (1ull << 61) ? limit_ns : (1ull << 61)) * 2;
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
 
 // Sum v[0..U) over the 32 lanes of the warp.  On return lane l holds the
 // total of column u = l >> (5 - log2 U); the additions happen in a fixed
@@ -67,6 +147,33 @@ __device__ __forceinline__ T reduce_scatter(T (&v)[U], int lane) {
   return v[0];
 }
 
+// How off-diagonal columns travel from HBM to the arithmetic.
+enum Pipe {
+  kPipeRegisters = 0,   // 16-byte loads straight into registers, U columns at a time
+  kPipeBulk = 1,        // per-warp shared-memory ring filled by cp.async.bulk (TMA) copies
+  kPipeLdgsts = 2,      // per-warp shared-memory ring filled by per-lane cp.async copies
+};
+
+// Per-warp ring of STAGES chunks in shared memory; chunk = U column segments
+// of NB elements (plus one mbarrier per stage for the bulk-copy ring).
+template <class T, int VR, int U, int STAGES, int PIPE>
+struct RingLayout {
+  static constexpr int NB = 32 * Ops<T>::VPL * VR;
+  static constexpr int COL_BYTES = NB * (int)sizeof(T);
+  static constexpr int STAGE_BYTES = U * COL_BYTES;
+  static constexpr int DATA_BYTES = PIPE != kPipeRegisters ? STAGES * STAGE_BYTES : 0;
+  static constexpr int BAR_BYTES = PIPE == kPipeBulk ? ((STAGES * 8 + 15) / 16) * 16 : 0;
+  static constexpr int WARP_BYTES = DATA_BYTES + BAR_BYTES;
+};
+
+struct Ring {
+  uint32_t data;      // shared address of stage 0
+  uint32_t bars;      // shared address of the first mbarrier
+  int head;           // stage of the next chunk to consume
+  uint32_t phase;     // bit s: parity of stage s's next completion
+  uint32_t extra_tx;  // bytes announced beyond the copies (0; > 0 only to test the time limit)
+};
+
 template <class T, int VR, int U>
 struct WarpTile {
   static constexpr int VPL = Ops<T>::VPL;
@@ -81,16 +188,32 @@ struct WarpTile {
     return r0 + (long long)(v * 32 + lane) * VPL + k;
   }
 
-  // write the U reduced column sums of one chunk (cnt valid columns)
-  __device__ __forceinline__ static void emit_columns(T (&cp)[U], int lane, int cnt, T* wc_row,
-                                                      long long j0) {
+  // row terms into racc; column terms reduced over the warp and written for
+  // the cnt valid columns j0 .. j0+cnt-1 (a[u] = column j0+u, xl on lane u =
+  // x(j0+u))
+  __device__ __forceinline__ void accumulate(T (&a)[U][VR][VPL], T xl, int cnt, T* wc_row,
+                                             long long j0, int lane) {
+    T cp[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const T xj = Ops<T>::shfl(xl, u);
+      T c = Ops<T>::zero();
+#pragma unroll
+      for (int v = 0; v < VR; ++v)
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+          racc[v][k] = Ops<T>::madd(racc[v][k], a[u][v][k], xj);
+          c = Ops<T>::maddc(c, a[u][v][k], xi[v][k]);
+        }
+      cp[u] = c;
+    }
     T red = reduce_scatter<T, U>(cp, lane);
     const int uo = lane >> (5 - H);
     if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc_row[j0 + uo] = red;
   }
 
-  // Columns [ja, jb) of block row starting at row r0, all NB rows stored
-  // (off-diagonal, complete block row).  ALIGNED: 16-byte vector loads.
+  // Columns [ja, jb) of the block row at r0, all NB rows stored, read with
+  // 16-byte vector loads (ALIGNED) or element loads straight into registers.
   template <bool ALIGNED>
   __device__ __forceinline__ void dense_cols(const T* __restrict__ A, long long lda,
                                              const T* __restrict__ x, long long incx, long long r0,
@@ -119,64 +242,192 @@ struct WarpTile {
             for (int k = 0; k < VPL; ++k)
               a[u][v][k] = Ops<T>::load(A + (j0 + u) * lda + row_of(r0, v, lane, k));
       }
-      T cp[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const T xj = Ops<T>::shfl(xl, u);
-        T c = Ops<T>::zero();
-#pragma unroll
-        for (int v = 0; v < VR; ++v)
-#pragma unroll
-          for (int k = 0; k < VPL; ++k) {
-            racc[v][k] = Ops<T>::madd(racc[v][k], a[u][v][k], xj);
-            c = Ops<T>::maddc(c, a[u][v][k], xi[v][k]);
-          }
-        cp[u] = c;
-      }
-      emit_columns(cp, lane, U, wc_row, j0);
+      accumulate(a, xl, U, wc_row, j0, lane);
     }
     if (j0 < jb) masked_cols<false>(A, lda, x, incx, r0, j0, jb, wc_row, lane, 0, 0);
+  }
+
+  // issue the bulk copies of chunk c (columns ja + c*U ..) into its stage
+  template <int STAGES>
+  __device__ __forceinline__ static void ring_fill(const Ring& rg, long long c,
+                                                   const T* __restrict__ A, long long lda,
+                                                   long long r0, long long ja, long long jb,
+                                                   int lane) {
+    constexpr int COL_BYTES = NB * (int)sizeof(T);
+    const int st = (int)((rg.head + c) % STAGES);
+    const long long j0 = ja + c * U;
+    const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+    const uint32_t bar = rg.bars + 8u * st;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(cnt * COL_BYTES) + rg.extra_tx);
+    __syncwarp();
+    if (lane < cnt)
+      bulk_g2s(rg.data + (uint32_t)(st * U + lane) * COL_BYTES, A + (j0 + lane) * lda + r0,
+               COL_BYTES, bar);
+  }
+
+  // Columns [ja, jb) of the block row at r0 (all NB rows stored, 16-byte
+  // aligned), streamed through the warp's ring.  Returns false if a wait ran
+  // out (after draining the copies still in flight).
+  template <int STAGES>
+  __device__ __forceinline__ bool dense_cols_ring(Ring& rg, const T* __restrict__ A,
+                                                  long long lda, const T* __restrict__ x,
+                                                  long long incx, long long r0, long long ja,
+                                                  long long jb, T* wc_row, int lane,
+                                                  unsigned long long limit_ns) {
+    constexpr int COL_BYTES = NB * (int)sizeof(T);
+    const long long nch = (jb - ja + U - 1) / U;
+    for (long long c = 0; c < nch && c < STAGES; ++c)
+      ring_fill<STAGES>(rg, c, A, lda, r0, ja, jb, lane);
+    // x of the chunk's columns, loaded two chunks ahead so that its L2
+    // latency overlaps the waits and arithmetic of the chunks before
+    auto load_x = [&](long long c) -> T {
+      const long long j0 = ja + c * U;
+      return (c < nch && lane < U && j0 + lane < jb) ? Ops<T>::load(x + (j0 + lane) * incx)
+                                                     : Ops<T>::zero();
+    };
+    T x_next = load_x(0);
+    T x_after = load_x(1);
+    for (long long c = 0; c < nch; ++c) {
+      const int st = (int)((rg.head + c) % STAGES);
+      const uint32_t par = (rg.phase >> st) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(rg.bars + 8u * st, par, limit_ns));
+      if (!ok) {
+        // drain: every chunk c .. min(c+STAGES, nch)-1 has copies in flight
+        for (long long k = c; k < nch && k < c + STAGES; ++k) {
+          const int s2 = (int)((rg.head + k) % STAGES);
+          mbar_wait_bounded(rg.bars + 8u * s2, (rg.phase >> s2) & 1u, limit_ns);
+        }
+        return false;
+      }
+      rg.phase ^= 1u << st;
+      const long long j0 = ja + c * U;
+      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+      const T xl = x_next;
+      x_next = x_after;
+      x_after = load_x(c + 2);
+      T a[U][VR][VPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VR; ++v) {
+          if (u < cnt) {
+            const uint4 raw = lds128(rg.data + (uint32_t)(st * U + u) * COL_BYTES +
+                                     (uint32_t)(v * 32 + lane) * 16u);
+            Unpack<T>::run(raw, a[u][v]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::zero();
+          }
+        }
+      // the stage is refilled only after its values have been used by the
+      // arithmetic, so the asynchronous write cannot overtake the reads
+      accumulate(a, xl, cnt, wc_row, j0, lane);
+      __syncwarp();
+      if (c + STAGES < nch) ring_fill<STAGES>(rg, c + STAGES, A, lda, r0, ja, jb, lane);
+    }
+    rg.head = (int)((rg.head + nch) % STAGES);
+    return true;
+  }
+
+  // Columns [ja, jb) of the block row at r0 (all NB rows stored, 16-byte
+  // aligned), through the warp's ring filled by per-lane cp.async copies:
+  // every lane copies and later reads only its own 16-byte pieces, so the
+  // lanes need no synchronisation; chunk c+STAGES-1 is issued before chunk c
+  // is consumed.
+  template <int STAGES>
+  __device__ __forceinline__ void dense_cols_ldgsts(uint32_t ring, const T* __restrict__ A,
+                                                    long long lda, const T* __restrict__ x,
+                                                    long long incx, long long r0, long long ja,
+                                                    long long jb, T* wc_row, int lane) {
+    constexpr int COL_BYTES = NB * (int)sizeof(T);
+    const long long nch = (jb - ja + U - 1) / U;
+    auto fill = [&](long long c) {
+      if (c < nch) {
+        const int st = (int)(c % STAGES);
+        const long long j0 = ja + c * U;
+        const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (u < cnt)
+#pragma unroll
+            for (int v = 0; v < VR; ++v)
+              cp_async16(ring + (uint32_t)(st * U + u) * COL_BYTES + (uint32_t)(v * 32 + lane) * 16u,
+                         A + (j0 + u) * lda + row_of(r0, v, lane, 0));
+      }
+      cp_async_commit();   // empty groups keep the group count uniform
+    };
+    auto load_x = [&](long long c) -> T {
+      const long long j0 = ja + c * U;
+      return (c < nch && lane < U && j0 + lane < jb) ? Ops<T>::load(x + (j0 + lane) * incx)
+                                                     : Ops<T>::zero();
+    };
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) fill(c);
+    T x_next = load_x(0);
+    for (long long c = 0; c < nch; ++c) {
+      fill(c + STAGES - 1);
+      const T xl = x_next;
+      x_next = load_x(c + 1);
+      cp_async_wait<STAGES - 1>();   // this lane's copies of chunk c have landed
+      const int st = (int)(c % STAGES);
+      const long long j0 = ja + c * U;
+      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+      T a[U][VR][VPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VR; ++v) {
+          if (u < cnt) {
+            const uint4 raw =
+                lds128(ring + (uint32_t)(st * U + u) * COL_BYTES + (uint32_t)(v * 32 + lane) * 16u);
+            Unpack<T>::run(raw, a[u][v]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::zero();
+          }
+        }
+      accumulate(a, xl, cnt, wc_row, j0, lane);
+    }
+    cp_async_wait<0>();
   }
 
   // Columns [ja, jb) with per-element masks: rows must be < n and, when
   // DIAG, inside the stored triangle (upper: row <= col; lower: row >= col).
   // On the diagonal only the row term is taken (and for a Hermitian matrix
   // only the real part of the element).  Elements outside the mask are
-  // never read.
+  // never read.  One column at a time (diagonal tiles and ragged edges are a
+  // small share of the work, and this keeps the kernel's register count low);
+  // each column sum is a full butterfly over the warp, written by lane 0.
   template <bool DIAG>
   __device__ __forceinline__ void masked_cols(const T* __restrict__ A, long long lda,
                                               const T* __restrict__ x, long long incx,
                                               long long r0, long long ja, long long jb,
                                               T* wc_row, int lane, long long n, int upper) {
-    for (long long j0 = ja; j0 < jb; j0 += U) {
-      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
-      const T xl = (lane < cnt) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
-      T cp[U];
+#pragma unroll 1
+    for (long long j = ja; j < jb; ++j) {
+      const T xj = Ops<T>::load(x + j * incx);
+      const T* col = A + j * lda;
+      T c = Ops<T>::zero();
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const long long j = j0 + u;
-        const T xj = Ops<T>::shfl(xl, u);
-        T c = Ops<T>::zero();
+      for (int v = 0; v < VR; ++v)
 #pragma unroll
-        for (int v = 0; v < VR; ++v)
-#pragma unroll
-          for (int k = 0; k < VPL; ++k) {
-            const long long r = row_of(r0, v, lane, k);
-            bool valid = u < cnt;
-            if (DIAG) valid = valid && r < n && (upper ? r <= j : r >= j);
-            if (valid) {
-              T a = Ops<T>::load(A + j * lda + r);
-              if (DIAG && r == j) {
-                racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::diag(a), xj);
-              } else {
-                racc[v][k] = Ops<T>::madd(racc[v][k], a, xj);
-                c = Ops<T>::maddc(c, a, xi[v][k]);
-              }
+        for (int k = 0; k < VPL; ++k) {
+          const long long r = row_of(r0, v, lane, k);
+          bool valid = true;
+          if (DIAG) valid = r < n && (upper ? r <= j : r >= j);
+          if (valid) {
+            T a = Ops<T>::load(col + r);
+            if (DIAG && r == j) {
+              racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::diag(a), xj);
+            } else {
+              racc[v][k] = Ops<T>::madd(racc[v][k], a, xj);
+              c = Ops<T>::maddc(c, a, xi[v][k]);
             }
           }
-        cp[u] = c;
-      }
-      emit_columns(cp, lane, cnt, wc_row, j0);
+        }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) c = Ops<T>::add(c, Ops<T>::shfl_xor(c, o));
+      if (lane == 0) wc_row[j] = c;
     }
   }
 };
@@ -184,16 +435,43 @@ struct WarpTile {
 // ----------------------------------------------------------------------------
 // main kernel
 // ----------------------------------------------------------------------------
-template <class T, int VR, int U, int WARPS, bool ALIGNED>
+// PIPE (see enum Pipe) applies to 16-byte aligned matrices; otherwise
+// off-diagonal columns are read with element loads.  Dynamic shared memory
+// = WARPS * RingLayout::WARP_BYTES.
+template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED>
 __global__ void __launch_bounds__(WARPS * 32)
 symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, long long incx,
-          T* __restrict__ Wc, T* __restrict__ Wr) {
+          T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
+          unsigned long long limit_ns, uint32_t extra_tx) {
   using Tile = WarpTile<T, VR, U>;
+  using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
+  constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
+  constexpr bool ASYNC = (PIPE == kPipeLdgsts) && ALIGNED;
   constexpr int VPL = Tile::VPL;
   constexpr int NB = Tile::NB;
+  // let the finaliser (launched as a programmatic dependent) get scheduled as
+  // blocks of this grid retire; it waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
+  const int wl = threadIdx.x >> 5;
   const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   if (w >= p.W) return;
+
+  Ring rg{0u, 0u, 0, 0u, extra_tx};
+  if (RING || ASYNC) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* base = smem + (size_t)wl * Lay::WARP_BYTES;
+    rg.data = smem_addr(base);
+    rg.bars = smem_addr(base + Lay::DATA_BYTES);
+  }
+  if (RING) {
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < (STAGES > 0 ? STAGES : 1); ++s) mbar_init(rg.bars + 8u * s, 1);
+      mbar_init_fence();
+    }
+    __syncwarp();
+  }
 
   long long s = plan_wstart(p, w);
   const long long send = plan_wstart(p, w + 1);
@@ -223,21 +501,38 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     const long long dA = r0;
     const long long dB = (r0 + NB < n) ? r0 + NB : n;   // diagonal tile columns [dA, dB)
     const bool complete = (r0 + NB <= n);               // all NB rows exist
+    // the dense (off-diagonal, complete) column range of this segment
+    long long b0, b1;
     if (p.upper) {
       // diagonal tile first, then the off-diagonal columns (rows all stored)
       const long long a0 = ja > dA ? ja : dA, a1 = jb < dB ? jb : dB;
       if (a0 < a1) t.template masked_cols<true>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, 1);
-      const long long b0 = ja > dB ? ja : dB;
-      if (b0 < jb) t.template dense_cols<ALIGNED>(A, lda, x, incx, r0, b0, jb, wc_row, lane);
+      b0 = ja > dB ? ja : dB;
+      b1 = jb;
     } else {
-      // off-diagonal columns first, then the diagonal tile
-      const long long b1 = jb < dA ? jb : dA;
-      if (ja < b1) {
-        if (complete)
-          t.template dense_cols<ALIGNED>(A, lda, x, incx, r0, ja, b1, wc_row, lane);
-        else
-          t.template masked_cols<true>(A, lda, x, incx, r0, ja, b1, wc_row, lane, n, 0);
+      b0 = ja;
+      b1 = jb < dA ? jb : dA;
+      if (!complete && b0 < b1) {
+        t.template masked_cols<true>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
+        b1 = b0;
       }
+    }
+    if (b0 < b1) {
+      if (RING) {
+        if (!t.template dense_cols_ring<(STAGES > 0 ? STAGES : 1)>(rg, A, lda, x, incx, r0, b0, b1,
+                                                                   wc_row, lane, limit_ns)) {
+          if (lane == 0) atomicMax(status, epoch);
+          return;
+        }
+      } else if (ASYNC) {
+        t.template dense_cols_ldgsts<(STAGES > 1 ? STAGES : 2)>(rg.data, A, lda, x, incx, r0, b0,
+                                                                b1, wc_row, lane);
+      } else {
+        t.template dense_cols<ALIGNED>(A, lda, x, incx, r0, b0, b1, wc_row, lane);
+      }
+    }
+    if (!p.upper) {
+      // off-diagonal columns done, then the diagonal tile
       const long long a0 = ja > dA ? ja : dA;
       if (a0 < jb) t.template masked_cols<true>(A, lda, x, incx, r0, a0, jb, wc_row, lane, n, 0);
     }
@@ -258,28 +553,49 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
 // ----------------------------------------------------------------------------
 enum FinalMode { kFull = 0, kBetaZero = 1, kAlphaZero = 2, kZero = 3 };
 
+constexpr int kFinParts = 8;    // partial sums per output element
+constexpr int kFinCols = 32;    // output elements per block
+
+// Block (kFinParts x kFinCols threads) handles 32 consecutive outputs, which
+// lie in one block row K because NB is a multiple of 32.  Thread (part, c)
+// adds, in increasing order, the column partials of block rows I = I0+part,
+// I0+part+kFinParts, ... and the row-partial slots q = part, part+kFinParts,
+// ...; the kFinParts sums are then added in part order.  The order depends
+// only on (n, NB, W), never on timing.
 template <class T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFinParts * kFinCols)
 symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alpha, T beta,
-              int mode, T* __restrict__ y, long long incy) {
-  const long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= p.n) return;
-  T* yj = y + j * incy;
+              int mode, T* __restrict__ y, long long incy, const int* status, int epoch) {
+  __shared__ T part[kFinParts][kFinCols];
+  // wait until the preceding grid on the stream (the main kernel) has
+  // completed and its writes are visible (no-op without a programmatic launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int c = threadIdx.x % kFinCols;
+  const int pp = threadIdx.x / kFinCols;
+  const long long j = (long long)blockIdx.x * kFinCols + c;
+  const bool live = j < p.n;
   T s = Ops<T>::zero();
-  if (mode == kFull || mode == kBetaZero) {
+  if (live && (mode == kFull || mode == kBetaZero)) {
     const int K = (int)(j / p.NB);
     const int jj = (int)(j - (long long)K * p.NB);
     const int I0 = p.upper ? 0 : K;
     const int I1 = p.upper ? K : p.nb - 1;
     const T* wc = Wc + j;
-#pragma unroll 8
-    for (int I = I0; I <= I1; ++I) s = Ops<T>::add(s, wc[(long long)I * p.n]);
+#pragma unroll 4
+    for (int I = I0 + pp; I <= I1; I += kFinParts) s = Ops<T>::add(s, wc[(long long)I * p.n]);
     const long long rs = plan_rowstart(p, K);
     const int q0 = plan_owner(p, rs);
     const int nq = plan_owner(p, rs + plan_rowlen(p, K) - 1) - q0 + 1;
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
-    for (int q = 0; q < nq; ++q) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
+    for (int q = pp; q < nq; q += kFinParts) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
   }
+  part[pp][c] = s;
+  __syncthreads();
+  if (pp != 0 || !live) return;
+  s = part[0][c];
+#pragma unroll
+  for (int k = 1; k < kFinParts; ++k) s = Ops<T>::add(s, part[k][c]);
+  T* yj = y + j * incy;
   T out;
   if (mode == kFull)
     out = Ops<T>::add(Ops<T>::mul(alpha, s), Ops<T>::mul(beta, *yj));
@@ -289,6 +605,7 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
     out = Ops<T>::mul(beta, *yj);
   else
     out = Ops<T>::zero();
+  if (status != nullptr && *status == epoch) out = Ops<T>::nan();   // the main kernel gave up
   *yj = out;
 }
 

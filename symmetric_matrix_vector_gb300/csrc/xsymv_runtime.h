@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 namespace xsymv {
 
@@ -17,7 +18,16 @@ bool current_device(int* dev, int* sm_count);
 // buffer of at least `bytes` for (current device, stream, slot); nullptr and
 // *status set on failure.  Slot 0: the kernels' workspace; slot 1: device
 // copies of host operands for the host-buffer entry points.
-void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot = 0);
+// For slot 0 the first 256 bytes (the status header) are zeroed when the
+// buffer is allocated, and *epoch receives a fresh call number (> 0) that the
+// kernels write to the status word if they give up on a wait.
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch);
+
+// time limit of every bounded wait in the kernels
+unsigned long long wait_limit_ns();
+// extra bytes announced on every ring barrier: 0, except when a test makes
+// the waits run out on purpose
+uint32_t test_extra_tx();
 
 // bytes moved by the last host-buffer call
 void note_host_traffic(long long h2d, long long d2h);

@@ -6,10 +6,14 @@
 
 namespace xsymv {
 static const Variant<float> kVariants_s[] = {
-    XSYMV_VARIANT(float, 1, 8, 8),
-    XSYMV_VARIANT(float, 1, 16, 4),
-    XSYMV_VARIANT(float, 2, 4, 8),
-    XSYMV_VARIANT(float, 1, 4, 8),
+    XSYMV_REG(float, 1, 4, 8),
+    XSYMV_REG(float, 1, 8, 8),
+    XSYMV_REG(float, 1, 2, 8),
+    XSYMV_REG(float, 1, 4, 4),
+    XSYMV_REG(float, 2, 2, 8),
+    XSYMV_REG(float, 2, 4, 8),
+    XSYMV_ASYNC(float, 1, 4, 4, 8),
+    XSYMV_TMA(float, 1, 8, 3, 8),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv
@@ -59,9 +63,11 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
 // * The first call on a device looks up the array's device address
 //   (cudaGetSymbolAddress, with that device current) and caches it; make
 //   that first call before any stream capture.
-// * Nothing in the array has to start at zero: the main kernel writes every
-//   workspace slot the finaliser then reads.  The array keeps the last
-//   call's contents.
+// * Only the array's first 256 bytes (a status word the kernels set if a
+//   bounded wait runs out) must start at zero; the first call on a device
+//   clears them with cudaMemsetAsync on its stream.  Every other workspace
+//   slot the finaliser reads is written by the main kernel of the same
+//   call.  The array keeps the last call's contents.
 // * All calls share the one array: calls that overlap on the GPU (on
 //   different streams, or from different host threads) race and corrupt
 //   each other's results.  Order them, e.g. on one stream.
@@ -72,12 +78,14 @@ namespace {
 struct NoallocDevice {
   int device;
   void* scratch;
+  int epoch;   // last call number on this device
 };
 std::mutex g_noalloc_mu;
 std::vector<NoallocDevice> g_noalloc_devices;
 
-// device address of g_noalloc_scratch on the current device
-int noalloc_scratch(void** out) {
+// device address of g_noalloc_scratch on the current device and a fresh call
+// number; the first call on a device clears the status header on `stream`
+int noalloc_scratch(void** out, int* epoch, cudaStream_t stream) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) {
@@ -85,19 +93,23 @@ int noalloc_scratch(void** out) {
     return XSYMV_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  for (const NoallocDevice& s : g_noalloc_devices)
+  for (NoallocDevice& s : g_noalloc_devices)
     if (s.device == d) {
+      s.epoch = (s.epoch >= 0x7ffffffe) ? 1 : s.epoch + 1;
       *out = s.scratch;
+      *epoch = s.epoch;
       return XSYMV_OK;
     }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e == cudaSuccess && p != nullptr) e = cudaMemsetAsync(p, 0, 256, stream);
   if (e != cudaSuccess || p == nullptr) {
     xsymv::record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  g_noalloc_devices.push_back(NoallocDevice{d, p});
+  g_noalloc_devices.push_back(NoallocDevice{d, p, 1});
   *out = p;
+  *epoch = 1;
   return XSYMV_OK;
 }
 }  // namespace
@@ -116,17 +128,15 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   cudaStream_t st = current_stream();
   float* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
   const float* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
-  const unsigned fgrid = (unsigned)((n + 255) / 256);
-
   void* scratch = nullptr;
-  int status = noalloc_scratch(&scratch);
+  int epoch = 0;
+  int status = noalloc_scratch(&scratch, &epoch, st);
   if (status) return status;
 
   if (az) {  // y := beta*y, no workspace needed
     Plan p = plan_make(n, 32, upper, 1);
-    symv_finalize<float><<<fgrid, 256, 0, st>>>(p, nullptr, nullptr, alpha, beta,
-                                                 bz ? kZero : kAlphaZero, y0, incy);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_finalize<float>(p, nullptr, nullptr, alpha, beta,
+                                           bz ? kZero : kAlphaZero, y0, incy, nullptr, 0, st);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       return XSYMV_ERR_CUDA;
@@ -140,16 +150,15 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
   if (status) return status;
   if (wl.bytes > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
-  float* Wc = static_cast<float*>(scratch);
-  float* Wr = reinterpret_cast<float*>(static_cast<char*>(scratch) + wl.wc_bytes);
-  const bool aligned =
-      (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (((long long)lda * 4) % 16 == 0);
-  cudaError_t e = wl.variant->launch(wl.plan, A, lda, x0, incx, Wc, Wr, aligned, st);
-  if (e == cudaSuccess) {
-    symv_finalize<float><<<fgrid, 256, 0, st>>>(wl.plan, Wc, Wr, alpha, beta,
-                                                 bz ? kBetaZero : kFull, y0, incy);
-    e = cudaGetLastError();
-  }
+  char* ws = static_cast<char*>(scratch);
+  MainArgs<float> m{wl.plan, A, lda, x0, incx, reinterpret_cast<float*>(ws + wl.wc_off),
+                    reinterpret_cast<float*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
+                    (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (((long long)lda * 4) % 16 == 0),
+                    st};
+  cudaError_t e = wl.variant->launch(m);
+  if (e == cudaSuccess)
+    e = launch_finalize<float>(wl.plan, m.Wc, m.Wr, alpha, beta, bz ? kBetaZero : kFull, y0,
+                               incy, m.status, epoch, st);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return XSYMV_ERR_CUDA;

@@ -65,6 +65,7 @@ template <> struct Ops<float> {
   static constexpr int VPL = 4;
   static constexpr bool HERM = false;
   __device__ __forceinline__ static float zero() { return 0.f; }
+  __device__ __forceinline__ static float nan() { return __int_as_float(0x7fffffff); }
   __device__ __forceinline__ static float add(float a, float b) { return a + b; }
   __device__ __forceinline__ static float mul(float a, float b) { return a * b; }
   // acc + a*b and acc + conj(a)*b
@@ -80,6 +81,7 @@ template <> struct Ops<double> {
   static constexpr int VPL = 2;
   static constexpr bool HERM = false;
   __device__ __forceinline__ static double zero() { return 0.0; }
+  __device__ __forceinline__ static double nan() { return __longlong_as_double(0x7fffffffffffffffll); }
   __device__ __forceinline__ static double add(double a, double b) { return a + b; }
   __device__ __forceinline__ static double mul(double a, double b) { return a * b; }
   __device__ __forceinline__ static double madd(double acc, double a, double b) { return fma(a, b, acc); }
@@ -94,6 +96,7 @@ template <> struct Ops<c32> {
   static constexpr int VPL = 2;
   static constexpr bool HERM = true;
   __device__ __forceinline__ static c32 zero() { return c32{0.f, 0.f}; }
+  __device__ __forceinline__ static c32 nan() { return c32{Ops<float>::nan(), Ops<float>::nan()}; }
   __device__ __forceinline__ static c32 add(c32 a, c32 b) { return c32{a.re + b.re, a.im + b.im}; }
   __device__ __forceinline__ static c32 mul(c32 a, c32 b) {
     return c32{a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
@@ -131,6 +134,7 @@ template <> struct Ops<c64> {
   static constexpr int VPL = 1;
   static constexpr bool HERM = true;
   __device__ __forceinline__ static c64 zero() { return c64{0.0, 0.0}; }
+  __device__ __forceinline__ static c64 nan() { return c64{Ops<double>::nan(), Ops<double>::nan()}; }
   __device__ __forceinline__ static c64 add(c64 a, c64 b) { return c64{a.re + b.re, a.im + b.im}; }
   __device__ __forceinline__ static c64 mul(c64 a, c64 b) {
     return c64{a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
@@ -166,6 +170,7 @@ template <> struct Ops<dd> {
   static constexpr int VPL = 1;
   static constexpr bool HERM = false;
   __device__ __forceinline__ static dd zero() { return dd{0.0, 0.0}; }
+  __device__ __forceinline__ static dd nan() { return dd{Ops<double>::nan(), Ops<double>::nan()}; }
   __device__ __forceinline__ static dd add(dd a, dd b) { return dd_add(a, b); }
   __device__ __forceinline__ static dd mul(dd a, dd b) { return dd_mul(a, b); }
   __device__ __forceinline__ static dd madd(dd acc, dd a, dd b) { return dd_add(acc, dd_mul(a, b)); }

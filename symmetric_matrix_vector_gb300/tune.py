@@ -1,0 +1,176 @@
+"""Offline tuner: times every compiled kernel variant on the current GPU and
+writes the per-(kind, uplo, n) choice into csrc/xsymv_tuned.h.
+
+The report tunes (Tx, Ty, U) thread-block shapes offline and builds the best
+kernels into its library, with an if-then table over n per GPU
+("CUDA-xSYMV の実装と評価", §3 and Tables I, 2, 3).  The GB300 kernels'
+parameter space is the variant list compiled into libxsymv.so (vectors per
+lane, columns in flight, shared-memory ring depth, warps per block); this
+script measures each one with CUDA events on synthetic problems and keeps the
+fastest per size.
+
+Results are appended to a JSONL file (one line per measurement) and reused on
+a rerun, so an interrupted sweep resumes where it stopped.
+
+    python -m symmetric_matrix_vector_gb300.tune --kinds s --n 8192,16384,32768 \\
+        --results gpurun_out/tune.jsonl --write-header csrc_copy.h
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+
+from . import _build, inputs
+
+DEFAULT_N = {"s": [4096, 8192, 16384, 24576, 32768], "d": [8192, 24576], "c": [8192, 16384],
+             "z": [8192, 16384], "w": [4096, 8192]}
+TUNED_H = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "xsymv_tuned.h")
+INT_MAX = 2147483647
+
+
+def measure(xs, kind, uplo, n, variant, reps, prob):
+    import torch
+
+    assert xs.xsymv_set_variant(kind, variant) == 0
+    try:
+        A, x, y, lda = prob["A"], prob["x"], prob["y"], prob["lda"]
+        alpha = prob["alpha"]
+        beta = prob["beta"]
+        for _ in range(3):
+            xs.check(xs.symv(kind, uplo, n, alpha, A, lda, x, 1, beta, y, 1))
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                xs.check(xs.symv(kind, uplo, n, alpha, A, lda, x, 1, beta, y, 1))
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / reps)
+        return statistics.median(times)
+    finally:
+        xs.xsymv_set_variant(kind, -1)
+
+
+def load_results(path):
+    done = {}
+    if path and os.path.exists(path):
+        with open(path) as f:
+            for line in f:
+                try:
+                    r = json.loads(line)
+                except ValueError:
+                    continue
+                done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
+    return done
+
+
+def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9):
+    import torch
+
+    import symmetric_matrix_vector_gb300 as xs
+
+    _build.build()
+    xs.load()
+    done = load_results(results_path)
+    out = open(results_path, "a") if results_path else None
+    es = inputs.ELEM_BYTES
+    for kind in kinds:
+        for uplo in uplos:
+            for n in sizes.get(kind, DEFAULT_N[kind]):
+                prob = None
+                for v in range(xs.xsymv_variant_count(kind)):
+                    name = xs.xsymv_variant_name(kind, v)
+                    if (kind, uplo, n, name) in done:
+                        continue
+                    if prob is None:
+                        al = {"s": 1.0, "d": 1.0, "c": 1.0, "z": 1.0, "w": (1.0, 0.0)}[kind]
+                        be = {"s": 0.0, "d": 0.0, "c": 0.0, "z": 0.0, "w": (0.0, 0.0)}[kind]
+                        prob = inputs.device_problem(kind, uplo, n, lda=n, alpha=al, beta=be,
+                                                     seed=n)
+                    tri = n * (n + 1) / 2 * es[kind]
+                    reps = int(max(5, min(500, reps_bytes / tri)))
+                    ms = measure(xs, kind, uplo, n, v, reps, prob)
+                    rec = {"kind": kind, "uplo": uplo, "n": n, "variant": v, "variant_name": name,
+                           "ms": ms, "gbs": tri / (ms * 1e-3) / 1e9,
+                           "gpu": torch.cuda.get_device_name()}
+                    done[(kind, uplo, n, name)] = rec
+                    if out:
+                        out.write(json.dumps(rec) + "\n")
+                        out.flush()
+                    print("%s %s n=%6d %-16s %8.4f ms %8.1f GB/s" % (kind, uplo, n, name, ms,
+                                                                     rec["gbs"]), flush=True)
+                del prob
+                torch.cuda.empty_cache()
+    if out:
+        out.close()
+    return done
+
+
+def choose(done):
+    """best variant per (kind, uplo, n) -> table entries with n_max buckets"""
+    best = {}
+    for (kind, uplo, n, _name), r in done.items():
+        key = (kind, uplo, n)
+        if key not in best or r["ms"] < best[key]["ms"]:
+            best[key] = r
+    entries = []
+    for kind in "sdczw":
+        for uplo in ("U", "L"):
+            ns = sorted(n for (k, u, n) in best if k == kind and u == uplo)
+            for i, n in enumerate(ns):
+                n_max = INT_MAX if i + 1 == len(ns) else (n + ns[i + 1]) // 2
+                entries.append((kind, 1 if uplo == "U" else 0, n_max, best[(kind, uplo, n)]))
+    return entries
+
+
+def render_table(entries, kinds_all="sdczw"):
+    lines = ["static const TunedEntry kTuned[] = {"]
+    have = set()
+    for kind, upper, n_max, r in entries:
+        have.add(kind)
+        lines.append("    {'%s', %d, %d, %d},   // %s %.1f GB/s at n=%d" % (
+            kind, upper, n_max, r["variant"], r["variant_name"], r["gbs"], r["n"]))
+    for kind in kinds_all:
+        if kind not in have:
+            lines.append("    {'%s', -1, %d, 0}," % (kind, INT_MAX))
+    lines.append("};")
+    return "\n".join(lines)
+
+
+def write_header(entries, path):
+    with open(TUNED_H) as f:
+        src = f.read()
+    table = render_table(entries)
+    new = re.sub(r"// BEGIN TUNED TABLE\n.*?// END TUNED TABLE",
+                 "// BEGIN TUNED TABLE\n" + table + "\n// END TUNED TABLE", src, flags=re.S)
+    with open(path, "w") as f:
+        f.write(new)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kinds", default="s")
+    ap.add_argument("--n", default="", help="comma-separated sizes (default: per kind)")
+    ap.add_argument("--uplo", default="U,L")
+    ap.add_argument("--results", default="tune_results.jsonl")
+    ap.add_argument("--write-header", default="", help="write the tuned header here")
+    args = ap.parse_args()
+    kinds = [k for k in args.kinds.split(",") if k]
+    sizes = {}
+    if args.n:
+        ns = [int(v) for v in args.n.split(",")]
+        sizes = {k: ns for k in kinds}
+    done = sweep(kinds, sizes, args.uplo.split(","), args.results)
+    if args.write_header:
+        write_header(choose(done), args.write_header)
+        print("wrote", args.write_header)
+
+
+if __name__ == "__main__":
+    main()

@@ -69,7 +69,7 @@ def test_argument_errors_on_host(lib, kind):
 
 
 def test_status_strings(lib):
-    for st in (0, 1, 2, 5, 7, 10, -1, -2, -3, -4):
+    for st in (0, 1, 2, 5, 7, 10, -1, -2, -3, -4, -5, -6):
         assert xs.xsymv_status_string(st) != "unknown status"
     assert xs.xsymv_status_string(12345) == "unknown status"
 
@@ -79,7 +79,7 @@ def test_variants_introspection(lib):
         cnt = xs.xsymv_variant_count(kind)
         assert cnt >= 1
         for i in range(cnt):
-            assert re.fullmatch(r"vr\d+_u\d+_w\d+", xs.xsymv_variant_name(kind, i))
+            assert re.fullmatch(r"vr\d+_u\d+_[rta]\d+_w\d+", xs.xsymv_variant_name(kind, i))
         assert xs.xsymv_variant_name(kind, cnt) is None
         assert xs.xsymv_set_variant(kind, cnt) == -4
         assert xs.xsymv_set_variant(kind, -1) == 0

@@ -291,3 +291,35 @@ def test_host_buffer_entry(o, lib, kind, uplo):
         assert d2h == n * es
         # only the triangle (plus a few percent in panel corners) travels
         assert h2d <= (n * (n + 1) / 2 * 1.05 + 2 * n + 64 * n) * es
+
+
+def test_bounded_wait_reports_timeout(lib):
+    """A bulk-copy barrier that never completes (test hook: 16 bytes are
+    announced that never arrive) makes the kernel's bounded waits run out:
+    the call's y becomes NaN, the host reads XSYMV_ERR_TIMEOUT, and the next
+    normal call on the same context is correct again."""
+    import torch
+
+    p = inputs.make_problem("s", "U", 1500, lda=1500, alpha=1.0, beta=0.0, seed=2)
+    dp = DeviceProblem(p)
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+    # the waits live in the bulk-copy (TMA) ring variants
+    tma = [v for v in range(lib.xsymv_variant_count("s")) if "_t" in lib.xsymv_variant_name("s", v)]
+    assert tma and lib.xsymv_set_variant("s", tma[0]) == 0
+    st, good = dp.run()
+    assert st == 0 and lib.xsymv_sync_status() == 0
+    try:
+        lib.xsymv_set_wait_limit(2_000_000)          # 2 ms
+        lib.xsymv_test_stall(True)
+        st, bad = dp.run()
+        assert st == 0
+        assert lib.xsymv_sync_status() == -6
+        yb = from_device(bad, p.y)
+        assert np.all(np.isnan(yb))
+    finally:
+        lib.xsymv_test_stall(False)
+        lib.xsymv_set_wait_limit(0)
+    st, again = dp.run()
+    lib.xsymv_set_variant("s", -1)
+    assert st == 0 and lib.xsymv_sync_status() == 0
+    assert bool((again == good).all())
