@@ -194,12 +194,12 @@ XSYMV_API long long xsymv_launch_count(void);
 /* ---- kernel variants: the tuner's parameter space ----------------------- */
 
 /* kind: 's', 'd', 'c', 'z' or 'w'.  Number of compiled variants (0 for an
- * unknown kind) and the name of variant index: "vr<VR>_u<U>_<p><S>_w<W>" =
- * 16-byte vectors per lane (the tile edge is 32 lanes x VR vectors), columns
- * per chunk, how off-diagonal columns reach the arithmetic (p = r: loads
- * into registers; t: a per-warp shared-memory ring of S chunks filled by
- * bulk (TMA) copies; a: the same ring filled by per-lane cp.async copies)
- * and warps per block. */
+ * unknown kind) and the name of variant index: "vr<VR>_u<U>_<p><S>_w<W>"
+ * with an optional "_b<B>" = 16-byte vectors per lane (the tile edge is 32
+ * lanes x VR vectors), columns per chunk, how off-diagonal columns reach the
+ * arithmetic (p = r: 16-byte loads into registers; t: a per-warp
+ * shared-memory ring of S chunks filled by bulk (TMA) copies), warps per
+ * block, and a register cap that fits B blocks per SM. */
 XSYMV_API int xsymv_variant_count(char kind);
 XSYMV_API const char *xsymv_variant_name(char kind, int index);
 

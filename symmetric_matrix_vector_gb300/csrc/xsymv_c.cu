@@ -3,11 +3,13 @@
 
 namespace xsymv {
 static const Variant<c32> kVariants_c[] = {
-    XSYMV_REG(c32, 2, 4, 8),
-    XSYMV_REG(c32, 2, 2, 8),
     XSYMV_REG(c32, 1, 4, 8),
+    XSYMV_REG(c32, 2, 2, 8),
+    XSYMV_REG(c32, 2, 4, 8),
     XSYMV_REG(c32, 1, 8, 8),
-    XSYMV_ASYNC(c32, 1, 8, 4, 4),
+    XSYMV_REG_MB(c32, 1, 4, 8, 5),
+    XSYMV_REG_MB(c32, 1, 2, 8, 5),
+    XSYMV_REG_MB(c32, 2, 2, 8, 5),
     XSYMV_TMA(c32, 1, 8, 4, 4),
 };
 static_assert(sizeof(c32) == sizeof(xsymv_c32), "C-ABI type layout");

@@ -3,11 +3,12 @@
 
 namespace xsymv {
 static const Variant<double> kVariants_d[] = {
+    XSYMV_REG(double, 4, 2, 8),
     XSYMV_REG(double, 2, 4, 8),
     XSYMV_REG(double, 2, 2, 8),
     XSYMV_REG(double, 1, 4, 8),
-    XSYMV_REG(double, 4, 2, 8),
-    XSYMV_ASYNC(double, 2, 4, 4, 4),
+    XSYMV_REG_MB(double, 2, 2, 8, 5),
+    XSYMV_REG_MB(double, 4, 2, 8, 4),
     XSYMV_TMA(double, 2, 4, 4, 4),
 };
 static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");

@@ -25,7 +25,7 @@ struct MainArgs {
   const T* A;
   long long lda;
   const T* x;      // logical element 0
-  long long incx;
+  int incx;
   T* Wc;
   T* Wr;
   int* status;
@@ -42,6 +42,7 @@ struct Variant {
   int warps;   // warps per block
   int stages;  // shared-memory ring depth
   int pipe;    // enum Pipe
+  int waves;   // warps launched = waves x the warps that fit on the GPU at once
   cudaError_t (*launch)(const MainArgs<T>&);
   int (*ctas_per_sm)();
 };
@@ -51,13 +52,13 @@ constexpr int ring_smem_bytes() {
   return WARPS * RingLayout<T, VR, U, S, P>::WARP_BYTES;
 }
 
-template <class T, int VR, int U, int S, int P, int WARPS>
+template <class T, int VR, int U, int S, int P, int WARPS, int MB>
 cudaError_t launch_main(const MainArgs<T>& a) {
   constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
   static bool configured = false;
   if (!configured) {
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true>,
+      cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
     }
@@ -67,24 +68,24 @@ cudaError_t launch_main(const MainArgs<T>& a) {
   const unsigned long long limit = wait_limit_ns();
   const uint32_t extra = test_extra_tx();
   if (a.aligned)
-    symv_main<T, VR, U, S, P, WARPS, true><<<grid, WARPS * 32, smem, a.stream>>>(
+    symv_main<T, VR, U, S, P, WARPS, true, MB><<<grid, WARPS * 32, smem, a.stream>>>(
         a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   else
-    symv_main<T, VR, U, S, P, WARPS, false><<<grid, WARPS * 32, 0, a.stream>>>(
+    symv_main<T, VR, U, S, P, WARPS, false, MB><<<grid, WARPS * 32, 0, a.stream>>>(
         a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   return cudaGetLastError();
 }
 
-template <class T, int VR, int U, int S, int P, int WARPS>
+template <class T, int VR, int U, int S, int P, int WARPS, int MB>
 int ctas_per_sm() {
   static int cached = 0;
   if (!cached) {
     constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
     int b = 0;
     if (smem > 48 * 1024)
-      cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true>,
+      cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true, MB>,
                                                       WARPS * 32, smem) != cudaSuccess || b < 1) {
       cudaGetLastError();
       b = 1;
@@ -94,16 +95,23 @@ int ctas_per_sm() {
   return cached;
 }
 
-// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>, pipe r = registers,
-// t = bulk-copy (TMA) ring, a = cp.async ring.
-#define XSYMV_VARIANT_P(T, VR, U, S, P, L, W)                                             \
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>],
+// pipe r = loads into registers, t = bulk-copy (TMA) ring of STAGES chunks
+// per warp; _b<MINB>: registers capped so that MINB blocks fit on an SM;
+// _x<WAVES>: that many waves of blocks instead of one resident wave.
+#define XSYMV_VARIANT_P(T, VR, U, S, P, L, W, MB, X, SUF)                                 \
   Variant<T> {                                                                            \
-    "vr" #VR "_u" #U "_" L #S "_w" #W, 32 * Ops<T>::VPL * (VR), (W), (S), (P),           \
-        &launch_main<T, VR, U, S, P, W>, &ctas_per_sm<T, VR, U, S, P, W>                  \
+    "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
+        &launch_main<T, VR, U, S, P, W, MB>, &ctas_per_sm<T, VR, U, S, P, W, MB>          \
   }
-#define XSYMV_REG(T, VR, U, W) XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W)
-#define XSYMV_TMA(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeBulk, "t", W)
-#define XSYMV_ASYNC(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeLdgsts, "a", W)
+#define XSYMV_REG(T, VR, U, W) XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, 0, 1, "")
+#define XSYMV_REG_MB(T, VR, U, W, MB) \
+  XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, MB, 1, "_b" #MB)
+// X waves of warps: each warp gets 1/X of a resident warp's share and the
+// hardware starts new blocks as earlier ones finish
+#define XSYMV_REG_MBX(T, VR, U, W, MB, X) \
+  XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, MB, X, "_b" #MB "_x" #X)
+#define XSYMV_TMA(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeBulk, "t", W, 0, 1, "")
 
 template <class T>
 cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, T alpha, T beta, int mode,
@@ -170,7 +178,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   int dev = 0, sms = 0;
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
   const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n)];
-  const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps;
+  const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps * v->waves;
   out->plan = plan_make(n, v->NB, upper, wmax);
   out->variant = v;
   out->wc_off = kHeaderBytes;

@@ -14,30 +14,32 @@
 //                  segments (see xsymv_plan.h).  A column segment is the
 //                  NB-row piece of one matrix column inside one block row:
 //                  the 32 lanes cover its NB rows (VR 16-byte vectors per
-//                  lane), U columns at a time.  Off-diagonal columns travel
-//                  HBM -> shared memory by bulk asynchronous copies
-//                  (cp.async.bulk, the TMA engine) into a ring of STAGES
-//                  chunks per warp, completed on mbarriers, so several chunks
-//                  are in flight while the warp computes; without 16-byte
-//                  alignment they are read with element loads instead.  Row
-//                  terms stay in the lane's registers for the whole block row
-//                  (each lane owns its rows); column terms are summed across
-//                  the 32 lanes with a butterfly reduce-scatter of the U
-//                  columns and written to the workspace.  The diagonal tile
-//                  goes through the same arithmetic with a triangle mask: its
-//                  stored part is read once and contributes to both sides,
-//                  which is what the report's mirrored copy in shared memory
-//                  (part two) achieves.
+//                  lane), U columns at a time.  Off-diagonal columns are read
+//                  either straight into registers (kPipeRegisters) or through
+//                  a per-warp shared-memory ring filled by bulk asynchronous
+//                  copies (cp.async.bulk, the TMA engine) completed on
+//                  mbarriers (kPipeBulk).  Row terms stay in the lane's
+//                  registers for the whole block row (each lane owns its
+//                  rows); column terms are summed across the 32 lanes with a
+//                  butterfly reduce-scatter of the U columns and written to
+//                  the workspace.  The diagonal tile goes through the same
+//                  arithmetic with a triangle mask: its stored part is read
+//                  once and contributes to both sides, which is what the
+//                  report's mirrored copy in shared memory (part two)
+//                  achieves.
 //   symv_finalize  For every output element, sums the workspace slots of its
 //                  row in a fixed order and applies y = alpha*s + beta*y (the
 //                  report's part three and beta scaling).  No atomic
 //                  operation touches data, so results are bit-identical from
 //                  run to run.
 //
-// Every wait on an mbarrier has a time limit.  A wait that runs out marks the
-// call failed (status word := the call's epoch), waits (again with a limit)
-// for the warp's copies still in flight and leaves the kernel; the finaliser
-// then writes NaN to y and the host can read the status.
+// On GB300 the register path is the faster one for SSYMV/CHEMV: with about
+// 48 registers per thread, 40 warps per SM keep enough 16-byte loads in
+// flight to run near the copy bandwidth.  Every wait of the bulk-copy ring
+// on an mbarrier has a time limit.  A wait that runs out marks the call
+// failed (status word := the call's epoch), waits (again with a limit) for
+// the warp's copies still in flight and leaves the kernel; the finaliser then
+// writes NaN to y and the host can read the status.
 #pragma once
 
 #include "xsymv_plan.h"
@@ -88,18 +90,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// per-thread asynchronous 16-byte copy HBM -> shared (LDGSTS, L2 only)
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// wait until at most N of this thread's committed groups are still pending
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 r;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -107,6 +97,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "r"(addr));
   return r;
 }
+
 // Wait for phase `parity` of the mbarrier, giving up after about limit_ns.
 // The limit is counted in SM clock cycles (at most 2 per ns, i.e. a clock of
 // up to 2 GHz; a slower clock only lengthens the wait), read every 256 tries.
@@ -151,17 +142,16 @@ __device__ __forceinline__ T reduce_scatter(T (&v)[U], int lane) {
 enum Pipe {
   kPipeRegisters = 0,   // 16-byte loads straight into registers, U columns at a time
   kPipeBulk = 1,        // per-warp shared-memory ring filled by cp.async.bulk (TMA) copies
-  kPipeLdgsts = 2,      // per-warp shared-memory ring filled by per-lane cp.async copies
 };
 
-// Per-warp ring of STAGES chunks in shared memory; chunk = U column segments
-// of NB elements (plus one mbarrier per stage for the bulk-copy ring).
+// Per-warp ring of STAGES chunks in shared memory (bulk-copy pipe only);
+// chunk = U column segments of NB elements, plus one mbarrier per stage.
 template <class T, int VR, int U, int STAGES, int PIPE>
 struct RingLayout {
   static constexpr int NB = 32 * Ops<T>::VPL * VR;
   static constexpr int COL_BYTES = NB * (int)sizeof(T);
   static constexpr int STAGE_BYTES = U * COL_BYTES;
-  static constexpr int DATA_BYTES = PIPE != kPipeRegisters ? STAGES * STAGE_BYTES : 0;
+  static constexpr int DATA_BYTES = PIPE == kPipeBulk ? STAGES * STAGE_BYTES : 0;
   static constexpr int BAR_BYTES = PIPE == kPipeBulk ? ((STAGES * 8 + 15) / 16) * 16 : 0;
   static constexpr int WARP_BYTES = DATA_BYTES + BAR_BYTES;
 };
@@ -184,15 +174,15 @@ struct WarpTile {
   T xi[VR][VPL];
   T racc[VR][VPL];
 
-  __device__ __forceinline__ static long long row_of(long long r0, int v, int lane, int k) {
-    return r0 + (long long)(v * 32 + lane) * VPL + k;
+  // row held by (vector v, element k) of this lane, relative to the block row
+  __device__ __forceinline__ static int lane_row(int v, int lane, int k) {
+    return (v * 32 + lane) * VPL + k;
   }
 
-  // row terms into racc; column terms reduced over the warp and written for
-  // the cnt valid columns j0 .. j0+cnt-1 (a[u] = column j0+u, xl on lane u =
-  // x(j0+u))
-  __device__ __forceinline__ void accumulate(T (&a)[U][VR][VPL], T xl, int cnt, T* wc_row,
-                                             long long j0, int lane) {
+  // row terms into racc; column terms reduced over the warp and written to
+  // wc[0 .. cnt) (a[u] = column u of the chunk, xl on lane u = its x)
+  __device__ __forceinline__ void accumulate(T (&a)[U][VR][VPL], T xl, int cnt, T* wc,
+                                             int lane) {
     T cp[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -209,42 +199,53 @@ struct WarpTile {
     }
     T red = reduce_scatter<T, U>(cp, lane);
     const int uo = lane >> (5 - H);
-    if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc_row[j0 + uo] = red;
+    if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc[uo] = red;
   }
 
   // Columns [ja, jb) of the block row at r0, all NB rows stored, read with
   // 16-byte vector loads (ALIGNED) or element loads straight into registers.
+  // The loop keeps only running pointers and a 32-bit count live.
   template <bool ALIGNED>
   __device__ __forceinline__ void dense_cols(const T* __restrict__ A, long long lda,
-                                             const T* __restrict__ x, long long incx, long long r0,
+                                             const T* __restrict__ x, int incx, long long r0,
                                              long long ja, long long jb, T* wc_row, int lane) {
-    long long j0 = ja;
-    for (; j0 + U <= jb; j0 += U) {
-      const T xl = (lane < U) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
+    const T* col = A + ja * lda + r0 + lane_row(0, lane, 0);   // this lane, column ja
+    const T* xp = x + ja * (long long)incx;
+    T* wc = wc_row + ja;
+    int left = (int)(jb - ja);
+    for (; left >= U; left -= U) {
+      const T xl = (lane < U) ? Ops<T>::load(xp + lane * incx) : Ops<T>::zero();
       T a[U][VR][VPL];
       if (ALIGNED) {
         uint4 raw[U][VR];
+        const T* c = col;
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u) {
 #pragma unroll
-          for (int v = 0; v < VR; ++v)
-            raw[u][v] = ldg_stream16(A + (j0 + u) * lda + row_of(r0, v, lane, 0));
+          for (int v = 0; v < VR; ++v) raw[u][v] = ldg_stream16(c + v * 32 * VPL);
+          c += lda;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int v = 0; v < VR; ++v) Unpack<T>::run(raw[u][v], a[u][v]);
       } else {
+        const T* c = col;
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < U; ++u) {
 #pragma unroll
           for (int v = 0; v < VR; ++v)
 #pragma unroll
-            for (int k = 0; k < VPL; ++k)
-              a[u][v][k] = Ops<T>::load(A + (j0 + u) * lda + row_of(r0, v, lane, k));
+            for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::load(c + v * 32 * VPL + k);
+          c += lda;
+        }
       }
-      accumulate(a, xl, U, wc_row, j0, lane);
+      accumulate(a, xl, U, wc, lane);
+      col += U * lda;
+      xp += U * incx;
+      wc += U;
     }
-    if (j0 < jb) masked_cols<false>(A, lda, x, incx, r0, j0, jb, wc_row, lane, 0, 0);
+    if (left > 0) masked_cols<false>(A, lda, x, incx, r0, jb - left, jb, wc_row, lane, 0, 0);
   }
 
   // issue the bulk copies of chunk c (columns ja + c*U ..) into its stage
@@ -271,7 +272,7 @@ struct WarpTile {
   template <int STAGES>
   __device__ __forceinline__ bool dense_cols_ring(Ring& rg, const T* __restrict__ A,
                                                   long long lda, const T* __restrict__ x,
-                                                  long long incx, long long r0, long long ja,
+                                                  int incx, long long r0, long long ja,
                                                   long long jb, T* wc_row, int lane,
                                                   unsigned long long limit_ns) {
     constexpr int COL_BYTES = NB * (int)sizeof(T);
@@ -321,7 +322,7 @@ struct WarpTile {
         }
       // the stage is refilled only after its values have been used by the
       // arithmetic, so the asynchronous write cannot overtake the reads
-      accumulate(a, xl, cnt, wc_row, j0, lane);
+      accumulate(a, xl, cnt, wc_row + j0, lane);
       __syncwarp();
       if (c + STAGES < nch) ring_fill<STAGES>(rg, c + STAGES, A, lda, r0, ja, jb, lane);
     }
@@ -329,105 +330,55 @@ struct WarpTile {
     return true;
   }
 
-  // Columns [ja, jb) of the block row at r0 (all NB rows stored, 16-byte
-  // aligned), through the warp's ring filled by per-lane cp.async copies:
-  // every lane copies and later reads only its own 16-byte pieces, so the
-  // lanes need no synchronisation; chunk c+STAGES-1 is issued before chunk c
-  // is consumed.
-  template <int STAGES>
-  __device__ __forceinline__ void dense_cols_ldgsts(uint32_t ring, const T* __restrict__ A,
-                                                    long long lda, const T* __restrict__ x,
-                                                    long long incx, long long r0, long long ja,
-                                                    long long jb, T* wc_row, int lane) {
-    constexpr int COL_BYTES = NB * (int)sizeof(T);
-    const long long nch = (jb - ja + U - 1) / U;
-    auto fill = [&](long long c) {
-      if (c < nch) {
-        const int st = (int)(c % STAGES);
-        const long long j0 = ja + c * U;
-        const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (u < cnt)
-#pragma unroll
-            for (int v = 0; v < VR; ++v)
-              cp_async16(ring + (uint32_t)(st * U + u) * COL_BYTES + (uint32_t)(v * 32 + lane) * 16u,
-                         A + (j0 + u) * lda + row_of(r0, v, lane, 0));
-      }
-      cp_async_commit();   // empty groups keep the group count uniform
-    };
-    auto load_x = [&](long long c) -> T {
-      const long long j0 = ja + c * U;
-      return (c < nch && lane < U && j0 + lane < jb) ? Ops<T>::load(x + (j0 + lane) * incx)
-                                                     : Ops<T>::zero();
-    };
-#pragma unroll
-    for (int c = 0; c < STAGES - 1; ++c) fill(c);
-    T x_next = load_x(0);
-    for (long long c = 0; c < nch; ++c) {
-      fill(c + STAGES - 1);
-      const T xl = x_next;
-      x_next = load_x(c + 1);
-      cp_async_wait<STAGES - 1>();   // this lane's copies of chunk c have landed
-      const int st = (int)(c % STAGES);
-      const long long j0 = ja + c * U;
-      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
-      T a[U][VR][VPL];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int v = 0; v < VR; ++v) {
-          if (u < cnt) {
-            const uint4 raw =
-                lds128(ring + (uint32_t)(st * U + u) * COL_BYTES + (uint32_t)(v * 32 + lane) * 16u);
-            Unpack<T>::run(raw, a[u][v]);
-          } else {
-#pragma unroll
-            for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::zero();
-          }
-        }
-      accumulate(a, xl, cnt, wc_row, j0, lane);
-    }
-    cp_async_wait<0>();
-  }
-
   // Columns [ja, jb) with per-element masks: rows must be < n and, when
   // DIAG, inside the stored triangle (upper: row <= col; lower: row >= col).
   // On the diagonal only the row term is taken (and for a Hermitian matrix
   // only the real part of the element).  Elements outside the mask are
-  // never read.  One column at a time (diagonal tiles and ragged edges are a
-  // small share of the work, and this keeps the kernel's register count low);
-  // each column sum is a full butterfly over the warp, written by lane 0.
+  // never read.  U columns per step, like the dense loop, so that diagonal
+  // tiles keep as many loads in flight and do not hold their warps back;
+  // each element address is a running column pointer plus a constant.
   template <bool DIAG>
   __device__ __forceinline__ void masked_cols(const T* __restrict__ A, long long lda,
-                                              const T* __restrict__ x, long long incx,
-                                              long long r0, long long ja, long long jb,
-                                              T* wc_row, int lane, long long n, int upper) {
+                                              const T* __restrict__ x, int incx, long long r0,
+                                              long long ja, long long jb, T* wc_row, int lane,
+                                              long long n, int upper) {
+    const T* col = A + ja * lda + r0;
+    // rows and columns relative to r0 fit in 32 bits (|j - r0| < n)
+    const int nl = (int)((n - r0) < NB ? (n - r0) : NB);
 #pragma unroll 1
-    for (long long j = ja; j < jb; ++j) {
-      const T xj = Ops<T>::load(x + j * incx);
-      const T* col = A + j * lda;
-      T c = Ops<T>::zero();
+    for (long long j0 = ja; j0 < jb; j0 += U, col += U * lda) {
+      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+      const int jl0 = (int)(j0 - r0);
+      const T xl = (lane < cnt) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
+      T cp[U];
+      const T* c = col;
 #pragma unroll
-      for (int v = 0; v < VR; ++v)
+      for (int u = 0; u < U; ++u, c += lda) {
+        const int jl = jl0 + u;
+        const T xj = Ops<T>::shfl(xl, u);
+        T cu = Ops<T>::zero();
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-          const long long r = row_of(r0, v, lane, k);
-          bool valid = true;
-          if (DIAG) valid = r < n && (upper ? r <= j : r >= j);
-          if (valid) {
-            T a = Ops<T>::load(col + r);
-            if (DIAG && r == j) {
-              racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::diag(a), xj);
-            } else {
-              racc[v][k] = Ops<T>::madd(racc[v][k], a, xj);
-              c = Ops<T>::maddc(c, a, xi[v][k]);
+        for (int v = 0; v < VR; ++v)
+#pragma unroll
+          for (int k = 0; k < VPL; ++k) {
+            const int rl = lane_row(v, lane, k);
+            bool valid = u < cnt;
+            if (DIAG) valid = valid && rl < nl && (upper ? rl <= jl : rl >= jl);
+            if (valid) {
+              T a = Ops<T>::load(c + rl);
+              if (DIAG && rl == jl) {
+                racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::diag(a), xj);
+              } else {
+                racc[v][k] = Ops<T>::madd(racc[v][k], a, xj);
+                cu = Ops<T>::maddc(cu, a, xi[v][k]);
+              }
             }
           }
-        }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) c = Ops<T>::add(c, Ops<T>::shfl_xor(c, o));
-      if (lane == 0) wc_row[j] = c;
+        cp[u] = cu;
+      }
+      T red = reduce_scatter<T, U>(cp, lane);
+      const int uo = lane >> (5 - H);
+      if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc_row[j0 + uo] = red;
     }
   }
 };
@@ -437,16 +388,16 @@ struct WarpTile {
 // ----------------------------------------------------------------------------
 // PIPE (see enum Pipe) applies to 16-byte aligned matrices; otherwise
 // off-diagonal columns are read with element loads.  Dynamic shared memory
-// = WARPS * RingLayout::WARP_BYTES.
-template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED>
-__global__ void __launch_bounds__(WARPS * 32)
-symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, long long incx,
+// = WARPS * RingLayout::WARP_BYTES.  MINB > 0 asks the compiler to fit MINB
+// blocks per SM (a register cap); 0 leaves the choice to the compiler.
+template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
           T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
           unsigned long long limit_ns, uint32_t extra_tx) {
   using Tile = WarpTile<T, VR, U>;
   using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
   constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
-  constexpr bool ASYNC = (PIPE == kPipeLdgsts) && ALIGNED;
   constexpr int VPL = Tile::VPL;
   constexpr int NB = Tile::NB;
   // let the finaliser (launched as a programmatic dependent) get scheduled as
@@ -458,13 +409,11 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
   if (w >= p.W) return;
 
   Ring rg{0u, 0u, 0, 0u, extra_tx};
-  if (RING || ASYNC) {
+  if (RING) {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* base = smem + (size_t)wl * Lay::WARP_BYTES;
     rg.data = smem_addr(base);
     rg.bars = smem_addr(base + Lay::DATA_BYTES);
-  }
-  if (RING) {
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < (STAGES > 0 ? STAGES : 1); ++s) mbar_init(rg.bars + 8u * s, 1);
@@ -473,26 +422,26 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     __syncwarp();
   }
 
-  long long s = plan_wstart(p, w);
+  // this warp's segments [s, send)
   const long long send = plan_wstart(p, w + 1);
+  long long s = plan_wstart(p, w);
   int I = plan_row_of(p, s);
   const long long n = p.n;
   Tile t;
 
   while (s < send) {
     const long long rs = plan_rowstart(p, I);
-    const long long rl = plan_rowlen(p, I);
+    const long long rend = rs + plan_rowlen(p, I);
     const long long cb = plan_colbase(p, I);
     const long long ja = cb + (s - rs);
-    const long long jb = cb + ((send - rs) < rl ? (send - rs) : rl);
-    const int q = w - plan_owner(p, rs);
+    const long long jb = cb + ((send < rend ? send : rend) - rs);
     const long long r0 = (long long)I * NB;
 
 #pragma unroll
     for (int v = 0; v < VR; ++v)
 #pragma unroll
       for (int k = 0; k < VPL; ++k) {
-        const long long r = Tile::row_of(r0, v, lane, k);
+        const long long r = r0 + Tile::lane_row(v, lane, k);
         t.xi[v][k] = (r < n) ? Ops<T>::load(x + r * incx) : Ops<T>::zero();
         t.racc[v][k] = Ops<T>::zero();
       }
@@ -500,50 +449,41 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     T* wc_row = Wc + (long long)I * n;
     const long long dA = r0;
     const long long dB = (r0 + NB < n) ? r0 + NB : n;   // diagonal tile columns [dA, dB)
-    const bool complete = (r0 + NB <= n);               // all NB rows exist
-    // the dense (off-diagonal, complete) column range of this segment
-    long long b0, b1;
-    if (p.upper) {
-      // diagonal tile first, then the off-diagonal columns (rows all stored)
-      const long long a0 = ja > dA ? ja : dA, a1 = jb < dB ? jb : dB;
-      if (a0 < a1) t.template masked_cols<true>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, 1);
-      b0 = ja > dB ? ja : dB;
-      b1 = jb;
-    } else {
-      b0 = ja;
-      b1 = jb < dA ? jb : dA;
-      if (!complete && b0 < b1) {
-        t.template masked_cols<true>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
-        b1 = b0;
-      }
-    }
+    // the diagonal tile's columns of this segment first (masked), then the
+    // off-diagonal ones: upper [max(ja,dB), jb), lower [ja, min(jb,dA)), so
+    // that nothing but the row terms is live after the long dense loop
+    const long long a0 = ja > dA ? ja : dA;
+    const long long a1 = p.upper ? (jb < dB ? jb : dB) : jb;
+    if (a0 < a1)
+      t.template masked_cols<true>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, p.upper);
+    const long long b0 = p.upper ? (ja > dB ? ja : dB) : ja;
+    const long long b1 = p.upper ? jb : (jb < dA ? jb : dA);
     if (b0 < b1) {
-      if (RING) {
+      if (r0 + NB > n) {
+        // a last, incomplete block row (lower storage only): rows masked
+        t.template masked_cols<true>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
+      } else if (RING) {
         if (!t.template dense_cols_ring<(STAGES > 0 ? STAGES : 1)>(rg, A, lda, x, incx, r0, b0, b1,
                                                                    wc_row, lane, limit_ns)) {
           if (lane == 0) atomicMax(status, epoch);
           return;
         }
-      } else if (ASYNC) {
-        t.template dense_cols_ldgsts<(STAGES > 1 ? STAGES : 2)>(rg.data, A, lda, x, incx, r0, b0,
-                                                                b1, wc_row, lane);
       } else {
         t.template dense_cols<ALIGNED>(A, lda, x, incx, r0, b0, b1, wc_row, lane);
       }
     }
-    if (!p.upper) {
-      // off-diagonal columns done, then the diagonal tile
-      const long long a0 = ja > dA ? ja : dA;
-      if (a0 < jb) t.template masked_cols<true>(A, lda, x, incx, r0, a0, jb, wc_row, lane, n, 0);
-    }
 
+    // the row partial goes to slot q of block row I, q = this warp's index
+    // among the warps touching the row
+    const int q = w - plan_owner(p, plan_rowstart(p, I));
     T* wr = Wr + ((long long)I * p.qmax + q) * NB;
 #pragma unroll
     for (int v = 0; v < VR; ++v)
 #pragma unroll
-      for (int k = 0; k < VPL; ++k) wr[(v * 32 + lane) * VPL + k] = t.racc[v][k];
+      for (int k = 0; k < VPL; ++k) wr[Tile::lane_row(v, lane, k)] = t.racc[v][k];
 
-    s = rs + (jb - cb);
+    const long long e = plan_rowstart(p, I) + plan_rowlen(p, I);
+    s = send < e ? send : e;
     ++I;
   }
 }
@@ -553,7 +493,8 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
 // ----------------------------------------------------------------------------
 enum FinalMode { kFull = 0, kBetaZero = 1, kAlphaZero = 2, kZero = 3 };
 
-constexpr int kFinParts = 8;    // partial sums per output element
+constexpr int kFinParts = 8;    // partial sums per output element (the combination order
+                                // below depends on it: changing it changes the rounding)
 constexpr int kFinCols = 32;    // output elements per block
 
 // Block (kFinParts x kFinCols threads) handles 32 consecutive outputs, which
@@ -581,8 +522,16 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
     const int I0 = p.upper ? 0 : K;
     const int I1 = p.upper ? K : p.nb - 1;
     const T* wc = Wc + j;
-#pragma unroll 4
-    for (int I = I0 + pp; I <= I1; I += kFinParts) s = Ops<T>::add(s, wc[(long long)I * p.n]);
+    // loads issued in groups of 8 ahead of the (ordered) additions
+    int I = I0 + pp;
+    for (; I + 7 * kFinParts <= I1; I += 8 * kFinParts) {
+      T v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = wc[(long long)(I + k * kFinParts) * p.n];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s = Ops<T>::add(s, v[k]);
+    }
+    for (; I <= I1; I += kFinParts) s = Ops<T>::add(s, wc[(long long)I * p.n]);
     const long long rs = plan_rowstart(p, K);
     const int q0 = plan_owner(p, rs);
     const int nq = plan_owner(p, rs + plan_rowlen(p, K) - 1) - q0 + 1;

@@ -7,13 +7,15 @@
 namespace xsymv {
 static const Variant<float> kVariants_s[] = {
     XSYMV_REG(float, 1, 4, 8),
-    XSYMV_REG(float, 1, 8, 8),
     XSYMV_REG(float, 1, 2, 8),
+    XSYMV_REG(float, 1, 8, 8),
     XSYMV_REG(float, 1, 4, 4),
     XSYMV_REG(float, 2, 2, 8),
-    XSYMV_REG(float, 2, 4, 8),
-    XSYMV_ASYNC(float, 1, 4, 4, 8),
+    XSYMV_REG_MB(float, 1, 4, 8, 5),
+    XSYMV_REG_MB(float, 1, 2, 8, 5),
+    XSYMV_REG_MB(float, 1, 2, 8, 6),
     XSYMV_TMA(float, 1, 8, 3, 8),
+    XSYMV_REG_MBX(float, 1, 2, 8, 6, 4),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

@@ -6,8 +6,7 @@ static const Variant<dd> kVariants_w[] = {
     XSYMV_REG(dd, 4, 2, 8),
     XSYMV_REG(dd, 2, 2, 8),
     XSYMV_REG(dd, 4, 1, 8),
-    XSYMV_REG(dd, 2, 4, 8),
-    XSYMV_ASYNC(dd, 4, 2, 4, 4),
+    XSYMV_REG_MB(dd, 4, 2, 8, 3),
     XSYMV_TMA(dd, 4, 2, 4, 4),
 };
 static_assert(sizeof(dd) == sizeof(xsymv_dd), "C-ABI type layout");
