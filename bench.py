@@ -395,7 +395,8 @@ def run_ours(args):
         h2d, d2h = xs.xsymv_host_traffic()
         e2e = {"value": world * flops(n) / (ems * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
-               "steps": esteps, "api": "xsymv_s_host (pinned host buffers)"}
+               "steps": esteps,
+               "api": "xsymv_s_host on pinned host buffers (read in place over the host link)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

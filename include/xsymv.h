@@ -120,13 +120,15 @@ XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float *A, int
 
 /* ---- host-buffer variants ----------------------------------------------
  * Same arguments, semantics and status codes as the five calls above, but A,
- * x and y are HOST pointers (pageable or, for full link bandwidth, pinned;
- * device pointers also work).  Each call copies the stored triangle (in
- * column panels, so at most a few percent of the other triangle travels
- * too), x and, when beta != 0, y into library-owned device buffers on the
- * current stream, runs the same kernels, copies the n elements of y back
- * and waits for the stream: y holds the result when the call returns.  The
- * device buffers are kept per (device, stream) for reuse, like the
+ * x and y are HOST pointers (device pointers also work).  When all three are
+ * page-locked (pinned or cudaHostRegister'ed) host memory, the kernels read
+ * A and x and write y in place over the host link (zero-copy; only the
+ * stored triangle crosses the link).  Otherwise each call copies the stored
+ * triangle (in column panels, so at most a few percent of the other
+ * triangle travels too), x and, when beta != 0, y into library-owned device
+ * buffers, runs the same kernels and copies the n elements of y back.  The
+ * call waits for the current stream: y holds the result when it returns.
+ * Staging buffers are kept per (device, stream) for reuse, like the
  * workspace.  On a CUDA error y may be partly written. */
 XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float *A, int lda,
                            const float *x, int incx, float beta, float *y, int incy);
@@ -139,7 +141,8 @@ XSYMV_API int xhemv_z_host(char uplo, int n, xsymv_c64 alpha, const xsymv_c64 *A
 XSYMV_API int xsymv_w_host(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int lda,
                            const xsymv_dd *x, int incx, xsymv_dd beta, xsymv_dd *y, int incy);
 
-/* Bytes the last host-buffer call copied host-to-device and back. */
+/* Bytes the last host-buffer call moved host-to-device and back (copied,
+ * or read / written in place over the link). */
 XSYMV_API int xsymv_host_traffic(long long *h2d_bytes, long long *d2h_bytes);
 
 /* Stream for subsequent calls from any thread (a cudaStream_t; NULL = the

@@ -248,9 +248,26 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
 }
 
 // -------------------------------------------------- host-buffer variant --
-// Copies the stored triangle (in column panels), x and, when beta != 0, y to
-// library-owned device memory on the call's stream, runs symv_entry there,
-// copies y back and waits for the stream.
+// device-side address of p when the GPU can read it in place: page-locked
+// (pinned or registered) host memory, managed or device memory; nullptr for
+// ordinary pageable memory
+inline const void* device_view(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged ||
+      at.type == cudaMemoryTypeDevice)
+    return at.devicePointer;
+  return nullptr;
+}
+
+// With page-locked host buffers the kernels read A and x and write y in
+// place over the host link (zero-copy).  Otherwise the stored triangle (in
+// column panels), x and, when beta != 0, y are copied to library-owned device
+// memory on the call's stream, the kernels run there and y is copied back.
+// Either way the call waits for the stream.
 template <class T>
 int symv_host_entry(const Variant<T>* table, int count, char kind, char uplo, int n, T alpha,
                     const T* hA, int lda, const T* hx, int incx, T beta, T* hy, int incy) {
@@ -265,6 +282,25 @@ int symv_host_entry(const Variant<T>* table, int count, char kind, char uplo, in
 
   const int upper = (uplo == 'U' || uplo == 'u');
   const long long es = (long long)sizeof(T);
+
+  const void* vA = device_view(hA);
+  const void* vx = device_view(hx);
+  const void* vy = device_view(hy);
+  if (vA && vx && vy) {
+    int status = symv_entry<T>(table, count, kind, uplo, n, alpha, static_cast<const T*>(vA), lda,
+                               static_cast<const T*>(vx), incx, beta,
+                               const_cast<T*>(static_cast<const T*>(vy)), incy);
+    if (status) return status;
+    cudaError_t e = cudaStreamSynchronize(current_stream());
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    const long long tri = az ? 0 : ((long long)n * (n + 1) / 2 + n) * es;
+    note_host_traffic(tri + (bz ? 0 : (long long)n * es), (long long)n * es);
+    return XSYMV_OK;
+  }
+
   const long long per16 = 16 / es > 0 ? 16 / es : 1;
   const long long ldd = align_up(n, per16);          // 16-byte aligned columns
   const long long a_bytes = align_up(ldd * n * es, 256);

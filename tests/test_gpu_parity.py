@@ -293,6 +293,35 @@ def test_host_buffer_entry(o, lib, kind, uplo):
         assert h2d <= (n * (n + 1) / 2 * 1.05 + 2 * n + 64 * n) * es
 
 
+@pytest.mark.parametrize("kind", KINDS)
+def test_host_buffer_entry_pinned_zero_copy(o, lib, kind):
+    """with page-locked host buffers the kernels read A, x and write y in
+    place; the result is bitwise the device-buffer result"""
+    import torch
+
+    al, be = SCAL[kind]
+    n = 777
+    p = inputs.make_problem(kind, "L", n, lda=n + 4, alpha=al, beta=be, incx=2, incy=-1, seed=41)
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).pin_memory()
+
+    hA, hx, hy = pinned(p.A), pinned(p.x), pinned(p.y)
+    st = lib.symv_host(kind, "L", n, al, hA.data_ptr(), p.lda, hx.data_ptr(), 2, be,
+                       hy.data_ptr(), -1)
+    assert st == 0
+    y = hy.numpy().view(p.y.dtype).reshape(p.y.shape)
+    err, _ = errors(o, p, y)
+    assert np.max(err) <= TOL[kind]
+    dp = DeviceProblem(p)
+    st, yd = dp.run()
+    assert st == 0
+    assert np.array_equal(from_device(yd, p.y).view(np.uint8), y.view(np.uint8))
+    h2d, d2h = lib.xsymv_host_traffic()
+    es = p.A.itemsize * (2 if kind == "w" else 1)
+    assert d2h == n * es and h2d == (n * (n + 1) // 2 + 2 * n) * es
+
+
 def test_bounded_wait_reports_timeout(lib):
     """A bulk-copy barrier that never completes (test hook: 16 bytes are
     announced that never arrive) makes the kernel's bounded waits run out:
