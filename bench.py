@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true", help="skip the n = 8K..32K sweep")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kinds", action="store_true",
+                    help="skip the one-shot measurements of DSYMV, CHEMV, ZHEMV, WSYMV")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -175,6 +177,71 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(value: float, dist, device="cuda") -> float:
+    """The largest value over all ranks (for times: the slowest rank)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rate(world: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job GFLOP/s when each of `world` ranks runs its own replica and
+    the slowest rank takes ms_per_step per step."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e9
+
+
+# per kind: (workload name, flops per call / n^2, fp64 instructions per stored element)
+KIND_WORKLOADS = {
+    "d": ("dsymv", 2, 2), "c": ("chemv", 8, 0), "z": ("zhemv", 8, 8), "w": ("wsymv", 2, 57),
+}
+
+
+def measure_kinds(xs, inputs, torch, peaks, reps=10):
+    """One timed measurement per other kind at its workload size (whole
+    calls, CUDA events); HBM roofline for c, FP64 ALU roofline for d, z, w."""
+    out = []
+    for kind, (name, fl, f64) in KIND_WORKLOADS.items():
+        spec = {"dsymv": ("L", 24576, dict(dist="normal", diag_shift=4.0), -0.75, 2.0, 7),
+                "chemv": ("U", 16384, {}, complex(1, 0.5), complex(0.5, -0.25), 11),
+                "zhemv": ("U", 16384, {}, complex(1, 0.5), complex(0.5, -0.25), 11),
+                "wsymv": ("L", 8192, {}, (1.0, 0.0), (1.0, 0.0), 13)}[name]
+        uplo, n, kw, al, be, seed = spec
+        pr = inputs.device_problem(kind, uplo, n, lda=n, alpha=al, beta=be, seed=seed, **kw)
+        A, x, y = pr["A"], pr["x"], pr["y"]
+        for _ in range(3):
+            xs.check(xs.symv(kind, uplo, n, al, A, n, x, 1, be, y, 1))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            xs.check(xs.symv(kind, uplo, n, al, A, n, x, 1, be, y, 1))
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        elems = n * (n + 1) / 2
+        gbs = elems * inputs.ELEM_BYTES[kind] / (ms * 1e-3) / 1e9
+        rec = {"kind": kind, "workload": "%s n=%d uplo=%s lda=n" % (name, n, uplo), "ms": ms,
+               "gflops": fl * n * n / (ms * 1e-3) / 1e9, "gbs": gbs,
+               "variant": xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))}
+        if f64:
+            issue = peaks["fp64_tflops"] * 1e12 / 2          # FP64 instructions per second
+            rec["roofline"] = {"bound": "alu", "unit": "FP64 inst/s",
+                               "achieved": elems * f64 / (ms * 1e-3), "peak": issue,
+                               "frac": elems * f64 / (ms * 1e-3) / issue,
+                               "per_element": f64, "peak_source": "same-run FMA probe"}
+        else:
+            rec["roofline"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs,
+                               "peak": peaks["hbm"], "frac": gbs / peaks["hbm"]}
+        out.append(rec)
+        del pr, A, x, y
+        torch.cuda.empty_cache()
+    return out
 
 
 def dist_info():
@@ -301,13 +368,9 @@ def run_ours(args):
     barrier()
     launches = xs.xsymv_launch_count() - l0
     clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
     ms_per_step = ms / args.steps
-    value = world * flops(n) / (ms_per_step * 1e-3) / 1e9
+    value = replica_rate(world, flops(n), ms_per_step)
 
     # ---- timed region 2: per-kernel durations via the library's events
     xs.xsymv_timing_enable(True)
@@ -387,16 +450,16 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = e0.elapsed_time(e1) / esteps
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1) / esteps, dist)
         h2d, d2h = xs.xsymv_host_traffic()
-        e2e = {"value": world * flops(n) / (ems * 1e-3) / 1e9, "unit": UNIT,
+        e2e = {"value": replica_rate(world, flops(n), ems), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
                "steps": esteps,
                "api": "xsymv_s_host on pinned host buffers (read in place over the host link)"}
+
+    kinds = []
+    if rank == 0 and not args.no_kinds and probes:
+        kinds = measure_kinds(xs, inputs, torch, {"hbm": peak, **probes})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -418,6 +481,7 @@ def run_ours(args):
             "hbm_gbs": triangle_bytes(n) / (ms_per_step * 1e-3) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(), "gpu_launches": launches, "sweep": sweep,
+            "kinds": kinds,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -515,14 +515,25 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
   const int pp = threadIdx.x / kFinCols;
   const long long j = (long long)blockIdx.x * kFinCols + c;
   const bool live = j < p.n;
+  T* yj = y + j * incy;
+  // y, and the first row-partial slot, are loaded up front so that their
+  // latency overlaps the column-partial loads
+  const bool need_y = live && pp == 0 && (mode == kFull || mode == kAlphaZero);
+  const T y_old = need_y ? *yj : Ops<T>::zero();
   T s = Ops<T>::zero();
   if (live && (mode == kFull || mode == kBetaZero)) {
     const int K = (int)(j / p.NB);
     const int jj = (int)(j - (long long)K * p.NB);
     const int I0 = p.upper ? 0 : K;
     const int I1 = p.upper ? K : p.nb - 1;
+    const long long rs = plan_rowstart(p, K);
+    const int q0 = plan_owner(p, rs);
+    const int nq = plan_owner(p, rs + plan_rowlen(p, K) - 1) - q0 + 1;
+    const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
+    const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
     const T* wc = Wc + j;
-    // loads issued in groups of 8 ahead of the (ordered) additions
+    // column partials, loads issued in groups of 8 ahead of the (ordered)
+    // additions
     int I = I0 + pp;
     for (; I + 7 * kFinParts <= I1; I += 8 * kFinParts) {
       T v[8];
@@ -532,11 +543,9 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
       for (int k = 0; k < 8; ++k) s = Ops<T>::add(s, v[k]);
     }
     for (; I <= I1; I += kFinParts) s = Ops<T>::add(s, wc[(long long)I * p.n]);
-    const long long rs = plan_rowstart(p, K);
-    const int q0 = plan_owner(p, rs);
-    const int nq = plan_owner(p, rs + plan_rowlen(p, K) - 1) - q0 + 1;
-    const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
-    for (int q = pp; q < nq; q += kFinParts) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
+    // then the row partials q = pp, pp + kFinParts, ...
+    if (pp < nq) s = Ops<T>::add(s, wr_first);
+    for (int q = pp + kFinParts; q < nq; q += kFinParts) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
   }
   part[pp][c] = s;
   __syncthreads();
@@ -544,14 +553,13 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
   s = part[0][c];
 #pragma unroll
   for (int k = 1; k < kFinParts; ++k) s = Ops<T>::add(s, part[k][c]);
-  T* yj = y + j * incy;
   T out;
   if (mode == kFull)
-    out = Ops<T>::add(Ops<T>::mul(alpha, s), Ops<T>::mul(beta, *yj));
+    out = Ops<T>::add(Ops<T>::mul(alpha, s), Ops<T>::mul(beta, y_old));
   else if (mode == kBetaZero)
     out = Ops<T>::mul(alpha, s);
   else if (mode == kAlphaZero)
-    out = Ops<T>::mul(beta, *yj);
+    out = Ops<T>::mul(beta, y_old);
   else
     out = Ops<T>::zero();
   if (status != nullptr && *status == epoch) out = Ops<T>::nan();   // the main kernel gave up
