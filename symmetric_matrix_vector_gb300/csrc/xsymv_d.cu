@@ -10,6 +10,10 @@ static const Variant<double> kVariants_d[] = {
     XSYMV_REG_MB(double, 2, 2, 8, 5),
     XSYMV_REG_MB(double, 4, 2, 8, 4),
     XSYMV_TMA(double, 2, 4, 4, 4),
+    XSYMV_REG_G(double, 4, 2, 8, 0, 4),
+    XSYMV_REG_G(double, 4, 2, 8, 0, 5),
+    XSYMV_REG_G(double, 4, 2, 8, 0, 6),
+    XSYMV_REG_G(double, 2, 4, 8, 0, 5),
 };
 static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");
 }  // namespace xsymv

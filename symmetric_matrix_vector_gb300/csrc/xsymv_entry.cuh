@@ -18,6 +18,18 @@ namespace xsymv {
 constexpr long long kHeaderBytes = 256;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // 2 s
 
+// Partition costs (see xsymv_plan.h): a dense column costs kDenseCost; a
+// diagonal-tile column, read with masked element loads, costs more for the
+// bandwidth-bound types and less for the FP64-bound ones (it holds half a
+// column's elements on average).
+constexpr int kDenseCost = 4;
+template <class T> struct DiagCost { static constexpr int v = 4; };
+template <> struct DiagCost<float> { static constexpr int v = 6; };
+template <> struct DiagCost<c32> { static constexpr int v = 6; };
+template <> struct DiagCost<double> { static constexpr int v = 3; };
+template <> struct DiagCost<c64> { static constexpr int v = 3; };
+template <> struct DiagCost<dd> { static constexpr int v = 3; };
+
 // Everything one launch of the main kernel needs.
 template <class T>
 struct MainArgs {
@@ -43,6 +55,7 @@ struct Variant {
   int stages;  // shared-memory ring depth
   int pipe;    // enum Pipe
   int waves;   // warps launched = waves x the warps that fit on the GPU at once
+  int diag_cost;  // partition cost of a diagonal-tile column (a dense one costs kDenseCost)
   cudaError_t (*launch)(const MainArgs<T>&);
   int (*ctas_per_sm)();
 };
@@ -95,15 +108,18 @@ int ctas_per_sm() {
   return cached;
 }
 
-// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>],
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>],
 // pipe r = loads into registers, t = bulk-copy (TMA) ring of STAGES chunks
 // per warp; _b<MINB>: registers capped so that MINB blocks fit on an SM;
-// _x<WAVES>: that many waves of blocks instead of one resident wave.
-#define XSYMV_VARIANT_P(T, VR, U, S, P, L, W, MB, X, SUF)                                 \
+// _x<WAVES>: that many waves of blocks instead of one resident wave;
+// _g<G>: partition cost G of a diagonal-tile column (default DiagCost).
+#define XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, G, SUF)                              \
   Variant<T> {                                                                            \
     "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
-        &launch_main<T, VR, U, S, P, W, MB>, &ctas_per_sm<T, VR, U, S, P, W, MB>          \
+        (G), &launch_main<T, VR, U, S, P, W, MB>, &ctas_per_sm<T, VR, U, S, P, W, MB>     \
   }
+#define XSYMV_VARIANT_P(T, VR, U, S, P, L, W, MB, X, SUF) \
+  XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, DiagCost<T>::v, SUF)
 #define XSYMV_REG(T, VR, U, W) XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, 0, 1, "")
 #define XSYMV_REG_MB(T, VR, U, W, MB) \
   XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, MB, 1, "_b" #MB)
@@ -111,6 +127,9 @@ int ctas_per_sm() {
 // hardware starts new blocks as earlier ones finish
 #define XSYMV_REG_MBX(T, VR, U, W, MB, X) \
   XSYMV_VARIANT_P(T, VR, U, 0, kPipeRegisters, "r", W, MB, X, "_b" #MB "_x" #X)
+// diagonal-tile columns costed G (dense = kDenseCost) in the partition
+#define XSYMV_REG_G(T, VR, U, W, MB, G) \
+  XSYMV_VARIANT_G(T, VR, U, 0, kPipeRegisters, "r", W, MB, 1, G, "_b" #MB "_g" #G)
 #define XSYMV_TMA(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeBulk, "t", W, 0, 1, "")
 
 template <class T>
@@ -179,7 +198,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
   const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n)];
   const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps * v->waves;
-  out->plan = plan_make(n, v->NB, upper, wmax);
+  out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost);
   out->variant = v;
   out->wc_off = kHeaderBytes;
   out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);

@@ -422,19 +422,24 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     __syncwarp();
   }
 
-  // this warp's segments [s, send)
-  const long long send = plan_wstart(p, w + 1);
-  long long s = plan_wstart(p, w);
-  int I = plan_row_of(p, s);
+  // this warp's cost range [cs, ce); it owns the columns whose first cost
+  // unit lies in it
+  const long long ce = plan_wstart(p, w + 1);
+  long long cs = plan_wstart(p, w);
+  int I = plan_row_of(p, cs);
   const long long n = p.n;
   Tile t;
 
-  while (s < send) {
-    const long long rs = plan_rowstart(p, I);
-    const long long rend = rs + plan_rowlen(p, I);
+  for (; cs < ce && I < p.nb; ++I) {
+    const long long rcs = plan_rowstart(p, I);
+    const long long rce = rcs + plan_rowcost(p, I);
+    const long long c0 = plan_cols_before(p, I, cs - rcs);
+    const long long c1 = plan_cols_before(p, I, (ce < rce ? ce : rce) - rcs);
+    cs = rce;
+    if (c0 >= c1) continue;   // no column of this row starts in the range
     const long long cb = plan_colbase(p, I);
-    const long long ja = cb + (s - rs);
-    const long long jb = cb + ((send < rend ? send : rend) - rs);
+    const long long ja = cb + c0;
+    const long long jb = cb + c1;
     const long long r0 = (long long)I * NB;
 
 #pragma unroll
@@ -474,17 +479,13 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     }
 
     // the row partial goes to slot q of block row I, q = this warp's index
-    // among the warps touching the row
-    const int q = w - plan_owner(p, plan_rowstart(p, I));
+    // among the warps owning columns of the row
+    const int q = w - plan_first_owner(p, I);
     T* wr = Wr + ((long long)I * p.qmax + q) * NB;
 #pragma unroll
     for (int v = 0; v < VR; ++v)
 #pragma unroll
       for (int k = 0; k < VPL; ++k) wr[Tile::lane_row(v, lane, k)] = t.racc[v][k];
-
-    const long long e = plan_rowstart(p, I) + plan_rowlen(p, I);
-    s = send < e ? send : e;
-    ++I;
   }
 }
 
@@ -526,9 +527,7 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
     const int jj = (int)(j - (long long)K * p.NB);
     const int I0 = p.upper ? 0 : K;
     const int I1 = p.upper ? K : p.nb - 1;
-    const long long rs = plan_rowstart(p, K);
-    const int q0 = plan_owner(p, rs);
-    const int nq = plan_owner(p, rs + plan_rowlen(p, K) - 1) - q0 + 1;
+    const int nq = plan_nq(p, K);
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
     const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
     const T* wc = Wc + j;

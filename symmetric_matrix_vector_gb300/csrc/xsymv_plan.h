@@ -5,20 +5,25 @@
 // stored triangle inside its rows:
 //   upper ('U'): j = I*NB .. n-1        (diagonal tile first, then the rest)
 //   lower ('L'): j = 0 .. min(n, I*NB+NB)-1   (off-diagonal first, diagonal last)
-// Segments are numbered row after row (block row 0 first), S in total, and
-// each of the W warps takes one contiguous run of ceil or floor S/W of them,
-// so every warp streams the same number of column segments from HBM.
+// Columns of the diagonal tile cost more than dense ones (masked loads), so
+// the warps do not get equal column counts but equal cost: a dense column
+// costs cd units, a diagonal-tile column cg units.  Costs are laid out row
+// after row (block row 0 first); warp w takes the cost range
+// [w*SC/W, (w+1)*SC/W) and owns the columns whose first cost unit falls in
+// it, so every column has exactly one owner.
 //
 // Deterministic cross-warp accumulation (the role the report's ordered
 // tickets play, "CUDA-xSYMV の実装と評価" §2.1, figure "Atomic"): a warp
 // writes
-//   * one column partial per segment it processes, to Wc[I*n + j], and
-//   * one row partial per block row it touches, to slot q of that row,
-//     Wr[(I*qmax + q)*NB + r], q = its index among the warps touching row I;
+//   * one column partial per column it owns, to Wc[I*n + j], and
+//   * one row partial per block row in which it owns columns, to slot q of
+//     that row, Wr[(I*qmax + q)*NB + r], q = w - (owner of the row's first
+//     column);
 // a second kernel then sums those slots for every output element in a fixed
-// order, so results are bit-identical from run to run.  W <= S guarantees
-// that every warp owns at least one segment, so every slot a finaliser reads
-// has been written.
+// order, so results are bit-identical from run to run.  Warp ranges are at
+// least max(cd, cg) units long, so every warp between the owners of a row's
+// first and last columns owns columns in that row: no slot a finaliser reads
+// is left unwritten.
 #pragma once
 
 #ifdef __CUDACC__
@@ -34,8 +39,10 @@ struct Plan {
   int NB;           // tile edge (rows per block row)
   int nb;           // number of block rows, ceil(n / NB)
   int upper;        // 1: upper triangle stored, 0: lower
-  long long S;      // total column segments
-  int W;            // warps sharing the segments (1 <= W <= S)
+  int cd;           // cost of a dense column
+  int cg;           // cost of a diagonal-tile column
+  long long SC;     // total cost
+  int W;            // warps sharing the cost (1 <= W <= SC / max(cd, cg))
   int qmax;         // most warps that touch one block row
 };
 
@@ -45,34 +52,79 @@ XSYMV_HD long long plan_rowlen(const Plan& p, int I) {
   return e < p.n ? e : (long long)p.n;
 }
 
-// first segment of block row I (0 <= I <= nb-1; and I == nb for upper)
-XSYMV_HD long long plan_rowstart(const Plan& p, int I) {
+// columns of block row I that lie in its diagonal tile
+XSYMV_HD long long plan_dlen(const Plan& p, int I) {
+  long long r = (long long)p.n - (long long)I * p.NB;
+  return r < p.NB ? r : (long long)p.NB;
+}
+
+// column segments in block rows before I
+XSYMV_HD long long plan_segstart(const Plan& p, int I) {
   if (p.upper) return (long long)I * p.n - (long long)p.NB * I * (I - 1) / 2;
   return (long long)p.NB * I * (I + 1) / 2;
 }
 
-XSYMV_HD long long plan_total(int n, int NB, int upper) {
-  if (n <= 0) return 0;
-  Plan p{n, NB, (n + NB - 1) / NB, upper, 0, 1, 1};
-  return plan_rowstart(p, p.nb - 1) + plan_rowlen(p, p.nb - 1);
+// first cost unit of block row I (0 <= I <= nb-1)
+XSYMV_HD long long plan_rowstart(const Plan& p, int I) {
+  // every block row before I has a full diagonal tile of NB columns
+  return (long long)p.cd * plan_segstart(p, I) + (long long)(p.cg - p.cd) * p.NB * I;
 }
 
-// first column (matrix index) of block row I's segments
+XSYMV_HD long long plan_rowcost(const Plan& p, int I) {
+  const long long d = plan_dlen(p, I);
+  return (long long)p.cd * (plan_rowlen(p, I) - d) + (long long)p.cg * d;
+}
+
+// the row's columns come in two runs: upper = diagonal tile then dense,
+// lower = dense then diagonal tile; (len1, unit1) describes the first run
+XSYMV_HD void plan_runs(const Plan& p, int I, long long* len1, int* unit1, int* unit2) {
+  const long long d = plan_dlen(p, I);
+  if (p.upper) {
+    *len1 = d;
+    *unit1 = p.cg;
+    *unit2 = p.cd;
+  } else {
+    *len1 = plan_rowlen(p, I) - d;
+    *unit1 = p.cd;
+    *unit2 = p.cg;
+  }
+}
+
+// number of columns of block row I whose first cost unit lies before
+// offset o (0 <= o <= rowcost) from the row's start
+XSYMV_HD long long plan_cols_before(const Plan& p, int I, long long o) {
+  long long len1;
+  int u1, u2;
+  plan_runs(p, I, &len1, &u1, &u2);
+  if (o <= (long long)u1 * len1) return (o + u1 - 1) / u1;
+  return len1 + (o - (long long)u1 * len1 + u2 - 1) / u2;
+}
+
+// cost offset of column c (0 <= c < rowlen) within block row I
+XSYMV_HD long long plan_col_cost(const Plan& p, int I, long long c) {
+  long long len1;
+  int u1, u2;
+  plan_runs(p, I, &len1, &u1, &u2);
+  return c < len1 ? (long long)u1 * c : (long long)u1 * len1 + (long long)u2 * (c - len1);
+}
+
+// first column (matrix index) of block row I's columns
 XSYMV_HD long long plan_colbase(const Plan& p, int I) { return p.upper ? (long long)I * p.NB : 0; }
 
-// first segment of warp w (w = W gives S)
-XSYMV_HD long long plan_wstart(const Plan& p, int w) { return (long long)w * p.S / p.W; }
+// first cost unit of warp w (w = W gives SC)
+XSYMV_HD long long plan_wstart(const Plan& p, int w) { return (long long)w * p.SC / p.W; }
 
-// the warp whose run contains segment s
-XSYMV_HD int plan_owner(const Plan& p, long long s) { return (int)(((s + 1) * p.W - 1) / p.S); }
+// the warp whose range contains cost unit s
+XSYMV_HD int plan_owner(const Plan& p, long long s) { return (int)(((s + 1) * p.W - 1) / p.SC); }
 
-// number of warps whose runs meet block row I
-XSYMV_HD int plan_nq(const Plan& p, int I) {
-  long long rs = plan_rowstart(p, I);
-  return plan_owner(p, rs + plan_rowlen(p, I) - 1) - plan_owner(p, rs) + 1;
+// warps owning the first and the last column of block row I
+XSYMV_HD int plan_first_owner(const Plan& p, int I) { return plan_owner(p, plan_rowstart(p, I)); }
+XSYMV_HD int plan_last_owner(const Plan& p, int I) {
+  return plan_owner(p, plan_rowstart(p, I) + plan_col_cost(p, I, plan_rowlen(p, I) - 1));
 }
+XSYMV_HD int plan_nq(const Plan& p, int I) { return plan_last_owner(p, I) - plan_first_owner(p, I) + 1; }
 
-// block row containing segment s (binary search)
+// block row containing cost unit s (binary search)
 XSYMV_HD int plan_row_of(const Plan& p, long long s) {
   int lo = 0, hi = p.nb - 1;
   while (lo < hi) {
@@ -82,15 +134,25 @@ XSYMV_HD int plan_row_of(const Plan& p, long long s) {
   return lo;
 }
 
-// Build the plan for n, NB, uplo with at most Wmax warps.
-inline Plan plan_make(int n, int NB, int upper, long long Wmax) {
+XSYMV_HD long long plan_total_cost(int n, int NB, int upper, int cd, int cg) {
+  if (n <= 0) return 0;
+  Plan p{n, NB, (n + NB - 1) / NB, upper, cd, cg, 0, 1, 1};
+  return plan_rowstart(p, p.nb - 1) + plan_rowcost(p, p.nb - 1);
+}
+
+// Build the plan for n, NB, uplo with at most Wmax warps; a dense column
+// costs cd units and a diagonal-tile column cg units (cd, cg >= 1).
+inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int cg = 1) {
   Plan p{};
   p.n = n;
   p.NB = NB;
   p.nb = (n + NB - 1) / NB;
   p.upper = upper;
-  p.S = plan_total(n, NB, upper);
-  long long W = Wmax < p.S ? Wmax : p.S;
+  p.cd = cd;
+  p.cg = cg;
+  p.SC = plan_total_cost(n, NB, upper, cd, cg);
+  const long long unit = cd > cg ? cd : cg;
+  long long W = Wmax < p.SC / unit ? Wmax : p.SC / unit;
   p.W = (int)(W < 1 ? 1 : W);
   p.qmax = 1;
   for (int I = 0; I < p.nb; ++I) {

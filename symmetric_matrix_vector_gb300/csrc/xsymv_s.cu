@@ -16,6 +16,8 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_REG_MB(float, 1, 2, 8, 6),
     XSYMV_TMA(float, 1, 8, 3, 8),
     XSYMV_REG_MBX(float, 1, 2, 8, 6, 4),
+    XSYMV_REG_G(float, 1, 2, 8, 6, 5),
+    XSYMV_REG_G(float, 1, 2, 8, 6, 7),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

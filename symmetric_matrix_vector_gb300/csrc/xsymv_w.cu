@@ -8,6 +8,9 @@ static const Variant<dd> kVariants_w[] = {
     XSYMV_REG(dd, 4, 1, 8),
     XSYMV_REG_MB(dd, 4, 2, 8, 3),
     XSYMV_TMA(dd, 4, 2, 4, 4),
+    XSYMV_REG_G(dd, 4, 2, 8, 0, 4),
+    XSYMV_REG_G(dd, 4, 2, 8, 0, 5),
+    XSYMV_REG_G(dd, 4, 2, 8, 0, 6),
 };
 static_assert(sizeof(dd) == sizeof(xsymv_dd), "C-ABI type layout");
 }  // namespace xsymv

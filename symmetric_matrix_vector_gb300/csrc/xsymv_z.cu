@@ -9,6 +9,9 @@ static const Variant<c64> kVariants_z[] = {
     XSYMV_REG(c64, 2, 4, 8),
     XSYMV_REG_MB(c64, 4, 2, 8, 4),
     XSYMV_TMA(c64, 4, 2, 4, 4),
+    XSYMV_REG_G(c64, 4, 2, 8, 0, 4),
+    XSYMV_REG_G(c64, 4, 2, 8, 0, 5),
+    XSYMV_REG_G(c64, 4, 2, 8, 0, 6),
 };
 static_assert(sizeof(c64) == sizeof(xsymv_c64), "C-ABI type layout");
 }  // namespace xsymv

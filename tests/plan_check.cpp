@@ -1,0 +1,107 @@
+// Brute-force check of the work partition in xsymv_plan.h (host logic of the
+// CUDA library): simulates the main kernel's per-warp loop and verifies that
+// every column segment of the stored triangle is owned exactly once, that the
+// row-partial slots of each block row have no holes, and that the finaliser's
+// block-row ranges are exactly the rows holding each column.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+
+#include "xsymv_plan.h"
+
+using namespace xsymv;
+
+static int fail(const char* what, int n, int NB, int upper, long long W, int cd, int cg) {
+  std::printf("FAIL %s n=%d NB=%d upper=%d W=%lld cd=%d cg=%d\n", what, n, NB, upper, W, cd, cg);
+  return 1;
+}
+
+static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
+  const Plan p = plan_make(n, NB, upper, Wmax, cd, cg);
+  const int nb = p.nb;
+  // owners[I][c] = warp owning column c of block row I, from the kernel loop
+  std::vector<std::vector<int>> own(nb);
+  for (int I = 0; I < nb; ++I) own[I].assign((size_t)plan_rowlen(p, I), -1);
+  std::vector<std::vector<int>> row_warps(nb);
+  for (int w = 0; w < p.W; ++w) {
+    const long long ce = plan_wstart(p, w + 1);
+    long long cs = plan_wstart(p, w);
+    int I = plan_row_of(p, cs);
+    for (; cs < ce && I < nb; ++I) {
+      const long long rcs = plan_rowstart(p, I);
+      const long long rce = rcs + plan_rowcost(p, I);
+      if (cs < rcs) return fail("range starts before row", n, NB, upper, Wmax, cd, cg);
+      const long long c0 = plan_cols_before(p, I, cs - rcs);
+      const long long c1 = plan_cols_before(p, I, (ce < rce ? ce : rce) - rcs);
+      cs = rce;
+      if (c0 >= c1) continue;
+      for (long long c = c0; c < c1; ++c) {
+        if (own[I][c] != -1) return fail("column owned twice", n, NB, upper, Wmax, cd, cg);
+        own[I][c] = w;
+        // the owner is the warp whose range holds the column's first cost unit
+        if (plan_owner(p, rcs + plan_col_cost(p, I, c)) != w)
+          return fail("owner rule", n, NB, upper, Wmax, cd, cg);
+      }
+      const int q = w - plan_first_owner(p, I);
+      if (q < 0 || q >= plan_nq(p, I) || q >= p.qmax)
+        return fail("slot index", n, NB, upper, Wmax, cd, cg);
+      row_warps[I].push_back(w);
+    }
+  }
+  long long total = 0;
+  for (int I = 0; I < nb; ++I) {
+    for (int o : own[I])
+      if (o < 0) return fail("column not owned", n, NB, upper, Wmax, cd, cg);
+    total += (long long)own[I].size();
+    // the warps of a row are exactly first_owner .. last_owner, each once
+    const int f = plan_first_owner(p, I), nq = plan_nq(p, I);
+    if ((int)row_warps[I].size() != nq) return fail("slot holes", n, NB, upper, Wmax, cd, cg);
+    for (int k = 0; k < nq; ++k)
+      if (row_warps[I][k] != f + k) return fail("slot order", n, NB, upper, Wmax, cd, cg);
+  }
+  // total segments = stored columns per block row, as the report's triangle
+  long long want = 0;
+  for (int I = 0; I < nb; ++I) want += upper ? n - (long long)I * NB : std::min<long long>(n, (long long)(I + 1) * NB);
+  if (total != want) return fail("segment count", n, NB, upper, Wmax, cd, cg);
+  // finaliser: column j gets column partials from block rows I0..I1
+  for (int j = 0; j < n; ++j) {
+    const int K = j / NB;
+    const int I0 = upper ? 0 : K, I1 = upper ? K : nb - 1;
+    for (int I = 0; I < nb; ++I) {
+      const long long cb = plan_colbase(p, I), len = plan_rowlen(p, I);
+      const bool has = j >= cb && j < cb + len;
+      if (has != (I >= I0 && I <= I1)) return fail("finaliser rows", n, NB, upper, Wmax, cd, cg);
+    }
+  }
+  // the diagonal-tile columns are the ones costed cg
+  for (int I = 0; I < nb; ++I) {
+    const long long d = plan_dlen(p, I), len = plan_rowlen(p, I), cb = plan_colbase(p, I);
+    for (long long c = 0; c < len; ++c) {
+      const long long j = cb + c;
+      const bool diag = j >= (long long)I * NB && j < (long long)I * NB + NB;
+      const long long next = c + 1 < len ? plan_col_cost(p, I, c + 1) : plan_rowcost(p, I);
+      if (next - plan_col_cost(p, I, c) != (diag ? cg : cd))
+        return fail("column cost", n, NB, upper, Wmax, cd, cg);
+    }
+    if (d != std::min<long long>(NB, n - (long long)I * NB)) return fail("dlen", n, NB, upper, Wmax, cd, cg);
+  }
+  return 0;
+}
+
+int main() {
+  int bad = 0, cases = 0;
+  const int sizes[] = {1, 2, 3, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 511, 700, 1025};
+  const int edges[] = {32, 64, 128, 256};
+  const long long warps[] = {1, 2, 3, 7, 64, 300, 1000, 7296, 1000000};
+  const int costs[][2] = {{1, 1}, {4, 6}, {4, 3}, {2, 7}, {5, 1}};
+  for (int n : sizes)
+    for (int NB : edges)
+      for (int upper = 0; upper < 2; ++upper)
+        for (long long W : warps)
+          for (auto& c : costs) {
+            bad += check(n, NB, upper, W, c[0], c[1]);
+            ++cases;
+          }
+  std::printf("%d cases, %d failures\n", cases, bad);
+  return bad ? 1 : 0;
+}
