@@ -80,6 +80,8 @@ class Oracle:
             fn.restype = i
         lib.oracle_rows.argtypes = [c, c, i, v, v, i, v, i, v, v, i, i, v, v, v, v]
         lib.oracle_rows.restype = i
+        lib.oracle_gemv_rows.argtypes = [c, i, v, v, i, v, i, v, v, i, i, v, v, v, v]
+        lib.oracle_gemv_rows.restype = i
         lib.oracle_quad_mant_dig.restype = i
         self.lib = lib
 
@@ -147,6 +149,29 @@ class Oracle:
             ref_lo = ref_lo.reshape(-1, 2)
         return info, ref_hi, ref_lo, denom
 
+    def gemv_rows(self, kind, n, alpha, A, lda, x, incx, beta, y0, incy, rows):
+        """Rows of the general product y := alpha*A*x + beta*y (all n*n
+        elements of A read; kind 's' or 'd').
+
+        Returns ``(info, ref_hi, ref_lo, denom)`` for the row indices in
+        ``rows``; ``denom`` is |alpha| * sum_j |A(i,j)| |x_j| + |beta| |y_i|.
+        """
+        kind = kind.lower()
+        dt = _DTYPES[kind]
+        A = np.ascontiguousarray(A, dtype=dt)
+        x = np.ascontiguousarray(x, dtype=dt)
+        y0 = np.ascontiguousarray(y0, dtype=dt)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        ref_hi = np.zeros(len(rows), dtype=np.float64)
+        ref_lo = np.zeros(len(rows), dtype=np.float64)
+        denom = np.zeros(len(rows), dtype=np.float64)
+        al = np.array(_scalar_as_doubles(alpha, kind), dtype=np.float64)
+        be = np.array(_scalar_as_doubles(beta, kind), dtype=np.float64)
+        info = self.lib.oracle_gemv_rows(kind.encode(), n, _ptr(al), _ptr(A), lda, _ptr(x), incx,
+                                         _ptr(be), _ptr(y0), incy, len(rows), _ptr(rows),
+                                         _ptr(ref_hi), _ptr(ref_lo), _ptr(denom))
+        return info, ref_hi, ref_lo, denom
+
     def quad_mant_dig(self) -> int:
         return self.lib.oracle_quad_mant_dig()
 
@@ -191,3 +216,7 @@ def symv(*args, **kw):
 
 def rows(*args, **kw):
     return get().rows(*args, **kw)
+
+
+def gemv_rows(*args, **kw):
+    return get().gemv_rows(*args, **kw)

@@ -501,3 +501,51 @@ int oracle_rows(char kind, char uplo, int n, const double *alpha, const void *A,
     }
     return 0;
 }
+
+/* ------------------ general matrix-vector product (GEMV) ---------------- */
+/* The report measures SYMV against the general product y := alpha*A*x +
+ * beta*y, which reads all n*n elements of A (§1: GEMV needs twice the
+ * memory traffic of SYMV).  This is that product by its definition, for
+ * selected rows, in binary128: y_i = beta*y_i + alpha*sum_j A(i,j)*x_j. */
+
+int oracle_gemv_rows(char kind, int n, const double *alpha, const void *A, int lda,
+                     const void *x, int incx, const double *beta, const void *y0,
+                     int incy, int nrows, const long long *rows, double *ref_hi,
+                     double *ref_lo, double *denom)
+{
+    if (n < 0) return 1;
+    if (lda < (n > 1 ? n : 1)) return 4;
+    if (incx == 0) return 6;
+    if (incy == 0) return 9;
+    if (kind != 's' && kind != 'd') return -2;
+    const long kx = first_index(n, incx), ky = first_index(n, incy);
+    const quad_t al = alpha[0], be = beta[0];
+
+    for (int r = 0; r < nrows; r++) {
+        const long i = rows[r];
+        if (i < 0 || i >= n) return -3;
+        quad_t s = 0;
+        double d = 0.0;
+        if (al != 0) {
+            for (long j = 0; j < n; j++) {
+                const quad_t a = load_val(kind, A, i + j * (long)lda).re;
+                const quad_t xj = load_val(kind, x, kx + j * incx).re;
+                s += a * xj;
+                d += fabs((double)a) * fabs((double)xj);
+            }
+        }
+        quad_t out = al * s;
+        double dy = 0.0;
+        if (be != 0) {
+            const quad_t yi = load_val(kind, y0, ky + i * incy).re;
+            out += be * yi;
+            dy = fabs((double)be) * fabs((double)yi);
+        }
+        double h, l;
+        split_quad(out, &h, &l);
+        if (ref_hi) ref_hi[r] = h;
+        if (ref_lo) ref_lo[r] = l;
+        if (denom) denom[r] = fabs((double)al) * d + dy;
+    }
+    return 0;
+}

@@ -20,6 +20,9 @@
  *   oracle_rows — the definition y_i = beta*y_i + alpha*sum_j A(i,j)*x_j on
  *       the explicitly mirrored matrix, for selected rows, in binary128,
  *       together with the error normaliser |alpha|*(|A||x|)_i + |beta|*|y_i|.
+ * and, for the general product the report compares SYMV with (§1),
+ *   oracle_gemv_rows — y_i = beta*y_i + alpha*sum_j A(i,j)*x_j over all n*n
+ *       elements of an unsymmetric A, for selected rows, in binary128.
  *
  * Storage conventions (all host memory, owned by the caller):
  *   s: float      d: double
@@ -71,6 +74,20 @@ int oracle_rows(char kind, char uplo, int n, const double *alpha, const void *A,
                 int lda, const void *x, int incx, const double *beta,
                 const void *y0, int incy, int nrows, const long long *rows,
                 double *ref_hi, double *ref_lo, double *denom);
+
+/* The general (unsymmetric) product y := alpha*A*x + beta*y that the report
+ * compares SYMV with (§1), by its definition, for the nrows row indices in
+ * rows[]: all n*n elements of A are read.  kind 's' or 'd' only; alpha and
+ * beta point at one double each (for 's' the float values widened).  Writes
+ * ref_hi + ref_lo (binary128 result as a double pair) and, if denom is not
+ * NULL, |alpha| * sum_j |A(i,j)| |x_j| + |beta| |y_i|.  Returns 0, or the
+ * argument position of the first bad argument of the library's xgemv_<t>
+ * (1 n, 4 lda, 6 incx, 9 incy); -2 for another kind, -3 for a row out of
+ * range. */
+int oracle_gemv_rows(char kind, int n, const double *alpha, const void *A, int lda,
+                     const void *x, int incx, const double *beta, const void *y0,
+                     int incy, int nrows, const long long *rows, double *ref_hi,
+                     double *ref_lo, double *denom);
 
 /* Mantissa digits of the binary128 type the oracle accumulates in (113). */
 int oracle_quad_mant_dig(void);

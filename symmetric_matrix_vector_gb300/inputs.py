@@ -146,6 +146,28 @@ def make_problem(kind: str, uplo: str, n: int, *, lda: int | None = None, alpha=
                    incx=incx, incy=incy, seed=seed, name=name)
 
 
+def make_general(kind: str, n: int, *, lda: int | None = None, alpha=1.0, beta=0.0,
+                 dist: str = "uniform", seed: int = 0, incx: int = 1, incy: int = 1,
+                 name: str = "", column_chunk: int = 2048) -> Problem:
+    """Dense random unsymmetric n-by-n problem for the general product
+    (kind 's' or 'd'): every element of the n-by-n matrix gets an i.i.d.
+    ``dist`` value, the padding rows n..lda-1 NaN.  ``uplo`` is "G"."""
+    kind = kind.lower()
+    if kind not in ("s", "d"):
+        raise ValueError(kind)
+    lda = max(1, n) if lda is None else lda
+    rng = np.random.default_rng(seed)
+    A = np.empty((n, lda), dtype=DTYPES[kind])
+    for j0 in range(0, n, column_chunk):
+        j1 = min(n, j0 + column_chunk)
+        A[j0:j1] = _values(rng, (j1 - j0) * lda, dist, kind).reshape(j1 - j0, lda)
+    A[:, n:] = np.nan
+    x = _strided(_values(rng, n, dist, kind), incx, kind)
+    y = _strided(_values(rng, n, dist, kind), incy, kind)
+    return Problem(kind=kind, uplo="G", n=n, lda=lda, alpha=alpha, beta=beta, A=A, x=x, y=y,
+                   incx=incx, incy=incy, seed=seed, name=name)
+
+
 # ---------------------------------------------------------------------------
 # The five workloads of the CUDA-xSYMV evaluation, restated at GB300 sizes
 # ---------------------------------------------------------------------------
@@ -253,3 +275,26 @@ def device_problem(kind: str, uplo: str, n: int, *, lda: int | None = None, alph
         A[idx, idx, 1] = float("nan")
     return dict(kind=kind, uplo=uplo, n=n, lda=lda, alpha=alpha, beta=beta, A=A.contiguous(),
                 x=values(n).contiguous(), y=values(n).contiguous())
+
+
+def device_general(kind: str, n: int, *, lda: int | None = None, alpha=1.0, beta=0.0,
+                   dist: str = "uniform", seed: int = 0, device: str = "cuda"):
+    """Dense random unsymmetric problem on the device for the general product
+    (kind 's' or 'd'), contiguous x and y; NaN in the padding rows only."""
+    import torch
+
+    kind = kind.lower()
+    lda = max(1, n) if lda is None else lda
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = {"s": torch.float32, "d": torch.float64}[kind]
+
+    def draw(shape):
+        if dist == "uniform":
+            return torch.rand(shape, generator=g, device=device, dtype=dt).mul_(2).sub_(1)
+        return torch.randn(shape, generator=g, device=device, dtype=dt)
+
+    A = draw((n, lda))
+    A[:, n:] = float("nan")
+    return dict(kind=kind, uplo="G", n=n, lda=lda, alpha=alpha, beta=beta, A=A.contiguous(),
+                x=draw((n,)).contiguous(), y=draw((n,)).contiguous())

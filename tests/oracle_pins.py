@@ -17,7 +17,7 @@ from fractions import Fraction as Fr
 
 import numpy as np
 
-from symmetric_matrix_vector_gb300.inputs import DTYPES, make_problem
+from symmetric_matrix_vector_gb300.inputs import DTYPES, make_general, make_problem
 
 KINDS = ("s", "d", "c", "z", "w")
 # unit roundoff of the oracle's accumulator per kind
@@ -501,6 +501,139 @@ def check_arg_errors(o):
         assert info == want, (uplo, n, lda, incx, incy, info)
         if want:
             assert np.array_equal(y, p.y, equal_nan=True)
+
+
+# ----------------------------------------------------------------------------
+# the general product the report compares SYMV with (§1): oracle_gemv_rows
+# ----------------------------------------------------------------------------
+
+def int_general(kind, n, *, lda=None, incx=1, incy=1, alpha=1.25, beta=0.5, seed=0):
+    """Unsymmetric small-integer problem: every oracle operation is exact."""
+    p = make_general(kind, n, lda=lda, incx=incx, incy=incy, alpha=alpha, beta=beta, seed=seed)
+    rng = np.random.default_rng(2000 + seed)
+    p.A[:, :n] = rng.integers(-4, 5, size=(n, n)).astype(p.A.dtype)
+    for v, inc in ((p.x, incx), (p.y, incy)):
+        for i in range(n):
+            v[vidx(n, inc, i)] = rng.integers(-4, 5)
+    return p
+
+
+def exact_gemv(p, rows=None):
+    """rows of alpha*A*x + beta*y by the definition, in exact rationals"""
+    n = p.n
+    al, be = Fr(float(np.float32(p.alpha) if p.kind == "s" else p.alpha)), \
+        Fr(float(np.float32(p.beta) if p.kind == "s" else p.beta))
+    out = []
+    for i in (range(n) if rows is None else rows):
+        s = Fr(0)
+        if al != 0:
+            for j in range(n):
+                s += Fr(float(p.A[j, i])) * Fr(float(p.x[vidx(n, p.incx, j)]))
+        r = al * s
+        if be != 0:
+            r += be * Fr(float(p.y[vidx(n, p.incy, i)]))
+        out.append(r)
+    return out
+
+
+def gemv(o, p, rows=None, alpha=None, beta=None, A=None, x=None, y=None):
+    rows = np.arange(p.n) if rows is None else np.asarray(rows)
+    return o.gemv_rows(p.kind, p.n, p.alpha if alpha is None else alpha, p.A if A is None else A,
+                       p.lda, p.x if x is None else x, p.incx, p.beta if beta is None else beta,
+                       p.y if y is None else y, p.incy, rows)
+
+
+def check_gemv_integer_bruteforce(o):
+    """exact unsymmetric data: the oracle equals brute-force rationals (a
+    transposed operand, a wrong stride or a dropped term changes the value)"""
+    for kind in ("s", "d"):
+        for n, incx, incy, (alpha, beta) in ((1, 1, 1, (1.25, 0.5)), (2, -1, 2, (1.25, 0.5)),
+                                             (3, 2, -3, (-2.0, 0.0)), (7, 1, 1, (0.75, -1.5)),
+                                             (12, -2, -1, (1.25, 0.5))):
+            p = int_general(kind, n, lda=n + 3, incx=incx, incy=incy, alpha=alpha, beta=beta,
+                            seed=n)
+            info, hi, lo, den = gemv(o, p)
+            assert info == 0
+            want = exact_gemv(p)
+            for i in range(n):
+                assert Fr(float(hi[i])) + Fr(float(lo[i])) == want[i], (kind, n, i)
+
+
+def check_gemv_closed_forms(o):
+    """A = I gives alpha*x + beta*y; A = u v^T gives alpha*(v.x)*u + beta*y"""
+    n = 9
+    for kind in ("s", "d"):
+        p = int_general(kind, n, lda=n + 1, seed=3)
+        A = p.A.copy()
+        A[:, :n] = 0
+        for j in range(n):
+            A[j, j] = 1
+        _, hi, lo, _ = gemv(o, p, A=A)
+        for i in range(n):
+            want = Fr(1.25) * Fr(float(p.x[i])) + Fr(0.5) * Fr(float(p.y[i]))
+            assert Fr(float(hi[i])) + Fr(float(lo[i])) == want, (kind, i)
+        u = np.arange(1, n + 1, dtype=np.float64)
+        v = np.arange(n, 0, -1, dtype=np.float64) - 4
+        A[:, :n] = np.outer(v, u)            # A[j, i] = A(i, j) = u_i v_j
+        vx = sum(Fr(float(v[j])) * Fr(float(p.x[j])) for j in range(n))
+        _, hi, lo, _ = gemv(o, p, A=A)
+        for i in range(n):
+            want = Fr(1.25) * vx * Fr(float(u[i])) + Fr(0.5) * Fr(float(p.y[i]))
+            assert Fr(float(hi[i])) + Fr(float(lo[i])) == want, (kind, i)
+
+
+def check_gemv_random_and_library(o):
+    """random data: within the binary128 accumulation bound of exact
+    arithmetic, and within working-precision tolerance of scipy's ?gemv"""
+    from scipy.linalg import blas
+
+    for kind, fn, tol in (("s", blas.sgemv, 5e-5), ("d", blas.dgemv, 1e-12)):
+        n = 23
+        p = make_general(kind, n, lda=n + 2, alpha=-0.75, beta=1.5, incx=-2, incy=3, seed=4)
+        info, hi, lo, den = gemv(o, p)
+        assert info == 0
+        want = exact_gemv(p)
+        for i in range(n):
+            err = abs(float(Fr(float(hi[i])) + Fr(float(lo[i])) - want[i]))
+            assert err <= 4 * (n + 2) * 2.0 ** -113 * den[i] + 2.0 ** -104 * den[i], (kind, i)
+        a = p.A[:, :n].T.copy()
+        xs = np.array([p.x[vidx(n, p.incx, j)] for j in range(n)])
+        ys = np.array([p.y[vidx(n, p.incy, i)] for i in range(n)])
+        ref = fn(p.alpha, a, xs, beta=p.beta, y=ys.copy())
+        assert np.max(np.abs(ref - hi) / den) <= tol, kind
+
+
+def check_gemv_symmetric_matches_symv(o):
+    """on the explicitly mirrored matrix the general product is SYMV"""
+    n = 17
+    p = make_problem("d", "L", n, lda=n, alpha=1.25, beta=0.5, seed=5)
+    full = np.where(np.isnan(p.A), p.A.T, p.A)        # A[j, i] for i < j from A[i, j]
+    g = make_general("d", n, lda=n, alpha=1.25, beta=0.5, seed=5)
+    _, gh, gl, gden = gemv(o, g, A=full, x=p.x, y=p.y)
+    _, sy, sh, sl = run(o, p)
+    for i in range(n):
+        d = abs((gh[i] - sh[i]) + (gl[i] - sl[i]))
+        assert d <= 8 * (n + 2) * 2.0 ** -105 * gden[i], i
+
+
+def check_gemv_special_and_errors(o):
+    """alpha = 0 reads neither A nor x; beta = 0 does not read y; padding rows
+    are never read; BLAS argument positions 1 n, 4 lda, 6 incx, 9 incy"""
+    for kind in ("s", "d"):
+        p = make_general(kind, 6, lda=8, alpha=1.25, beta=0.5, seed=6)
+        _, hi, lo, den = gemv(o, p)
+        assert np.all(np.isfinite(hi)) and np.all(np.isfinite(den))
+        nanA = np.full_like(p.A, np.nan)
+        _, hi, lo, _ = gemv(o, p, alpha=0.0, A=nanA, x=np.full_like(p.x, np.nan))
+        assert np.array_equal(hi, 0.5 * p.y.astype(np.float64)) and not np.any(lo)
+        _, hi, lo, _ = gemv(o, p, beta=0.0, y=np.full_like(p.y, np.nan))
+        assert np.all(np.isfinite(hi))
+    p = make_general("d", 4, seed=7)
+    for (n, lda, incx, incy), want in (((-1, 4, 1, 1), 1), ((4, 3, 1, 1), 4), ((4, 4, 0, 1), 6),
+                                       ((4, 4, 1, 0), 9), ((4, 4, -1, -1), 0)):
+        info, _, _, _ = o.gemv_rows("d", n, 1.0, p.A, lda, p.x, incx, 0.0, p.y, incy,
+                                    np.arange(max(n, 0)))
+        assert info == want, (n, lda, incx, incy, info)
 
 
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

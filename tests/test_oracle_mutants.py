@@ -53,6 +53,13 @@ MUTANTS = [
      "static long first_index(int n, int inc) { return inc > 0 ? 0 : 0 * n; }\n"
      "#define ORACLE_ABS_INC 1"),
     ("bad_lda_check", None, "if (lda < (n > 1 ? n : 1)) return 5;", "if (lda < 1) return 5;"),
+    ("gemv_transposed", "oracle_gemv_rows",
+     "load_val(kind, A, i + j * (long)lda)", "load_val(kind, A, j + i * (long)lda)"),
+    ("gemv_beta_dropped", "oracle_gemv_rows", "out += be * yi;", "out += yi;"),
+    ("gemv_alpha_dropped", "oracle_gemv_rows", "quad_t out = al * s;", "quad_t out = s;"),
+    ("gemv_last_column_dropped", "oracle_gemv_rows",
+     "for (long j = 0; j < n; j++) {", "for (long j = 0; j + 1 < n; j++) {"),
+    ("gemv_accumulator_double", "oracle_gemv_rows", "quad_t s = 0;", "double s = 0;"),
 ]
 
 
