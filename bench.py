@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kinds", action="store_true",
                     help="skip the one-shot measurements of DSYMV, CHEMV, ZHEMV, WSYMV")
+    ap.add_argument("--no-gemv", action="store_true",
+                    help="skip the SYMV-versus-GEMV comparison")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -242,6 +244,64 @@ def measure_kinds(xs, inputs, torch, peaks, reps=10):
         out.append(rec)
         del pr, A, x, y
         torch.cuda.empty_cache()
+    return out
+
+
+def _time_calls(torch, fn, reps):
+    """average ms of `reps` back-to-back calls (inputs larger than L2)"""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_gemv(xs, inputs, torch, reps=20):
+    """SYMV against the general product GEMV on the same loader (the
+    report's §1 expects SYMV at about twice GEMV's speed when memory-bound),
+    with cuBLAS's GEMV (torch.mv) beside it as an outside reference."""
+    out = []
+    for kind, n, uplo, lda_pad in (("s", 32768, "U", 32), ("d", 24576, "L", 0)):
+        lda = n + lda_pad
+        es = 4 if kind == "s" else 8
+        g = inputs.device_general(kind, n, lda=lda, alpha=1.0, beta=0.0, seed=n)
+        A, x, y = g["A"], g["x"], g["y"]
+        best = None
+        for v in range(xs.xgemv_variant_count(kind)):
+            xs.xgemv_set_variant(kind, v)
+            ms = _time_calls(torch, lambda: xs.check(xs.gemv(kind, n, 1.0, A, lda, x, 1, 0.0, y, 1)),
+                             reps)
+            if best is None or ms < best[0]:
+                best = (ms, xs.xgemv_variant_name(kind, v))
+        xs.xgemv_set_variant(kind, -1)
+        M = A[:, :n].t()                      # M[i, j] = A(i, j), strided view (no copy)
+        cub = _time_calls(torch, lambda: torch.mv(M, x, out=y), reps)
+        del g, A, x, y, M
+        torch.cuda.empty_cache()
+        s = inputs.device_problem(kind, uplo, n, lda=lda, alpha=1.0, beta=0.0, seed=n)
+        sy = _time_calls(torch, lambda: xs.check(xs.symv(kind, uplo, n, 1.0, s["A"], lda, s["x"],
+                                                         1, 0.0, s["y"], 1)), reps)
+        svar = xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))
+        del s
+        torch.cuda.empty_cache()
+        out.append({
+            "kind": kind, "n": n, "lda": lda, "symv_uplo": uplo,
+            "symv_ms": sy, "symv_variant": svar,
+            "gemv_ms": best[0], "gemv_variant": best[1],
+            "gemv_over_symv": best[0] / sy,
+            "symv_gflops": 2.0 * n * n / (sy * 1e-3) / 1e9,
+            "gemv_gflops": 2.0 * n * n / (best[0] * 1e-3) / 1e9,
+            "symv_gbs": n * (n + 1) / 2 * es / (sy * 1e-3) / 1e9,
+            "gemv_gbs": float(n) * n * es / (best[0] * 1e-3) / 1e9,
+            "cublas_gemv_ms": cub, "cublas_gemv_over_symv": cub / sy,
+            "note": "gemv_over_symv ~ 2 when both are memory-bound (half the bytes); ~ 1 when "
+                    "both are FP64-bound (the same n*n multiply-adds)",
+        })
     return out
 
 
@@ -485,6 +545,10 @@ def run_ours(args):
     if rank == 0 and not args.no_kinds and probes:
         kinds = measure_kinds(xs, inputs, torch, {"hbm": peak, **probes})
 
+    gemv_cmp = []
+    if rank == 0 and not args.no_gemv:
+        gemv_cmp = measure_gemv(xs, inputs, torch)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, calls_c, el = cpu_oracle_rate(8192, args.cpu_seconds)
@@ -505,7 +569,7 @@ def run_ours(args):
             "hbm_gbs": triangle_bytes(n) / (ms_per_step * 1e-3) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(), "gpu_launches": launches, "sweep": sweep,
-            "kinds": kinds,
+            "kinds": kinds, "gemv_vs_symv": gemv_cmp,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

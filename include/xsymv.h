@@ -217,6 +217,40 @@ XSYMV_API int xsymv_selected_variant(char kind, char uplo, int n);
  * device (< 0: XSYMV_ERR_*). */
 XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n);
 
+/* ---- the general product, for comparison ------------------------------
+ * "CUDA-xSYMV の実装と評価" (IPSJ 2014-HPC-146), §1 and the abstract:
+ * SYMV reads half the matrix that the general matrix-vector product (GEMV)
+ * reads, so a memory-bound SYMV is expected to run at about twice GEMV's
+ * speed.  These calls are that GEMV, streamed by the same warp loader as the
+ * SYMV kernels, so that the claim can be measured on one GPU:
+ *
+ *   y := alpha*A*x + beta*y,  A an n-by-n general matrix (no symmetry; all
+ *   n*n elements are read), column-major with leading dimension lda, no
+ *   transpose.  A, x and y are DEVICE pointers owned by the caller; A and x
+ *   are read only; y(0..n-1, incy) is the only memory written.  Negative
+ *   incx / incy start from the end (BLAS).  beta = 0 overwrites y without
+ *   reading it; alpha = 0 reads neither A nor x; n = 0 or (alpha = 0,
+ *   beta = 1) returns at once.  Results are bit-identical from run to run
+ *   for a fixed variant, stream and device.  Asynchronous on the library's
+ *   stream, like the SYMV calls.
+ *
+ * Returns 0, or the position of the first bad argument in this signature
+ * (1: n < 0; 4: lda < max(1, n); 6: incx = 0; 9: incy = 0) with nothing
+ * enqueued, or a negative XSYMV_ERR_* code. */
+XSYMV_API int xgemv_s(int n, float alpha, const float *A, int lda, const float *x, int incx,
+                      float beta, float *y, int incy);
+XSYMV_API int xgemv_d(int n, double alpha, const double *A, int lda, const double *x, int incx,
+                      double beta, double *y, int incy);
+
+/* type 's' or 'd': the compiled GEMV variants (names as for the SYMV
+ * register path, "vr<VR>_u<U>_r0_w<W>[_b<B>]"), forcing one (-1: variant 0),
+ * and the index the next call uses.  XSYMV_ERR_VALUE for another type or an
+ * index out of range (count: XSYMV_ERR_VALUE; name: NULL). */
+XSYMV_API int xgemv_variant_count(char type);
+XSYMV_API const char *xgemv_variant_name(char type, int index);
+XSYMV_API int xgemv_set_variant(char type, int index);
+XSYMV_API int xgemv_selected_variant(char type);
+
 #ifdef __cplusplus
 }
 #endif

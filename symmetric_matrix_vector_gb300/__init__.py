@@ -30,7 +30,8 @@ __all__ = [
     "xsymv_workspace_bytes", "XsymvError", "check", "load", "library_path", "ENTRY_POINTS",
     "xsymv_s_host", "xsymv_d_host", "xhemv_c_host", "xhemv_z_host", "xsymv_w_host", "symv_host",
     "xsymv_host_traffic", "xsymv_sync_status", "xsymv_set_wait_limit", "xsymv_test_stall",
-    "xsymv_probe_peaks",
+    "xsymv_probe_peaks", "xgemv_s", "xgemv_d", "gemv", "xgemv_variant_count",
+    "xgemv_variant_name", "xgemv_set_variant", "xgemv_selected_variant",
 ]
 
 ENTRY_POINTS = {"s": "xsymv_s", "d": "xsymv_d", "c": "xhemv_c", "z": "xhemv_z", "w": "xsymv_w"}
@@ -112,6 +113,18 @@ def load():
         lib.xsymv_selected_variant.restype = c_int
         lib.xsymv_workspace_bytes.argtypes = [c_char, c_char, c_int]
         lib.xsymv_workspace_bytes.restype = ctypes.c_longlong
+        for k in ("s", "d"):
+            fn = getattr(lib, "xgemv_" + k)
+            fn.argtypes = [c_int, scal[k], vp, c_int, vp, c_int, scal[k], vp, c_int]
+            fn.restype = c_int
+        lib.xgemv_variant_count.argtypes = [c_char]
+        lib.xgemv_variant_count.restype = c_int
+        lib.xgemv_variant_name.argtypes = [c_char, c_int]
+        lib.xgemv_variant_name.restype = ctypes.c_char_p
+        lib.xgemv_set_variant.argtypes = [c_char, c_int]
+        lib.xgemv_set_variant.restype = c_int
+        lib.xgemv_selected_variant.argtypes = [c_char]
+        lib.xgemv_selected_variant.restype = c_int
         _lib = lib
         return lib
 
@@ -318,3 +331,49 @@ def xsymv_selected_variant(kind: str, uplo: str, n: int) -> int:
 
 def xsymv_workspace_bytes(kind: str, uplo: str, n: int) -> int:
     return load().xsymv_workspace_bytes(kind.encode(), _uplo(uplo), int(n))
+
+
+# ------------------------------------------- the general product (GEMV) --
+
+def _set_stream(lib, stream):
+    s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
+                                                getattr(stream, "cuda_stream", stream))
+    lib.xsymv_set_stream(ctypes.c_void_p(s or 0))
+
+
+def gemv(kind, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    """y := alpha*A*x + beta*y for a general n-by-n A (kind 's' or 'd'),
+    device memory, on the SYMV kernels' loader (xgemv_s / xgemv_d)."""
+    kind = kind.lower()
+    if kind not in ("s", "d"):
+        raise ValueError("gemv kind must be 's' or 'd'")
+    lib = load()
+    _set_stream(lib, stream)
+    return getattr(lib, "xgemv_" + kind)(int(n), _scalar(kind, alpha), ctypes.c_void_p(_ptr(A)),
+                                         int(lda), ctypes.c_void_p(_ptr(x)), int(incx),
+                                         _scalar(kind, beta), ctypes.c_void_p(_ptr(y)), int(incy))
+
+
+def xgemv_s(n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return gemv("s", n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xgemv_d(n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    return gemv("d", n, alpha, A, lda, x, incx, beta, y, incy, stream)
+
+
+def xgemv_variant_count(kind: str) -> int:
+    return load().xgemv_variant_count(kind.encode())
+
+
+def xgemv_variant_name(kind: str, index: int):
+    r = load().xgemv_variant_name(kind.encode(), int(index))
+    return r.decode() if r else None
+
+
+def xgemv_set_variant(kind: str, index: int) -> int:
+    return load().xgemv_set_variant(kind.encode(), int(index))
+
+
+def xgemv_selected_variant(kind: str) -> int:
+    return load().xgemv_selected_variant(kind.encode())

@@ -18,7 +18,8 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIBNAME = "libxsymv.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
-UNITS = ["xsymv_api", "xsymv_probe", "xsymv_s", "xsymv_d", "xsymv_c", "xsymv_z", "xsymv_w"]
+UNITS = ["xsymv_api", "xsymv_probe", "xsymv_s", "xsymv_d", "xsymv_c", "xsymv_z", "xsymv_w",
+         "xsymv_gemv"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                      "-I", INCLUDE]

@@ -202,6 +202,37 @@ struct WarpTile {
     if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc[uo] = red;
   }
 
+  // the lane's rows of the U columns col, col + lda, ... (col: this lane's
+  // first element), with 16-byte vector loads (ALIGNED) or element loads
+  template <bool ALIGNED>
+  __device__ __forceinline__ static void load_cols(const T* col, long long lda,
+                                                   T (&a)[U][VR][VPL]) {
+    if (ALIGNED) {
+      uint4 raw[U][VR];
+      const T* c = col;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int v = 0; v < VR; ++v) raw[u][v] = ldg_stream16(c + v * 32 * VPL);
+        c += lda;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int v = 0; v < VR; ++v) Unpack<T>::run(raw[u][v], a[u][v]);
+    } else {
+      const T* c = col;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int v = 0; v < VR; ++v)
+#pragma unroll
+          for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::load(c + v * 32 * VPL + k);
+        c += lda;
+      }
+    }
+  }
+
   // Columns [ja, jb) of the block row at r0, all NB rows stored, read with
   // 16-byte vector loads (ALIGNED) or element loads straight into registers.
   // The loop keeps only running pointers and a 32-bit count live.
@@ -216,36 +247,68 @@ struct WarpTile {
     for (; left >= U; left -= U) {
       const T xl = (lane < U) ? Ops<T>::load(xp + lane * incx) : Ops<T>::zero();
       T a[U][VR][VPL];
-      if (ALIGNED) {
-        uint4 raw[U][VR];
-        const T* c = col;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int v = 0; v < VR; ++v) raw[u][v] = ldg_stream16(c + v * 32 * VPL);
-          c += lda;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int v = 0; v < VR; ++v) Unpack<T>::run(raw[u][v], a[u][v]);
-      } else {
-        const T* c = col;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int v = 0; v < VR; ++v)
-#pragma unroll
-            for (int k = 0; k < VPL; ++k) a[u][v][k] = Ops<T>::load(c + v * 32 * VPL + k);
-          c += lda;
-        }
-      }
+      load_cols<ALIGNED>(col, lda, a);
       accumulate(a, xl, U, wc, lane);
       col += U * lda;
       xp += U * incx;
       wc += U;
     }
     if (left > 0) masked_cols<false>(A, lda, x, incx, r0, jb - left, jb, wc_row, lane, 0, 0);
+  }
+
+  // ---- the general product (no symmetry): row terms only ----
+
+  // Columns [ja, jb) of the block row at r0 with all NB rows inside the
+  // matrix: racc += A(rows, j) * x(j), the same loads as dense_cols.
+  template <bool ALIGNED>
+  __device__ __forceinline__ void dense_rows(const T* __restrict__ A, long long lda,
+                                             const T* __restrict__ x, int incx, long long r0,
+                                             long long ja, long long jb, int lane) {
+    const T* col = A + ja * lda + r0 + lane_row(0, lane, 0);
+    const T* xp = x + ja * (long long)incx;
+    int left = (int)(jb - ja);
+    for (; left >= U; left -= U) {
+      const T xl = (lane < U) ? Ops<T>::load(xp + lane * incx) : Ops<T>::zero();
+      T a[U][VR][VPL];
+      load_cols<ALIGNED>(col, lda, a);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const T xj = Ops<T>::shfl(xl, u);
+#pragma unroll
+        for (int v = 0; v < VR; ++v)
+#pragma unroll
+          for (int k = 0; k < VPL; ++k) racc[v][k] = Ops<T>::madd(racc[v][k], a[u][v][k], xj);
+      }
+      col += U * lda;
+      xp += U * incx;
+    }
+    if (left > 0) masked_rows(A, lda, x, incx, r0, jb - left, jb, lane, NB);
+  }
+
+  // Columns [ja, jb) of the block row at r0, rows r0 .. r0 + nl - 1 only
+  // (nl <= NB): element loads, U columns per step.
+  __device__ __forceinline__ void masked_rows(const T* __restrict__ A, long long lda,
+                                              const T* __restrict__ x, int incx, long long r0,
+                                              long long ja, long long jb, int lane, int nl) {
+    const T* col = A + ja * lda + r0;
+#pragma unroll 1
+    for (long long j0 = ja; j0 < jb; j0 += U, col += U * lda) {
+      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+      const T xl = (lane < cnt) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
+      const T* c = col;
+#pragma unroll
+      for (int u = 0; u < U; ++u, c += lda) {
+        const T xj = Ops<T>::shfl(xl, u);
+#pragma unroll
+        for (int v = 0; v < VR; ++v)
+#pragma unroll
+          for (int k = 0; k < VPL; ++k) {
+            const int rl = lane_row(v, lane, k);
+            if (u < cnt && rl < nl)
+              racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::load(c + rl), xj);
+          }
+      }
+    }
   }
 
   // issue the bulk copies of chunk c (columns ja + c*U ..) into its stage

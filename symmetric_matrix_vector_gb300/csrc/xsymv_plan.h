@@ -166,4 +166,45 @@ inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int 
 inline long long plan_wc_elems(const Plan& p) { return (long long)p.nb * p.n; }
 inline long long plan_wr_elems(const Plan& p) { return (long long)p.nb * p.qmax * p.NB; }
 
+// ---------------------------------------------------------------------------
+// Partition of the general product y := alpha*A*x + beta*y (all n*n elements
+// of A read), the comparison the report makes in §1.  Block row I (rows
+// I*NB ..) holds n columns of equal cost; the nb*n (block row, column) units
+// are laid out row after row and warp w takes [w*T/W, (w+1)*T/W), T = nb*n.
+// Row partials go to slot q = w - (owner of the row's first column) of the
+// row, as for SYMV; there are no column partials.
+struct GemvPlan {
+  int n;
+  int NB;
+  int nb;
+  int W;      // 1 <= W <= nb*n, so every warp owns at least one unit
+  int qmax;
+};
+
+XSYMV_HD long long gemv_units(const GemvPlan& p) { return (long long)p.nb * p.n; }
+XSYMV_HD long long gemv_wstart(const GemvPlan& p, int w) { return (long long)w * gemv_units(p) / p.W; }
+XSYMV_HD int gemv_owner(const GemvPlan& p, long long s) {
+  return (int)(((s + 1) * p.W - 1) / gemv_units(p));
+}
+XSYMV_HD int gemv_first_owner(const GemvPlan& p, int I) { return gemv_owner(p, (long long)I * p.n); }
+XSYMV_HD int gemv_nq(const GemvPlan& p, int I) {
+  return gemv_owner(p, (long long)I * p.n + p.n - 1) - gemv_first_owner(p, I) + 1;
+}
+
+inline GemvPlan gemv_plan_make(int n, int NB, long long Wmax) {
+  GemvPlan p{};
+  p.n = n;
+  p.NB = NB;
+  p.nb = (n + NB - 1) / NB;
+  const long long units = (long long)p.nb * n;
+  const long long W = Wmax < units ? Wmax : units;
+  p.W = (int)(W < 1 ? 1 : W);
+  p.qmax = 1;
+  for (int I = 0; I < p.nb; ++I) {
+    const int q = gemv_nq(p, I);
+    if (q > p.qmax) p.qmax = q;
+  }
+  return p;
+}
+
 }  // namespace xsymv

@@ -98,3 +98,33 @@ def test_cpu_tensor_is_refused(lib):
     a = torch.zeros(4)
     with pytest.raises(ValueError):
         xs.xsymv_s("U", 2, 1.0, a, 2, a, 1, 0.0, a, 1, stream=0)
+
+
+@pytest.mark.parametrize("kind", ["s", "d"])
+def test_gemv_argument_errors_on_host(lib, kind):
+    bogus = 0x1000
+    f = getattr(xs, "xgemv_" + kind)
+    assert f(-1, 1.0, bogus, 4, bogus, 1, 0.0, bogus, 1, stream=0) == 1
+    assert f(4, 1.0, bogus, 3, bogus, 1, 0.0, bogus, 1, stream=0) == 4
+    assert f(4, 1.0, bogus, 4, bogus, 0, 0.0, bogus, 1, stream=0) == 6
+    assert f(4, 1.0, bogus, 4, bogus, 1, 0.0, bogus, 0, stream=0) == 9
+    assert f(-1, 1.0, bogus, 0, bogus, 0, 0.0, bogus, 0, stream=0) == 1
+    # quick returns touch nothing
+    assert f(0, 1.0, bogus, 1, bogus, 1, 0.0, bogus, 1, stream=0) == 0
+    assert f(5, 0.0, bogus, 5, bogus, 1, 1.0, bogus, 1, stream=0) == 0
+    with pytest.raises(ValueError):
+        xs.gemv("c", 1, 1.0, bogus, 1, bogus, 1, 0.0, bogus, 1)
+
+
+def test_gemv_variants_introspection(lib):
+    for kind in "sd":
+        cnt = xs.xgemv_variant_count(kind)
+        assert cnt >= 1
+        for i in range(cnt):
+            assert re.fullmatch(r"vr\d+_u\d+_r0_w\d+(_b\d+)?", xs.xgemv_variant_name(kind, i))
+        assert xs.xgemv_variant_name(kind, cnt) is None
+        assert xs.xgemv_set_variant(kind, cnt) == -4
+        assert xs.xgemv_set_variant(kind, 1) == 0 and xs.xgemv_selected_variant(kind) == 1
+        assert xs.xgemv_set_variant(kind, -1) == 0 and xs.xgemv_selected_variant(kind) == 0
+    assert xs.xgemv_variant_count("c") == -4
+    assert xs.xgemv_variant_name("c", 0) is None
