@@ -205,6 +205,20 @@ KIND_WORKLOADS = {
 }
 
 
+# FP64 issue rate of GB300: the nominal 1.25 TFLOP/s over 152 SMs x 2 flops x
+# 2.07 GHz is 1.99, i.e. 2 FP64 FMAs per clock per SM.  (A loop of nothing but
+# FP64 FMAs reaches 1.68 per clock; the general product on the same loader
+# reaches 1.88, so the unit itself is faster than the plain FMA loop shows.)
+FP64_PER_CLK_PER_SM = 2
+NOMINAL_SM_MHZ = 2070.0
+
+
+def fp64_issue_peak(torch, sm_max_mhz=None):
+    """FP64 instructions per second at the maximum SM clock"""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return FP64_PER_CLK_PER_SM * sms * (sm_max_mhz or NOMINAL_SM_MHZ) * 1e6
+
+
 def measure_kinds(xs, inputs, torch, peaks, reps=10):
     """One timed measurement per other kind at its workload size (whole
     calls, CUDA events); HBM roofline for c, FP64 ALU roofline for d, z, w."""
@@ -233,11 +247,14 @@ def measure_kinds(xs, inputs, torch, peaks, reps=10):
                "gflops": fl * n * n / (ms * 1e-3) / 1e9, "gbs": gbs,
                "variant": xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))}
         if f64:
-            issue = peaks["fp64_tflops"] * 1e12 / 2          # FP64 instructions per second
-            rec["roofline"] = {"bound": "alu", "unit": "FP64 inst/s",
-                               "achieved": elems * f64 / (ms * 1e-3), "peak": issue,
-                               "frac": elems * f64 / (ms * 1e-3) / issue,
-                               "per_element": f64, "peak_source": "same-run FMA probe"}
+            issue = fp64_issue_peak(torch, peaks.get("sm_max_mhz"))
+            probe = peaks["fp64_tflops"] * 1e12 / 2          # pure-FMA loop, a lower bound
+            ach = elems * f64 / (ms * 1e-3)
+            rec["roofline"] = {"bound": "alu", "unit": "FP64 inst/s", "achieved": ach,
+                               "peak": issue, "frac": ach / issue, "per_element": f64,
+                               "peak_source": "%d FP64 FMA/clock/SM x SMs x max SM clock"
+                                              % FP64_PER_CLK_PER_SM,
+                               "probe_pure_fma": probe, "frac_of_probe": ach / probe}
         else:
             rec["roofline"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs,
                                "peak": peaks["hbm"], "frac": gbs / peaks["hbm"]}
@@ -543,7 +560,8 @@ def run_ours(args):
 
     kinds = []
     if rank == 0 and not args.no_kinds and probes:
-        kinds = measure_kinds(xs, inputs, torch, {"hbm": peak, **probes})
+        kinds = measure_kinds(xs, inputs, torch, {"hbm": peak, **probes,
+                                                  "sm_max_mhz": clocks.summary().get("sm_max_mhz")})
 
     gemv_cmp = []
     if rank == 0 and not args.no_gemv:

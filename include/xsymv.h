@@ -185,9 +185,12 @@ XSYMV_API int xsymv_timing_read(int *calls, double *main_ms, double *call_ms);
 
 /* Roofline denominators measured now on the current device and stream:
  * HBM copy bandwidth (bytes read + written per second, 1 GiB buffers), HBM
- * read bandwidth, and FP64 / FP32 FMA throughput (2 flops per FMA), each the
- * best of a few timed runs.  Allocates and frees two 1 GiB buffers;
- * synchronises the stream.  Any output pointer may be NULL. */
+ * read bandwidth, and FP64 / FP32 FMA throughput (2 flops per FMA) of a loop
+ * of nothing but FMAs, each the best of a few timed runs.  On GB300 the FP64
+ * figure is a lower bound: such a loop issues about 1.68 FP64 FMAs per clock
+ * per SM, while streaming kernels that mix loads and FP64 FMAs sustain more.
+ * Allocates and frees two 1 GiB buffers; synchronises the stream.  Any
+ * output pointer may be NULL. */
 XSYMV_API int xsymv_probe_peaks(double *copy_gbs, double *read_gbs, double *fp64_tflops,
                                 double *fp32_tflops);
 

@@ -14,6 +14,11 @@ static const Variant<double> kVariants_d[] = {
     XSYMV_REG_G(double, 4, 2, 8, 0, 5),
     XSYMV_REG_G(double, 4, 2, 8, 0, 6),
     XSYMV_REG_G(double, 2, 4, 8, 0, 5),
+    XSYMV_REG_GC(double, 4, 2, 8, 0, 5, 8),
+    XSYMV_REG_GC(double, 4, 2, 8, 0, 5, 4),
+    XSYMV_REG_GC(double, 2, 4, 8, 0, 5, 8),
+    XSYMV_REG_GC(double, 4, 2, 8, 0, 5, 16),
+    XSYMV_REG_GC(double, 4, 2, 8, 0, 4, 8),
 };
 static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");
 }  // namespace xsymv

@@ -65,13 +65,13 @@ constexpr int ring_smem_bytes() {
   return WARPS * RingLayout<T, VR, U, S, P>::WARP_BYTES;
 }
 
-template <class T, int VR, int U, int S, int P, int WARPS, int MB>
+template <class T, int VR, int U, int S, int P, int WARPS, int MB, int R = U>
 cudaError_t launch_main(const MainArgs<T>& a) {
   constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
   static bool configured = false;
   if (!configured) {
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB>,
+      cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
     }
@@ -81,24 +81,24 @@ cudaError_t launch_main(const MainArgs<T>& a) {
   const unsigned long long limit = wait_limit_ns();
   const uint32_t extra = test_extra_tx();
   if (a.aligned)
-    symv_main<T, VR, U, S, P, WARPS, true, MB><<<grid, WARPS * 32, smem, a.stream>>>(
+    symv_main<T, VR, U, S, P, WARPS, true, MB, R><<<grid, WARPS * 32, smem, a.stream>>>(
         a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   else
-    symv_main<T, VR, U, S, P, WARPS, false, MB><<<grid, WARPS * 32, 0, a.stream>>>(
+    symv_main<T, VR, U, S, P, WARPS, false, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
         a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
   return cudaGetLastError();
 }
 
-template <class T, int VR, int U, int S, int P, int WARPS, int MB>
+template <class T, int VR, int U, int S, int P, int WARPS, int MB, int R = U>
 int ctas_per_sm() {
   static int cached = 0;
   if (!cached) {
     constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
     int b = 0;
     if (smem > 48 * 1024)
-      cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB>,
+      cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true, MB>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
                                                       WARPS * 32, smem) != cudaSuccess || b < 1) {
       cudaGetLastError();
       b = 1;
@@ -108,11 +108,12 @@ int ctas_per_sm() {
   return cached;
 }
 
-// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>],
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>],
 // pipe r = loads into registers, t = bulk-copy (TMA) ring of STAGES chunks
 // per warp; _b<MINB>: registers capped so that MINB blocks fit on an SM;
 // _x<WAVES>: that many waves of blocks instead of one resident wave;
-// _g<G>: partition cost G of a diagonal-tile column (default DiagCost).
+// _g<G>: partition cost G of a diagonal-tile column (default DiagCost);
+// _c<R>: column reductions batched over R columns (default U).
 #define XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, G, SUF)                              \
   Variant<T> {                                                                            \
     "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
@@ -131,6 +132,13 @@ int ctas_per_sm() {
 #define XSYMV_REG_G(T, VR, U, W, MB, G) \
   XSYMV_VARIANT_G(T, VR, U, 0, kPipeRegisters, "r", W, MB, 1, G, "_b" #MB "_g" #G)
 #define XSYMV_TMA(T, VR, U, S, W) XSYMV_VARIANT_P(T, VR, U, S, kPipeBulk, "t", W, 0, 1, "")
+// column reductions batched over R columns (_c<R>), diagonal cost G
+#define XSYMV_REG_GC(T, VR, U, W, MB, G, R)                                                  \
+  Variant<T> {                                                                              \
+    "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R, 32 * Ops<T>::VPL * (VR), (W), 0,    \
+        kPipeRegisters, 1, (G), &launch_main<T, VR, U, 0, kPipeRegisters, W, MB, R>,           \
+        &ctas_per_sm<T, VR, U, 0, kPipeRegisters, W, MB, R>                                   \
+  }
 
 template <class T>
 cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, T alpha, T beta, int mode,

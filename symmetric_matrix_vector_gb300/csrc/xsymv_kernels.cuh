@@ -236,14 +236,57 @@ struct WarpTile {
   // Columns [ja, jb) of the block row at r0, all NB rows stored, read with
   // 16-byte vector loads (ALIGNED) or element loads straight into registers.
   // The loop keeps only running pointers and a 32-bit count live.
-  template <bool ALIGNED>
+  //
+  // R > U batches the column reductions: the column terms of R columns,
+  // loaded U at a time, are reduced across the warp together, which takes
+  // one butterfly of R values (R - 1 + 5 - log2 R additions per lane) in
+  // place of R/U butterflies of U values, and keeps the shuffles' latency
+  // out of all but one load step in R/U.
+  template <bool ALIGNED, int R = U>
   __device__ __forceinline__ void dense_cols(const T* __restrict__ A, long long lda,
                                              const T* __restrict__ x, int incx, long long r0,
                                              long long ja, long long jb, T* wc_row, int lane) {
+    static_assert(R % U == 0 && R <= 32, "R: a multiple of U, at most 32");
     const T* col = A + ja * lda + r0 + lane_row(0, lane, 0);   // this lane, column ja
     const T* xp = x + ja * (long long)incx;
     T* wc = wc_row + ja;
     int left = (int)(jb - ja);
+    if (R > U) {
+      constexpr int HR = Log2<R>::v;
+      for (; left >= R; left -= R) {
+        const T xl = (lane < R) ? Ops<T>::load(xp + lane * incx) : Ops<T>::zero();
+        T cp[R];
+        // one load step per iteration (not unrolled, so that no more than U
+        // columns of loads are held in registers); the column terms move
+        // down the cp window by U per step, so that after R/U steps cp[i]
+        // holds column i
+#pragma unroll 1
+        for (int s = 0; s < R / U; ++s) {
+          T a[U][VR][VPL];
+          load_cols<ALIGNED>(col, lda, a);
+#pragma unroll
+          for (int i = 0; i < R - U; ++i) cp[i] = cp[i + U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const T xj = Ops<T>::shfl(xl, s * U + u);
+            T c = Ops<T>::zero();
+#pragma unroll
+            for (int v = 0; v < VR; ++v)
+#pragma unroll
+              for (int k = 0; k < VPL; ++k) {
+                racc[v][k] = Ops<T>::madd(racc[v][k], a[u][v][k], xj);
+                c = Ops<T>::maddc(c, a[u][v][k], xi[v][k]);
+              }
+            cp[R - U + u] = c;
+          }
+          col += U * lda;
+        }
+        const T red = reduce_scatter<T, R>(cp, lane);
+        if ((lane & ((32 >> HR) - 1)) == 0) wc[lane >> (5 - HR)] = red;
+        xp += R * incx;
+        wc += R;
+      }
+    }
     for (; left >= U; left -= U) {
       const T xl = (lane < U) ? Ops<T>::load(xp + lane * incx) : Ops<T>::zero();
       T a[U][VR][VPL];
@@ -452,8 +495,10 @@ struct WarpTile {
 // PIPE (see enum Pipe) applies to 16-byte aligned matrices; otherwise
 // off-diagonal columns are read with element loads.  Dynamic shared memory
 // = WARPS * RingLayout::WARP_BYTES.  MINB > 0 asks the compiler to fit MINB
-// blocks per SM (a register cap); 0 leaves the choice to the compiler.
-template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED, int MINB>
+// blocks per SM (a register cap); 0 leaves the choice to the compiler.  R:
+// columns per batched column reduction on the register path (R = U: none).
+template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED, int MINB,
+          int R = U>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
           T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
@@ -537,7 +582,7 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
           return;
         }
       } else {
-        t.template dense_cols<ALIGNED>(A, lda, x, incx, r0, b0, b1, wc_row, lane);
+        t.template dense_cols<ALIGNED, R>(A, lda, x, incx, r0, b0, b1, wc_row, lane);
       }
     }
 

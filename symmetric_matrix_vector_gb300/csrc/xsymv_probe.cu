@@ -19,17 +19,30 @@ __global__ void probe_copy(const uint4* __restrict__ src, uint4* __restrict__ ds
     dst[i] = src[i];
 }
 
+// UNR independent 16-byte loads in flight per thread and iteration
+template <int UNR>
 __global__ void probe_read(const uint4* __restrict__ src, size_t n, unsigned* sink) {
   unsigned acc = 0;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    uint4 v = __ldcs(src + i);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + (UNR - 1) * stride < n; i += UNR * stride) {
+    uint4 v[UNR];
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) v[k] = __ldcs(src + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+  }
+  for (; i < n; i += stride) {
+    const uint4 v = __ldcs(src + i);
     acc ^= v.x ^ v.y ^ v.z ^ v.w;
   }
   if (acc == 0x9e3779b9u) sink[0] = acc;   // practically never; keeps the loads
 }
 
-// 8 independent FMA chains per thread
+// 8 independent FMA chains per thread.  On GB300 a loop of nothing but
+// FP64 FMAs issues at about 1.68 per clock per SM whatever its parallelism,
+// while a memory-streaming FP64 kernel (the general product) sustains 1.88:
+// this is a lower bound of the FP64 rate, not the unit's peak.
 template <class F>
 __global__ void probe_fma(F* out, int iters) {
   F a[8];
@@ -80,12 +93,18 @@ extern "C" XSYMV_API int xsymv_probe_peaks(double* copy_gbs, double* read_gbs,
     e = cudaEventSynchronize(e1);
     const double c = 2.0 * bytes / (elapsed(e0, e1) * 1e-3) / 1e9;
     if (c > best_copy) best_copy = c;
-    cudaEventRecord(e0, st);
-    probe_read<<<grid, block, 0, st>>>((const uint4*)a, n16, (unsigned*)b);
-    cudaEventRecord(e1, st);
-    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
-    const double r = 1.0 * bytes / (elapsed(e0, e1) * 1e-3) / 1e9;
-    if (r > best_read) best_read = r;
+    // two shapes of the read stream; the faster one counts
+    for (int shape = 0; shape < 2 && e == cudaSuccess; ++shape) {
+      cudaEventRecord(e0, st);
+      if (shape == 0)
+        probe_read<4><<<(unsigned)sms * 4, block, 0, st>>>((const uint4*)a, n16, (unsigned*)b);
+      else
+        probe_read<8><<<(unsigned)sms * 4, block, 0, st>>>((const uint4*)a, n16, (unsigned*)b);
+      cudaEventRecord(e1, st);
+      e = cudaEventSynchronize(e1);
+      const double r = 1.0 * bytes / (elapsed(e0, e1) * 1e-3) / 1e9;
+      if (r > best_read) best_read = r;
+    }
   }
   const unsigned fgrid = (unsigned)sms * 8;
   const int iters64 = 1 << 12, iters32 = 1 << 15;
@@ -116,6 +135,6 @@ extern "C" XSYMV_API int xsymv_probe_peaks(double* copy_gbs, double* read_gbs,
   if (read_gbs) *read_gbs = best_read;
   if (fp64_tflops) *fp64_tflops = best64;
   if (fp32_tflops) *fp32_tflops = best32;
-  note_launches(20);
+  note_launches(21);
   return XSYMV_OK;
 }

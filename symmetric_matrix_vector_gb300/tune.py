@@ -112,10 +112,19 @@ def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9):
     return done
 
 
-def choose(done):
-    """best variant per (kind, uplo, n) -> table entries with n_max buckets"""
+def choose(done, index_of=None):
+    """best variant per (kind, uplo, n) -> table entries with n_max buckets.
+
+    ``index_of`` maps (kind, variant name) to the variant's index in the
+    library being tuned; results for names it does not know (variants since
+    removed) are skipped and the indices come from it, not from the results
+    file, whose indices may belong to an older variant table."""
     best = {}
-    for (kind, uplo, n, _name), r in done.items():
+    for (kind, uplo, n, name), r in done.items():
+        if index_of is not None:
+            if (kind, name) not in index_of:
+                continue
+            r = dict(r, variant=index_of[(kind, name)])
         key = (kind, uplo, n)
         if key not in best or r["ms"] < best[key]["ms"]:
             best[key] = r
@@ -168,7 +177,11 @@ def main():
         sizes = {k: ns for k in kinds}
     done = sweep(kinds, sizes, args.uplo.split(","), args.results)
     if args.write_header:
-        write_header(choose(done), args.write_header)
+        import symmetric_matrix_vector_gb300 as xs
+
+        index_of = {(k, xs.xsymv_variant_name(k, i)): i
+                    for k in "sdczw" for i in range(xs.xsymv_variant_count(k))}
+        write_header(choose(done, index_of), args.write_header)
         print("wrote", args.write_header)
 
 

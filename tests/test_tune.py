@@ -1,0 +1,38 @@
+"""Host logic of the offline tuner: choosing the best variant per size bucket
+and rendering the table, without a GPU."""
+from symmetric_matrix_vector_gb300 import tune
+
+
+def rec(kind, uplo, n, variant, name, ms):
+    return {"kind": kind, "uplo": uplo, "n": n, "variant": variant, "variant_name": name,
+            "ms": ms, "gbs": 1.0}
+
+
+def test_choose_picks_fastest_and_buckets():
+    done = {}
+    for r in (rec("s", "U", 4096, 0, "a", 2.0), rec("s", "U", 4096, 1, "b", 1.0),
+              rec("s", "U", 8192, 0, "a", 3.0), rec("s", "U", 8192, 1, "b", 4.0)):
+        done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
+    e = tune.choose(done)
+    assert [(k, u, nmax, r["variant"]) for k, u, nmax, r in e] == [
+        ("s", 1, (4096 + 8192) // 2, 1), ("s", 1, tune.INT_MAX, 0)]
+
+
+def test_choose_maps_names_to_current_indices():
+    # results recorded against an older table: "gone" no longer exists and
+    # "b" moved from index 1 to index 0
+    done = {}
+    for r in (rec("d", "L", 8192, 0, "gone", 0.5), rec("d", "L", 8192, 1, "b", 1.0),
+              rec("d", "L", 8192, 2, "c", 1.5)):
+        done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
+    index_of = {("d", "b"): 0, ("d", "c"): 1}
+    (entry,) = tune.choose(done, index_of)
+    assert entry[3]["variant_name"] == "b" and entry[3]["variant"] == 0
+
+
+def test_render_table_fills_missing_kinds():
+    done = {("z", "U", 16384, "x"): rec("z", "U", 16384, 3, "x", 1.0)}
+    text = tune.render_table(tune.choose(done))
+    assert "{'z', 1, %d, 3}" % tune.INT_MAX in text
+    for k in "sdcw":
+        assert "{'%s', -1, %d, 0}," % (k, tune.INT_MAX) in text
