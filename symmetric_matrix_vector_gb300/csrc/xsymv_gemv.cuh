@@ -77,7 +77,15 @@ gemv_finalize(GemvPlan p, const T* __restrict__ Wr, T alpha, T beta, int mode,
     const int K = (int)(j / p.NB);
     const int nq = gemv_nq(p, K);
     const T* wr = Wr + (long long)K * p.qmax * p.NB + (j - (long long)K * p.NB);
-    for (int q = pp; q < nq; q += kFinParts) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
+    for (int q = pp; q < nq; q += 8 * kFinParts) {   // loads 8 at a time, same order
+      T v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = (q + k * kFinParts < nq) ? wr[(long long)(q + k * kFinParts) * p.NB] : Ops<T>::zero();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (q + k * kFinParts < nq) s = Ops<T>::add(s, v[k]);
+    }
   }
   part[pp][c] = s;
   __syncthreads();

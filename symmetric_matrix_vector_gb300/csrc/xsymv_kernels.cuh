@@ -639,20 +639,29 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
     const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
     const T* wc = Wc + j;
-    // column partials, loads issued in groups of 8 ahead of the (ordered)
-    // additions
-    int I = I0 + pp;
-    for (; I + 7 * kFinParts <= I1; I += 8 * kFinParts) {
+    // column partials I = I0+pp, I0+pp+kFinParts, ... <= I1, then row
+    // partials q = pp, pp+kFinParts, ... < nq, added in that order; loads
+    // are issued 8 at a time (the last group predicated), so a thread waits
+    // for about (count / 8) memory round trips
+    for (int I = I0 + pp; I <= I1; I += 8 * kFinParts) {
       T v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = wc[(long long)(I + k * kFinParts) * p.n];
+      for (int k = 0; k < 8; ++k)
+        v[k] = (I + k * kFinParts <= I1) ? wc[(long long)(I + k * kFinParts) * p.n] : Ops<T>::zero();
 #pragma unroll
-      for (int k = 0; k < 8; ++k) s = Ops<T>::add(s, v[k]);
+      for (int k = 0; k < 8; ++k)
+        if (I + k * kFinParts <= I1) s = Ops<T>::add(s, v[k]);
     }
-    for (; I <= I1; I += kFinParts) s = Ops<T>::add(s, wc[(long long)I * p.n]);
-    // then the row partials q = pp, pp + kFinParts, ...
     if (pp < nq) s = Ops<T>::add(s, wr_first);
-    for (int q = pp + kFinParts; q < nq; q += kFinParts) s = Ops<T>::add(s, wr[(long long)q * p.NB]);
+    for (int q = pp + kFinParts; q < nq; q += 8 * kFinParts) {
+      T v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = (q + k * kFinParts < nq) ? wr[(long long)(q + k * kFinParts) * p.NB] : Ops<T>::zero();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (q + k * kFinParts < nq) s = Ops<T>::add(s, v[k]);
+    }
   }
   part[pp][c] = s;
   __syncthreads();

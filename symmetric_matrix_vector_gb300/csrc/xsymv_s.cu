@@ -18,6 +18,10 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_REG_MBX(float, 1, 2, 8, 6, 4),
     XSYMV_REG_G(float, 1, 2, 8, 6, 5),
     XSYMV_REG_G(float, 1, 2, 8, 6, 7),
+    XSYMV_REG_G(float, 1, 2, 8, 6, 9),
+    XSYMV_REG_G(float, 1, 2, 8, 6, 11),
+    XSYMV_REG_G(float, 1, 2, 8, 0, 9),
+    XSYMV_REG_G(float, 1, 2, 8, 6, 14),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

@@ -14,16 +14,16 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 1},   // vr1_u2_r0_w8 1816.7 GB/s at n=4096
-    {'s', 1, 12288, 1},   // vr1_u2_r0_w8 3622.7 GB/s at n=8192
-    {'s', 1, 20480, 11},   // vr1_u2_r0_w8_b6_g7 5353.5 GB/s at n=16384
-    {'s', 1, 28672, 11},   // vr1_u2_r0_w8_b6_g7 5963.9 GB/s at n=24576
-    {'s', 1, 2147483647, 7},   // vr1_u2_r0_w8_b6 6100.3 GB/s at n=32768
-    {'s', 0, 6144, 3},   // vr1_u4_r0_w4 1813.1 GB/s at n=4096
-    {'s', 0, 12288, 11},   // vr1_u2_r0_w8_b6_g7 3633.7 GB/s at n=8192
-    {'s', 0, 20480, 11},   // vr1_u2_r0_w8_b6_g7 5355.2 GB/s at n=16384
-    {'s', 0, 28672, 11},   // vr1_u2_r0_w8_b6_g7 5917.4 GB/s at n=24576
-    {'s', 0, 2147483647, 11},   // vr1_u2_r0_w8_b6_g7 6124.8 GB/s at n=32768
+    {'s', 1, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1820.0 GB/s at n=4096
+    {'s', 1, 12288, 14},   // vr1_u2_r0_w8_b0_g9 3658.8 GB/s at n=8192
+    {'s', 1, 20480, 13},   // vr1_u2_r0_w8_b6_g11 5352.9 GB/s at n=16384
+    {'s', 1, 28672, 11},   // vr1_u2_r0_w8_b6_g7 5934.3 GB/s at n=24576
+    {'s', 1, 2147483647, 11},   // vr1_u2_r0_w8_b6_g7 6205.6 GB/s at n=32768
+    {'s', 0, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1802.7 GB/s at n=4096
+    {'s', 0, 12288, 14},   // vr1_u2_r0_w8_b0_g9 3643.9 GB/s at n=8192
+    {'s', 0, 20480, 12},   // vr1_u2_r0_w8_b6_g9 5393.9 GB/s at n=16384
+    {'s', 0, 28672, 15},   // vr1_u2_r0_w8_b6_g14 5891.7 GB/s at n=24576
+    {'s', 0, 2147483647, 12},   // vr1_u2_r0_w8_b6_g9 6170.8 GB/s at n=32768
     {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1781.4 GB/s at n=8192
     {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2164.6 GB/s at n=24576
     {'d', 0, 16384, 12},   // vr4_u2_r0_w8_b0_g5_c4 1777.6 GB/s at n=8192
