@@ -41,11 +41,12 @@
  * Ownership: the caller owns A, x and y (device memory, not freed or kept).
  * The library owns a workspace per (device, stream), allocated with
  * cudaMalloc on first use and grown on demand; it lives until the process
- * exits.  Work is enqueued on the stream set by xsymv_set_stream (default:
- * the legacy default stream) and runs asynchronously: when a call returns
- * XSYMV_OK the result is ready once that stream has reached it.  Two calls
- * on the same stream are ordered; calls on different streams use different
- * workspaces.
+ * exits.  The ordered-ticket variants ("_tk", below) also keep a small
+ * ticket buffer per (device, stream), zeroed when it is allocated.  Work is
+ * enqueued on the stream set by xsymv_set_stream (default: the legacy
+ * default stream) and runs asynchronously: when a call returns XSYMV_OK the
+ * result is ready once that stream has reached it.  Two calls on the same
+ * stream are ordered; calls on different streams use different workspaces.
  *
  * Status (return value):
  *   0                 success.
@@ -151,10 +152,14 @@ XSYMV_API int xsymv_set_stream(void *stream);
 XSYMV_API void *xsymv_get_stream(void);
 
 /* ---- failure detection -------------------------------------------------
- * Every wait inside the kernels (for bulk copies landing in shared memory)
- * has a time limit, 2 s by default.  If one runs out, the kernel records
+ * Every wait inside the kernels has a time limit, 2 s by default: waits for
+ * bulk copies landing in shared memory (the "_t" variants) and waits for a
+ * ticket (the "_tk" variants).  If a copy wait runs out, the kernel records
  * the failure in the workspace, waits (again with the limit) for its copies
- * in flight and returns; the call's y is then filled with NaN.
+ * in flight and returns; the call's y is then filled with NaN.  If a ticket
+ * wait runs out, the kernel records the failure and every element of y
+ * whose sum could not be completed is set to NaN (elements whose sums
+ * completed keep their results).
  * xsymv_sync_status waits for the current stream and returns
  * XSYMV_ERR_TIMEOUT if the latest call on it (device, stream) failed that
  * way, else 0 (or XSYMV_ERR_CUDA). */
@@ -162,8 +167,9 @@ XSYMV_API int xsymv_sync_status(void);
 /* Time limit of those waits in ns (0: back to 2 s). */
 XSYMV_API int xsymv_set_wait_limit(unsigned long long ns);
 /* Test hook: on != 0 makes every bulk-copy barrier expect 16 bytes that
- * never arrive, so the next calls' waits run out (nothing faults; the
- * kernels return after the time limit).  0 restores normal operation. */
+ * never arrive, and makes the first contributor of every ticket chain keep
+ * its ticket, so the next calls' waits run out (nothing faults; the kernels
+ * return after the time limit).  0 restores normal operation. */
 XSYMV_API int xsymv_test_stall(int on);
 
 /* Human-readable text for a status code (static storage). */
@@ -201,23 +207,33 @@ XSYMV_API long long xsymv_launch_count(void);
 
 /* kind: 's', 'd', 'c', 'z' or 'w'.  Number of compiled variants (0 for an
  * unknown kind) and the name of variant index: "vr<VR>_u<U>_<p><S>_w<W>"
- * with an optional "_b<B>" = 16-byte vectors per lane (the tile edge is 32
- * lanes x VR vectors), columns per chunk, how off-diagonal columns reach the
- * arithmetic (p = r: 16-byte loads into registers; t: a per-warp
- * shared-memory ring of S chunks filled by bulk (TMA) copies), warps per
- * block, and a register cap that fits B blocks per SM. */
+ * with optional suffixes "_b<B>", "_x<X>", "_g<G>", "_c<R>", "_tk" =
+ * 16-byte vectors per lane (the tile edge is 32 lanes x VR vectors),
+ * columns per load step, how off-diagonal columns reach the arithmetic
+ * (p = r: 16-byte loads into registers; t: a per-warp shared-memory ring of
+ * S chunks filled by bulk (TMA) copies), warps per block, a register cap
+ * that fits B blocks per SM, X waves of blocks, the partition cost G of a
+ * diagonal-tile column (a dense one costs 4), column reductions batched
+ * over R columns, and "_tk": the partial sums are combined by ordered
+ * tickets in the same launch (the report's mechanism, §2.1, figures
+ * "kernel" and "Atomic": dynamic block IDs, one ticket per chunk of NB
+ * outputs passed from contributor to contributor in a fixed order) instead
+ * of by a second, fixed-order reduction kernel.  Both are bit-identical from
+ * run to run; their results differ from each other only in rounding. */
 XSYMV_API int xsymv_variant_count(char kind);
 XSYMV_API const char *xsymv_variant_name(char kind, int index);
 
 /* Force variant index for kind (-1: the built-in tuned choice).
- * Returns 0 or XSYMV_ERR_VALUE. */
+ * Returns 0 or XSYMV_ERR_VALUE.  xsymv_s_noalloc refuses a forced "_tk"
+ * variant (XSYMV_ERR_VALUE, nothing enqueued): it has no ticket buffer. */
 XSYMV_API int xsymv_set_variant(char kind, int index);
 
 /* The variant index a call of this kind, uplo and n would use. */
 XSYMV_API int xsymv_selected_variant(char kind, char uplo, int n);
 
 /* Workspace bytes a call of this kind, uplo and n needs on the current
- * device (< 0: XSYMV_ERR_*). */
+ * device (< 0: XSYMV_ERR_*); a "_tk" variant's ticket buffer (256 bytes
+ * + 32 bytes per chunk of NB outputs) is not included. */
 XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n);
 
 /* ---- the general product, for comparison ------------------------------

@@ -163,6 +163,67 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
   return w->ptr;
 }
 
+namespace {
+struct TkEntry {
+  int device;
+  cudaStream_t stream;
+  void* ptr;
+  size_t bytes;
+  unsigned long long call;   // last call number handed out
+};
+std::vector<TkEntry> g_tk;
+}  // namespace
+
+void* ticket_buffer(size_t bytes, cudaStream_t stream, int* status, unsigned long long* call) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    *status = XSYMV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  TkEntry* t = nullptr;
+  for (TkEntry& c : g_tk)
+    if (c.device == d && c.stream == stream) t = &c;
+  if (t == nullptr) {
+    g_tk.push_back(TkEntry{d, stream, nullptr, 0, 0});
+    t = &g_tk.back();
+  }
+  if (t->bytes < bytes) {
+    if (t->ptr != nullptr) {
+      // the old buffer may still be in use by work queued on `stream`
+      e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess) e = cudaFree(t->ptr);
+      t->ptr = nullptr;
+      t->bytes = 0;
+      if (e != cudaSuccess) {
+        record_cuda_error(e);
+        *status = XSYMV_ERR_CUDA;
+        return nullptr;
+      }
+    }
+    e = cudaMalloc(&t->ptr, bytes);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      cudaGetLastError();
+      t->ptr = nullptr;
+      *status = XSYMV_ERR_ALLOC;
+      return nullptr;
+    }
+    // zero counters, and tickets that name no call (call numbers start at 1)
+    e = cudaMemsetAsync(t->ptr, 0, bytes, stream);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      *status = XSYMV_ERR_CUDA;
+      return nullptr;
+    }
+    t->bytes = bytes;
+  }
+  *call = ++t->call;
+  return t->ptr;
+}
+
 unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
 uint32_t test_extra_tx() { return g_extra_tx.load(); }
 

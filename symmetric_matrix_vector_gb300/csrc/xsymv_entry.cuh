@@ -1,5 +1,6 @@
 // Host dispatch shared by the five entry points: BLAS argument checks, quick
-// returns, variant choice, work partition, workspace and the two launches.
+// returns, variant choice, work partition, workspace and the launches (main
+// kernel and finaliser, or the one ordered-ticket kernel).
 #pragma once
 
 #include <stdint.h>
@@ -7,6 +8,7 @@
 
 #include "../../include/xsymv.h"
 #include "xsymv_kernels.cuh"
+#include "xsymv_ticket.cuh"
 #include "xsymv_runtime.h"
 #include "xsymv_tuned.h"
 
@@ -44,6 +46,14 @@ struct MainArgs {
   int epoch;
   bool aligned;    // A and lda*sizeof(T) on the 16-byte grid
   cudaStream_t stream;
+  // ordered-ticket variants only: the final merge happens in the same launch
+  T* v;                       // n running sums (in the workspace, after Wr)
+  void* tk;                   // ticket buffer (counters, then the tickets)
+  unsigned long long call;    // the call's number in the tickets
+  T alpha, beta;
+  int mode;                   // kFull or kBetaZero
+  T* y0;                      // logical element 0 of y
+  long long incy;
 };
 
 // One compiled configuration of the main kernel.
@@ -58,6 +68,7 @@ struct Variant {
   int diag_cost;  // partition cost of a diagonal-tile column (a dense one costs kDenseCost)
   cudaError_t (*launch)(const MainArgs<T>&);
   int (*ctas_per_sm)();
+  int accum;   // enum Accum: workspace + finaliser, or ordered tickets (launch does it all)
 };
 
 template <class T, int VR, int U, int S, int P, int WARPS>
@@ -108,12 +119,58 @@ int ctas_per_sm() {
   return cached;
 }
 
-// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>],
+// The ordered-ticket kernel (register path): one launch streams the triangle,
+// chains the partial sums through the tickets and writes y.
+template <class T, int VR, int U, int WARPS, int MB, int R>
+cudaError_t launch_ticket(const MainArgs<T>& a) {
+  const unsigned grid = (unsigned)((a.plan.W + WARPS - 1) / WARPS);
+  TicketCtx<T> c;
+  c.Wc = a.Wc;
+  c.Wr = a.Wr;
+  c.v = a.v;
+  c.tk = reinterpret_cast<unsigned long long*>(static_cast<char*>(a.tk) + kTkHeaderBytes);
+  c.status = a.status;
+  c.epoch = a.epoch;
+  c.call = a.call;
+  c.limit_ns = wait_limit_ns();
+  c.withhold = test_extra_tx() != 0;
+  c.alpha = a.alpha;
+  c.beta = a.beta;
+  c.mode = a.mode;
+  c.y = a.y0;
+  c.incy = a.incy;
+  int* ctr = static_cast<int*>(a.tk);
+  if (a.aligned)
+    symv_ticket<T, VR, U, WARPS, true, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, ctr, c);
+  else
+    symv_ticket<T, VR, U, WARPS, false, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, ctr, c);
+  return cudaGetLastError();
+}
+
+template <class T, int VR, int U, int WARPS, int MB, int R>
+int ctas_per_sm_ticket() {
+  static int cached = 0;
+  if (!cached) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_ticket<T, VR, U, WARPS, true, MB, R>,
+                                                      WARPS * 32, 0) != cudaSuccess || b < 1) {
+      cudaGetLastError();
+      b = 1;
+    }
+    cached = b;
+  }
+  return cached;
+}
+
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>][_tk],
 // pipe r = loads into registers, t = bulk-copy (TMA) ring of STAGES chunks
 // per warp; _b<MINB>: registers capped so that MINB blocks fit on an SM;
 // _x<WAVES>: that many waves of blocks instead of one resident wave;
 // _g<G>: partition cost G of a diagonal-tile column (default DiagCost);
-// _c<R>: column reductions batched over R columns (default U).
+// _c<R>: column reductions batched over R columns (default U);
+// _tk: ordered tickets instead of the workspace finaliser (symv_ticket).
 #define XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, G, SUF)                              \
   Variant<T> {                                                                            \
     "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
@@ -138,6 +195,14 @@ int ctas_per_sm() {
     "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R, 32 * Ops<T>::VPL * (VR), (W), 0,    \
         kPipeRegisters, 1, (G), &launch_main<T, VR, U, 0, kPipeRegisters, W, MB, R>,           \
         &ctas_per_sm<T, VR, U, 0, kPipeRegisters, W, MB, R>                                   \
+  }
+
+// ordered tickets (register path): diagonal cost G, batched reductions R
+#define XSYMV_TICKET(T, VR, U, W, MB, G, R)                                                     \
+  Variant<T> {                                                                                \
+    "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R "_tk", 32 * Ops<T>::VPL * (VR), (W), 0, \
+        kPipeRegisters, 1, (G), &launch_ticket<T, VR, U, W, MB, R>,                            \
+        &ctas_per_sm_ticket<T, VR, U, W, MB, R>, kAccumTickets                                 \
   }
 
 template <class T>
@@ -189,6 +254,7 @@ struct Workload {
   const Variant<T>* variant;
   long long wc_off;     // byte offset of Wc in the workspace
   long long wr_off;     // byte offset of Wr
+  long long v_off;      // byte offset of v (ordered-ticket variants)
   long long bytes;      // total workspace bytes
 };
 
@@ -210,7 +276,12 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   out->variant = v;
   out->wc_off = kHeaderBytes;
   out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
-  out->bytes = out->wr_off + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
+  out->v_off = out->wr_off + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
+  out->bytes = out->v_off;
+  if (v->accum == kAccumTickets) {
+    if (out->plan.W >= (1 << kTkWarpBits)) return XSYMV_ERR_VALUE;
+    out->bytes += align_up((long long)n * (long long)sizeof(T), 256);
+  }
   return XSYMV_OK;
 }
 
@@ -258,6 +329,28 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
                 (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
                     (((long long)lda * (long long)sizeof(T)) % 16 == 0),
                 st};
+  if (wl.variant->accum == kAccumTickets) {
+    // one launch: the kernel also applies y = alpha*s + beta*y
+    const long long tk_bytes = kTkHeaderBytes + (long long)wl.plan.nb * kTkStride * 8;
+    m.tk = ticket_buffer((size_t)tk_bytes, st, &status, &m.call);
+    if (!m.tk) return status;
+    m.v = reinterpret_cast<T*>(ws + wl.v_off);
+    m.alpha = alpha;
+    m.beta = beta;
+    m.mode = bz ? kBetaZero : kFull;
+    m.y0 = y0;
+    m.incy = incy;
+    timing_begin(st);
+    cudaError_t e = wl.variant->launch(m);
+    timing_mid(st);
+    timing_end(st);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+    return XSYMV_OK;
+  }
   timing_begin(st);
   cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {

@@ -490,46 +490,22 @@ struct WarpTile {
 };
 
 // ----------------------------------------------------------------------------
-// main kernel
+// one warp's share of the triangle
 // ----------------------------------------------------------------------------
-// PIPE (see enum Pipe) applies to 16-byte aligned matrices; otherwise
-// off-diagonal columns are read with element loads.  Dynamic shared memory
-// = WARPS * RingLayout::WARP_BYTES.  MINB > 0 asks the compiler to fit MINB
-// blocks per SM (a register cap); 0 leaves the choice to the compiler.  R:
-// columns per batched column reduction on the register path (R = U: none).
-template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED, int MINB,
-          int R = U>
-__global__ void __launch_bounds__(WARPS * 32, MINB)
-symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
-          T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
-          unsigned long long limit_ns, uint32_t extra_tx) {
+// For every block row I in which warp w owns columns: the columns of the
+// diagonal tile (masked), then the off-diagonal ones (through the ring when
+// RING, else straight into registers), column partials to Wc[I*n + j], then
+// the row partial to the warp's slot of row I in Wr.  Returns false if a
+// bounded wait of the ring ran out (the warp then stops at once).
+template <class T, int VR, int U, int STAGES, bool RING, bool ALIGNED, int R>
+__device__ __forceinline__ bool stream_warp(const Plan& p, int w, int lane, Ring& rg,
+                                            const T* __restrict__ A, long long lda,
+                                            const T* __restrict__ x, int incx,
+                                            T* __restrict__ Wc, T* __restrict__ Wr,
+                                            unsigned long long limit_ns) {
   using Tile = WarpTile<T, VR, U>;
-  using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
-  constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
   constexpr int VPL = Tile::VPL;
   constexpr int NB = Tile::NB;
-  // let the finaliser (launched as a programmatic dependent) get scheduled as
-  // blocks of this grid retire; it waits for this grid's completion itself
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int wl = threadIdx.x >> 5;
-  const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
-  if (w >= p.W) return;
-
-  Ring rg{0u, 0u, 0, 0u, extra_tx};
-  if (RING) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* base = smem + (size_t)wl * Lay::WARP_BYTES;
-    rg.data = smem_addr(base);
-    rg.bars = smem_addr(base + Lay::DATA_BYTES);
-    if (lane == 0) {
-#pragma unroll
-      for (int s = 0; s < (STAGES > 0 ? STAGES : 1); ++s) mbar_init(rg.bars + 8u * s, 1);
-      mbar_init_fence();
-    }
-    __syncwarp();
-  }
-
   // this warp's cost range [cs, ce); it owns the columns whose first cost
   // unit lies in it
   const long long ce = plan_wstart(p, w + 1);
@@ -577,10 +553,8 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
         t.template masked_cols<true>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
       } else if (RING) {
         if (!t.template dense_cols_ring<(STAGES > 0 ? STAGES : 1)>(rg, A, lda, x, incx, r0, b0, b1,
-                                                                   wc_row, lane, limit_ns)) {
-          if (lane == 0) atomicMax(status, epoch);
-          return;
-        }
+                                                                   wc_row, lane, limit_ns))
+          return false;
       } else {
         t.template dense_cols<ALIGNED, R>(A, lda, x, incx, r0, b0, b1, wc_row, lane);
       }
@@ -595,6 +569,49 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
 #pragma unroll
       for (int k = 0; k < VPL; ++k) wr[Tile::lane_row(v, lane, k)] = t.racc[v][k];
   }
+  return true;
+}
+
+// ----------------------------------------------------------------------------
+// main kernel
+// ----------------------------------------------------------------------------
+// PIPE (see enum Pipe) applies to 16-byte aligned matrices; otherwise
+// off-diagonal columns are read with element loads.  Dynamic shared memory
+// = WARPS * RingLayout::WARP_BYTES.  MINB > 0 asks the compiler to fit MINB
+// blocks per SM (a register cap); 0 leaves the choice to the compiler.  R:
+// columns per batched column reduction on the register path (R = U: none).
+template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED, int MINB,
+          int R = U>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
+          T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
+          unsigned long long limit_ns, uint32_t extra_tx) {
+  using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
+  constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
+  // let the finaliser (launched as a programmatic dependent) get scheduled as
+  // blocks of this grid retire; it waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int wl = threadIdx.x >> 5;
+  const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  if (w >= p.W) return;
+
+  Ring rg{0u, 0u, 0, 0u, extra_tx};
+  if (RING) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* base = smem + (size_t)wl * Lay::WARP_BYTES;
+    rg.data = smem_addr(base);
+    rg.bars = smem_addr(base + Lay::DATA_BYTES);
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < (STAGES > 0 ? STAGES : 1); ++s) mbar_init(rg.bars + 8u * s, 1);
+      mbar_init_fence();
+    }
+    __syncwarp();
+  }
+  if (!stream_warp<T, VR, U, STAGES, RING, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr,
+                                                       limit_ns))
+    if (lane == 0) atomicMax(status, epoch);
 }
 
 // ----------------------------------------------------------------------------

@@ -167,6 +167,100 @@ inline long long plan_wc_elems(const Plan& p) { return (long long)p.nb * p.n; }
 inline long long plan_wr_elems(const Plan& p) { return (long long)p.nb * p.qmax * p.NB; }
 
 // ---------------------------------------------------------------------------
+// Ordered tickets (the report's own accumulation, "CUDA-xSYMV の実装と評価"
+// §2.1, figures "kernel" and "Atomic"): the partial sums of output chunk K
+// (outputs K*NB .. K*NB+NB-1) are added into one vector in a fixed order,
+// one contributing warp at a time, each handing a ticket to the next.
+//
+// Contributors of chunk K are the warps that wrote a column partial of one
+// of its columns or a row partial of block row K.  In row I they form the
+// contiguous warp range "link range t" below:
+//   upper: t = I = 0 .. K (column partials of rows I < K; all owners of row
+//          K, whose first columns are chunk K's diagonal tile),
+//   lower: t = I - K = 0 .. nb-1-K (all owners of row K, whose last columns
+//          are the diagonal tile; then column partials of rows I > K).
+// The ranges are sorted (their first and last warps never decrease with t),
+// so ordering the contributors by warp index orders them by block row, and a
+// warp waits only for warps with smaller indices.
+
+// columns [ja, jb) of block row I owned by warp w; false if it owns none
+XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long long* jb) {
+  const long long cs = plan_wstart(p, w), ce = plan_wstart(p, w + 1);
+  const long long rcs = plan_rowstart(p, I), rce = rcs + plan_rowcost(p, I);
+  const long long lo = cs > rcs ? cs : rcs, hi = ce < rce ? ce : rce;
+  if (lo >= hi) return false;
+  const long long c0 = plan_cols_before(p, I, lo - rcs), c1 = plan_cols_before(p, I, hi - rcs);
+  if (c0 >= c1) return false;
+  *ja = plan_colbase(p, I) + c0;
+  *jb = plan_colbase(p, I) + c1;
+  return true;
+}
+
+// number of link ranges of chunk K
+XSYMV_HD int plan_links(const Plan& p, int K) { return p.upper ? K + 1 : p.nb - K; }
+
+// first and last warp of link range t of chunk K
+XSYMV_HD void plan_link_range(const Plan& p, int K, int t, int* wa, int* wb) {
+  const int I = p.upper ? t : K + t;
+  if (I == K) {
+    *wa = plan_first_owner(p, K);
+    *wb = plan_last_owner(p, K);
+    return;
+  }
+  const long long cb = plan_colbase(p, I), rs = plan_rowstart(p, I);
+  const long long j0 = (long long)K * p.NB;
+  const long long j1 = ((long long)K + 1) * p.NB < p.n ? ((long long)K + 1) * p.NB : (long long)p.n;
+  *wa = plan_owner(p, rs + plan_col_cost(p, I, j0 - cb));
+  *wb = plan_owner(p, rs + plan_col_cost(p, I, j1 - 1 - cb));
+}
+
+// the first contributor of chunk K (it starts the chain without waiting)
+XSYMV_HD int plan_chain_first(const Plan& p, int K) {
+  int wa, wb;
+  plan_link_range(p, K, 0, &wa, &wb);
+  return wa;
+}
+
+// the contributor of chunk K that follows warp w, or -1 if w is the last
+// (binary search for the first link range that ends after w)
+XSYMV_HD int plan_chain_next(const Plan& p, int K, int w) {
+  int lo = 0, hi = plan_links(p, K);   // answer in [lo, hi]; hi = none
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    int wa, wb;
+    plan_link_range(p, K, mid, &wa, &wb);
+    if (wb > w) hi = mid; else lo = mid + 1;
+  }
+  if (lo == plan_links(p, K)) return -1;
+  int wa, wb;
+  plan_link_range(p, K, lo, &wa, &wb);
+  return wa > w + 1 ? wa : w + 1;
+}
+
+// the smallest chunk > after that a warp owning columns [ja, jb) of block
+// row I contributes to from that row (its row partial goes to chunk I, its
+// column partials to the chunks of its columns); a large value if none
+XSYMV_HD int plan_row_next_chunk(const Plan& p, int I, long long ja, long long jb, int after) {
+  int best = I > after ? I : 0x7fffffff;
+  const int a = (int)(ja / p.NB), b = (int)((jb - 1) / p.NB);
+  const int c = after + 1 > a ? after + 1 : a;
+  return (c <= b && c < best) ? c : best;
+}
+
+// the smallest chunk > after that warp w contributes to, with its rows
+// [Ia, Ib] (a large value if there is none)
+XSYMV_HD int plan_warp_next_chunk(const Plan& p, int w, int Ia, int Ib, int after) {
+  int best = 0x7fffffff;
+  for (int I = Ia; I <= Ib; ++I) {
+    long long ja, jb;
+    if (!plan_warp_cols(p, w, I, &ja, &jb)) continue;
+    const int c = plan_row_next_chunk(p, I, ja, jb, after);
+    if (c < best) best = c;
+  }
+  return best;
+}
+
+// ---------------------------------------------------------------------------
 // Partition of the general product y := alpha*A*x + beta*y (all n*n elements
 // of A read), the comparison the report makes in §1.  Block row I (rows
 // I*NB ..) holds n columns of equal cost; the nb*n (block row, column) units

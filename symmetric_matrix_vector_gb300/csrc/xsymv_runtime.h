@@ -23,6 +23,12 @@ bool current_device(int* dev, int* sm_count);
 // kernels write to the status word if they give up on a wait.
 void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch);
 
+// buffer of at least `bytes` for the ordered-ticket kernels on (current
+// device, stream): zeroed when it is allocated, written by nothing but those
+// kernels.  *call receives a fresh call number (>= 1, never reused for the
+// buffer) that the kernel's tickets carry.  nullptr and *status set on failure.
+void* ticket_buffer(size_t bytes, cudaStream_t stream, int* status, unsigned long long* call);
+
 // time limit of every bounded wait in the kernels
 unsigned long long wait_limit_ns();
 // extra bytes announced on every ring barrier: 0, except when a test makes

@@ -22,6 +22,9 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_REG_G(float, 1, 2, 8, 6, 11),
     XSYMV_REG_G(float, 1, 2, 8, 0, 9),
     XSYMV_REG_G(float, 1, 2, 8, 6, 14),
+    XSYMV_TICKET(float, 1, 2, 8, 6, 9, 2),
+    XSYMV_TICKET(float, 1, 2, 8, 0, 9, 2),
+    XSYMV_TICKET(float, 2, 2, 8, 0, 6, 2),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv
@@ -157,6 +160,8 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   Workload<float> wl;
   status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
   if (status) return status;
+  // the ordered-ticket kernels keep state in a second, allocated buffer
+  if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;
   if (wl.bytes > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
   char* ws = static_cast<char*>(scratch);
   MainArgs<float> m{wl.plan, A, lda, x0, incx, reinterpret_cast<float*>(ws + wl.wc_off),

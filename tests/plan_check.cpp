@@ -1,10 +1,14 @@
 // Brute-force check of the work partition in xsymv_plan.h (host logic of the
 // CUDA library): simulates the main kernel's per-warp loop and verifies that
 // every column segment of the stored triangle is owned exactly once, that the
-// row-partial slots of each block row have no holes, and that the finaliser's
-// block-row ranges are exactly the rows holding each column.
+// row-partial slots of each block row have no holes, that the finaliser's
+// block-row ranges are exactly the rows holding each column, and that the
+// ordered-ticket chains visit exactly the contributors of every output chunk,
+// in increasing warp order.
 #include <cstdio>
+#include <algorithm>
 #include <cstdlib>
+#include <set>
 #include <vector>
 
 #include "xsymv_plan.h"
@@ -84,6 +88,62 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
         return fail("column cost", n, NB, upper, Wmax, cd, cg);
     }
     if (d != std::min<long long>(NB, n - (long long)I * NB)) return fail("dlen", n, NB, upper, Wmax, cd, cg);
+  }
+  // ordered tickets: contributors of chunk K = owners of its columns in any
+  // row, plus the warps holding row K's partial slots
+  std::vector<std::set<int>> contrib(nb);
+  std::vector<std::set<int>> chunks_of(p.W);
+  for (int I = 0; I < nb; ++I) {
+    const long long cb = plan_colbase(p, I);
+    for (size_t c = 0; c < own[I].size(); ++c) {
+      const int K = (int)((cb + (long long)c) / NB);
+      contrib[K].insert(own[I][c]);
+      chunks_of[own[I][c]].insert(K);
+    }
+    for (int w : row_warps[I]) {
+      contrib[I].insert(w);
+      chunks_of[w].insert(I);
+    }
+  }
+  for (int K = 0; K < nb; ++K) {
+    const std::vector<int> v(contrib[K].begin(), contrib[K].end());
+    if (v.empty() || plan_chain_first(p, K) != v[0])
+      return fail("chain first", n, NB, upper, Wmax, cd, cg);
+    for (size_t k = 0; k < v.size(); ++k) {
+      const int want_next = k + 1 < v.size() ? v[k + 1] : -1;
+      if (plan_chain_next(p, K, v[k]) != want_next)
+        return fail("chain next", n, NB, upper, Wmax, cd, cg);
+    }
+    // link ranges sorted by first and last warp
+    int pa = -1, pb = -1;
+    for (int t = 0; t < plan_links(p, K); ++t) {
+      int wa, wb;
+      plan_link_range(p, K, t, &wa, &wb);
+      if (wa < pa || wb < pb || wa > wb) return fail("link ranges", n, NB, upper, Wmax, cd, cg);
+      pa = wa;
+      pb = wb;
+    }
+  }
+  if (p.W >= (1 << 24)) return fail("warp bits", n, NB, upper, Wmax, cd, cg);
+  for (int w = 0; w < p.W; ++w) {
+    const int Ia = plan_row_of(p, plan_wstart(p, w));
+    const int Ib = plan_row_of(p, plan_wstart(p, w + 1) - 1);
+    std::vector<int> got;
+    for (int K = plan_warp_next_chunk(p, w, Ia, Ib, -1); K < nb;
+         K = plan_warp_next_chunk(p, w, Ia, Ib, K))
+      got.push_back(K);
+    if (got != std::vector<int>(chunks_of[w].begin(), chunks_of[w].end()))
+      return fail("warp chunks", n, NB, upper, Wmax, cd, cg);
+    for (int I = Ia; I <= Ib; ++I) {
+      long long ja, jb;
+      const bool has = plan_warp_cols(p, w, I, &ja, &jb);
+      const bool want = std::find(row_warps[I].begin(), row_warps[I].end(), w) != row_warps[I].end();
+      if (has != want) return fail("warp cols", n, NB, upper, Wmax, cd, cg);
+      for (long long c = 0; has && c < (long long)own[I].size(); ++c) {
+        const long long j = plan_colbase(p, I) + c;
+        if ((own[I][c] == w) != (j >= ja && j < jb)) return fail("warp cols range", n, NB, upper, Wmax, cd, cg);
+      }
+    }
   }
   return 0;
 }
