@@ -60,6 +60,8 @@ def parse_args():
                     help="skip the one-shot measurements of DSYMV, CHEMV, ZHEMV, WSYMV")
     ap.add_argument("--no-gemv", action="store_true",
                     help="skip the SYMV-versus-GEMV comparison")
+    ap.add_argument("--no-tickets", action="store_true",
+                    help="skip the ordered-ticket versus workspace comparison")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -279,6 +281,53 @@ def _time_calls(torch, fn, reps):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / reps
+
+
+def ticket_variants(xs, kind):
+    return [i for i in range(xs.xsymv_variant_count(kind))
+            if xs.xsymv_variant_name(kind, i).endswith("_tk")]
+
+
+def time_variant(xs, torch, kind, variant, fn, reps):
+    """average ms of one call with `variant` forced for `kind`"""
+    assert xs.xsymv_set_variant(kind, variant) == 0
+    try:
+        return _time_calls(torch, fn, reps)
+    finally:
+        xs.xsymv_set_variant(kind, -1)
+
+
+def measure_tickets(xs, inputs, torch, reps=10):
+    """The report's ordered tickets (one launch; dynamic block IDs, per-chunk
+    tickets passed in block order) against the workspace reduction (main
+    kernel + fixed-order finaliser), both bit-identical run to run: whole
+    calls at each kind's workload, the tuned workspace variant against the
+    fastest ticket variant."""
+    cases = [("s", "U", 32768, 32, 1.0, 0.0, {}), ("s", "U", 8192, 32, 1.0, 0.0, {}),
+             ("d", "L", 24576, 0, -0.75, 2.0, dict(dist="normal", diag_shift=4.0)),
+             ("c", "U", 16384, 0, complex(1, 0.5), complex(0.5, -0.25), {}),
+             ("z", "U", 16384, 0, complex(1, 0.5), complex(0.5, -0.25), {}),
+             ("w", "L", 8192, 0, (1.0, 0.0), (1.0, 0.0), {})]
+    out = []
+    for kind, uplo, n, pad, al, be, kw in cases:
+        lda = n + pad
+        pr = inputs.device_problem(kind, uplo, n, lda=lda, alpha=al, beta=be, seed=n, **kw)
+
+        def call():
+            xs.check(xs.symv(kind, uplo, n, al, pr["A"], lda, pr["x"], 1, be, pr["y"], 1))
+
+        ws_v = xs.xsymv_selected_variant(kind, uplo, n)
+        ws = time_variant(xs, torch, kind, ws_v, call, reps)
+        tk = sorted((time_variant(xs, torch, kind, v, call, reps), v)
+                    for v in ticket_variants(xs, kind))
+        out.append({"kind": kind, "workload": "%s n=%d uplo=%s lda=%d" % (kind, n, uplo, lda),
+                    "workspace_ms": ws, "workspace_variant": xs.xsymv_variant_name(kind, ws_v),
+                    "tickets_ms": tk[0][0], "tickets_variant": xs.xsymv_variant_name(kind, tk[0][1]),
+                    "tickets_over_workspace": tk[0][0] / ws,
+                    "all_ticket_variants_ms": {xs.xsymv_variant_name(kind, v): t for t, v in tk}})
+        del pr
+        torch.cuda.empty_cache()
+    return out
 
 
 def measure_gemv(xs, inputs, torch, reps=20):
@@ -577,6 +626,10 @@ def run_ours(args):
     if rank == 0 and not args.no_gemv:
         gemv_cmp = measure_gemv(xs, inputs, torch)
 
+    tickets = []
+    if rank == 0 and not args.no_tickets:
+        tickets = measure_tickets(xs, inputs, torch)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, calls_c, el = cpu_oracle_rate(8192, args.cpu_seconds)
@@ -597,7 +650,7 @@ def run_ours(args):
             "hbm_gbs": triangle_bytes(n) / (ms_per_step * 1e-3) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(), "gpu_launches": launches, "sweep": sweep,
-            "kinds": kinds, "gemv_vs_symv": gemv_cmp,
+            "kinds": kinds, "gemv_vs_symv": gemv_cmp, "tickets_vs_workspace": tickets,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

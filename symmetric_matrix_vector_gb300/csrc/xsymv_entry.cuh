@@ -279,7 +279,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   out->v_off = out->wr_off + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
   out->bytes = out->v_off;
   if (v->accum == kAccumTickets) {
-    if (out->plan.W >= (1 << kTkWarpBits)) return XSYMV_ERR_VALUE;
+    if (out->plan.W >= (1 << kTkIdBits)) return XSYMV_ERR_VALUE;
     out->bytes += align_up((long long)n * (long long)sizeof(T), 256);
   }
   return XSYMV_OK;

@@ -183,9 +183,10 @@ inline long long plan_wr_elems(const Plan& p) { return (long long)p.nb * p.qmax 
 // so ordering the contributors by warp index orders them by block row, and a
 // warp waits only for warps with smaller indices.
 
-// columns [ja, jb) of block row I owned by warp w; false if it owns none
-XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long long* jb) {
-  const long long cs = plan_wstart(p, w), ce = plan_wstart(p, w + 1);
+// columns [ja, jb) of block row I whose first cost unit lies in [cs, ce);
+// false if there are none
+XSYMV_HD bool plan_cost_cols(const Plan& p, long long cs, long long ce, int I, long long* ja,
+                             long long* jb) {
   const long long rcs = plan_rowstart(p, I), rce = rcs + plan_rowcost(p, I);
   const long long lo = cs > rcs ? cs : rcs, hi = ce < rce ? ce : rce;
   if (lo >= hi) return false;
@@ -193,6 +194,22 @@ XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long lo
   if (c0 >= c1) return false;
   *ja = plan_colbase(p, I) + c0;
   *jb = plan_colbase(p, I) + c1;
+  return true;
+}
+
+// columns [ja, jb) of block row I owned by warp w; false if it owns none
+XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long long* jb) {
+  return plan_cost_cols(p, plan_wstart(p, w), plan_wstart(p, w + 1), I, ja, jb);
+}
+
+// columns of block row I owned by warps w0 .. w1-1 (a contiguous run,
+// their union) and those warps' row-partial slots qa .. qb in the row
+XSYMV_HD bool plan_group_cols(const Plan& p, int w0, int w1, int I, long long* ja, long long* jb,
+                              int* qa, int* qb) {
+  if (!plan_cost_cols(p, plan_wstart(p, w0), plan_wstart(p, w1), I, ja, jb)) return false;
+  const int f = plan_first_owner(p, I), l = plan_last_owner(p, I);
+  *qa = (w0 > f ? w0 : f) - f;
+  *qb = (w1 - 1 < l ? w1 - 1 : l) - f;
   return true;
 }
 
@@ -237,6 +254,20 @@ XSYMV_HD int plan_chain_next(const Plan& p, int K, int w) {
   return wa > w + 1 ? wa : w + 1;
 }
 
+// The same chains between groups of G consecutive warps (group g = warps
+// g*G .. g*G+G-1, e.g. the warps of one thread block): a group contributes
+// to chunk K if any of its warps does, and groups follow each other in
+// increasing order.  The first group of chunk K:
+XSYMV_HD int plan_group_first(const Plan& p, int K, int G) { return plan_chain_first(p, K) / G; }
+
+// the group after group g in chunk K's chain, or -1 if g is the last
+XSYMV_HD int plan_group_next(const Plan& p, int K, int g, int G) {
+  const long long e = ((long long)g + 1) * G;
+  const int last = (int)((e < p.W ? e : (long long)p.W) - 1);   // g's last warp
+  const int nx = plan_chain_next(p, K, last);
+  return nx < 0 ? -1 : nx / G;
+}
+
 // the smallest chunk > after that a warp owning columns [ja, jb) of block
 // row I contributes to from that row (its row partial goes to chunk I, its
 // column partials to the chunks of its columns); a large value if none
@@ -247,13 +278,13 @@ XSYMV_HD int plan_row_next_chunk(const Plan& p, int I, long long ja, long long j
   return (c <= b && c < best) ? c : best;
 }
 
-// the smallest chunk > after that warp w contributes to, with its rows
-// [Ia, Ib] (a large value if there is none)
-XSYMV_HD int plan_warp_next_chunk(const Plan& p, int w, int Ia, int Ib, int after) {
+// the smallest chunk > after that warps w0 .. w1-1 contribute to, with
+// their rows [Ia, Ib] (a large value if there is none)
+XSYMV_HD int plan_group_next_chunk(const Plan& p, int w0, int w1, int Ia, int Ib, int after) {
   int best = 0x7fffffff;
   for (int I = Ia; I <= Ib; ++I) {
     long long ja, jb;
-    if (!plan_warp_cols(p, w, I, &ja, &jb)) continue;
+    if (!plan_cost_cols(p, plan_wstart(p, w0), plan_wstart(p, w1), I, &ja, &jb)) continue;
     const int c = plan_row_next_chunk(p, I, ja, jb, after);
     if (c < best) best = c;
   }

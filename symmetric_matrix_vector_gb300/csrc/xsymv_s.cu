@@ -25,6 +25,7 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_TICKET(float, 1, 2, 8, 6, 9, 2),
     XSYMV_TICKET(float, 1, 2, 8, 0, 9, 2),
     XSYMV_TICKET(float, 2, 2, 8, 0, 6, 2),
+    XSYMV_TICKET(float, 2, 2, 8, 4, 6, 2),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

@@ -13,26 +13,28 @@
 //     warp w = ID * WARPS + warp-in-block streams the share of the triangle
 //     that warp w owns in the partition of xsymv_plan.h (column partials to
 //     Wc, row partials to Wr, exactly as symv_main does).
-//   * Then, for every output chunk K it contributed to, the warp waits for
-//     chunk K's ticket to name it, adds its own partial sums of the chunk
-//     (in a fixed order) into v, and hands the ticket to the next
-//     contributor.  The contributors of a chunk are ordered by warp index;
-//     the first one starts the chain by storing, the last one applies
-//     y = alpha*(v + its part) + beta*y.  No addition's order depends on
-//     timing, so results are bit-identical from run to run.
-//   * A warp waits only for warps with smaller indices, which started
-//     earlier (dynamic IDs), so the chain always progresses.  Every wait
-//     still has a time limit: when it runs out the warp marks the call
-//     failed (status word := the call's epoch), writes NaN to the outputs of
-//     every chunk it had not completed, and stops; the chains it would have
-//     continued then run out too, so every output whose sum did not
-//     complete is NaN.  Another warp that sees the failure stops the same
-//     way without waiting for its own limit.
+//   * Then the block's warps, which own consecutive column ranges, act as one
+//     contributor: for every output chunk K the block contributed to, one of
+//     its warps waits for chunk K's ticket to name the block, adds the
+//     block's partial sums of the chunk (in a fixed order) into v, and hands
+//     the ticket to the next contributing block.  Contributors of a chunk
+//     are ordered by block ID; the first one starts the chain by storing,
+//     the last one applies y = alpha*(v + its part) + beta*y.  No
+//     addition's order depends on timing, so results are bit-identical from
+//     run to run.
+//   * A block waits only for blocks with smaller IDs, which started earlier
+//     (dynamic IDs), so the chain always progresses.  Every wait still has
+//     a time limit: when it runs out the warp marks the call failed (status
+//     word := the call's epoch), writes NaN to the outputs of every chunk it
+//     had not completed, and stops; the chains it would have continued then
+//     run out too, so every output whose sum did not complete is NaN.
+//     Another warp that sees the failure stops the same way without waiting
+//     for its own limit.
 //   * The last block to finish resets the two block counters.
 //
-// Tickets are 64-bit words "(call << 24) | warp" in a buffer that only these
+// Tickets are 64-bit words "(call << 24) | block" in a buffer that only these
 // kernels write; the call number grows by one per launch, so a ticket left by
-// an earlier call can never name a warp of this one.
+// an earlier call can never name a block of this one.
 #pragma once
 
 #include "xsymv_kernels.cuh"
@@ -46,7 +48,8 @@ constexpr int kTkStart = 0;
 constexpr int kTkDone = 8;
 constexpr long long kTkHeaderBytes = 256;
 constexpr int kTkStride = 4;
-constexpr int kTkWarpBits = 24;   // warp index bits of a ticket
+constexpr int kTkIdBits = 24;     // block ID bits of a ticket
+constexpr int kTkRows = 32;       // block rows of a block kept in shared memory
 
 enum Accum {
   kAccumWorkspace = 0,   // symv_main + symv_finalize (fixed-order sums of the workspace)
@@ -61,6 +64,12 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long r;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ int ld_relaxed_int(const int* p) {
   int r;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
@@ -119,46 +128,26 @@ struct TicketCtx {
   long long incy;
 };
 
-// Warp w's block rows Ia..Ib: lane l < 32 caches row Ia + l (the columns
-// [ja, jb) it owns there and its row-partial slot q), so that the ticket
-// phase needs no plan arithmetic per link; rows past the first 32 (only
-// when a warp's share spans more than 32 block rows) are recomputed.
-struct WarpRows {
-  int Ia, Ib;
-  bool own;          // this lane's row: does the warp own columns there
-  long long ja, jb;  // and which
-  int q;             // its slot among the row's warps
+// A block's share of one block row: the columns [ja, jb) its warps own
+// (ja >= jb: none) and their row-partial slots qa .. qb.
+struct GroupRow {
+  long long ja, jb;
+  int qa, qb;
 };
 
-__device__ __forceinline__ WarpRows warp_rows(const Plan& p, int w, int lane) {
-  WarpRows r;
-  r.Ia = plan_row_of(p, plan_wstart(p, w));
-  r.Ib = plan_row_of(p, plan_wstart(p, w + 1) - 1);
-  r.own = false;
-  r.ja = r.jb = 0;
-  r.q = 0;
-  const int I = r.Ia + lane;
-  if (I <= r.Ib) {
-    r.own = plan_warp_cols(p, w, I, &r.ja, &r.jb);
-    if (r.own) r.q = w - plan_first_owner(p, I);
-  }
-  return r;
-}
+// the group's rows Ia..Ib; rows Ia .. Ia+kTkRows-1 are in shared memory,
+// later ones (only when a block's share spans more block rows) recomputed
+struct GroupRows {
+  int w0, w1;          // warps of the group
+  int Ia, Ib;
+  const GroupRow* sm;  // kTkRows entries
+};
 
-// row I's entry (every lane calls this for the same I)
-__device__ __forceinline__ bool row_cols(const Plan& p, const WarpRows& r, int w, int I,
-                                         long long* ja, long long* jb, int* q) {
-  const int l = I - r.Ia;
-  if (l < 32) {
-    const bool own = __shfl_sync(0xffffffffu, r.own, l);
-    *ja = __shfl_sync(0xffffffffu, r.ja, l);
-    *jb = __shfl_sync(0xffffffffu, r.jb, l);
-    *q = __shfl_sync(0xffffffffu, r.q, l);
-    return own;
-  }
-  if (!plan_warp_cols(p, w, I, ja, jb)) return false;
-  *q = w - plan_first_owner(p, I);
-  return true;
+__device__ __forceinline__ GroupRow group_row(const Plan& p, const GroupRows& g, int I) {
+  if (I - g.Ia < kTkRows) return g.sm[I - g.Ia];
+  GroupRow r{0, 0, 0, -1};
+  if (!plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb, &r.qa, &r.qb)) r.ja = r.jb = 0;
+  return r;
 }
 
 __device__ __forceinline__ int warp_min(int v) {
@@ -170,51 +159,48 @@ __device__ __forceinline__ int warp_min(int v) {
   return v;
 }
 
-// the smallest chunk > after that warp w contributes to (>= nb if none)
-__device__ __forceinline__ int next_chunk(const Plan& p, const WarpRows& r, int w, int lane,
-                                          int after) {
-  int best = (r.Ia + lane <= r.Ib && r.own) ? plan_row_next_chunk(p, r.Ia + lane, r.ja, r.jb, after)
-                                            : 0x7fffffff;
+// the smallest chunk > after that the group contributes to (>= nb if none);
+// lane l looks at row Ia + l
+__device__ __forceinline__ int next_chunk(const Plan& p, const GroupRows& g, int lane, int after) {
+  int best = 0x7fffffff;
+  if (lane < kTkRows && g.Ia + lane <= g.Ib) {
+    const GroupRow r = g.sm[lane];
+    if (r.ja < r.jb) best = plan_row_next_chunk(p, g.Ia + lane, r.ja, r.jb, after);
+  }
   best = warp_min(best);
 #pragma unroll 1
-  for (int I = r.Ia + 32; I <= r.Ib; ++I) {
-    long long ja, jb;
-    if (!plan_warp_cols(p, w, I, &ja, &jb)) continue;
-    const int c = plan_row_next_chunk(p, I, ja, jb, after);
+  for (int I = g.Ia + kTkRows; I <= g.Ib; ++I) {
+    const GroupRow r = group_row(p, g, I);
+    if (r.ja >= r.jb) continue;
+    const int c = plan_row_next_chunk(p, I, r.ja, r.jb, after);
     best = c < best ? c : best;
   }
   return best;
 }
 
-// Warp w's partial sums of chunk K: lane l holds outputs K*NB + l + 32m,
-// m < M.  Column partials of its rows in increasing row order, the row
-// partial of block row K after row K's column partials; has[m] is false
-// where the warp has no term.  Offsets within the chunk are 32-bit.
+// The group's partial sums of chunk K, added to s[m] (lane l holds outputs
+// K*NB + l + 32m, m < M): column partials of its rows in increasing row
+// order, then, in row K, the row partials of its slots in slot order.
+// has[m] is false where there was no term yet.  Offsets are 32-bit.
 template <class T, int M>
 __device__ __forceinline__ void chunk_part(const Plan& p, const TicketCtx<T>& c,
-                                           const WarpRows& rows, int w, int K, int lane,
-                                           T (&s)[M], bool (&has)[M]) {
+                                           const GroupRows& g, int K, int lane, T (&s)[M],
+                                           bool (&has)[M]) {
   const long long k0 = (long long)K * p.NB;
   const int live = (int)((long long)p.n - k0 < p.NB ? (long long)p.n - k0 : p.NB);
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    s[m] = Ops<T>::zero();
-    has[m] = false;
-  }
 #pragma unroll 1
-  for (int I = rows.Ia; I <= rows.Ib; ++I) {
-    long long ja, jb;
-    int q;
-    if (!row_cols(p, rows, w, I, &ja, &jb, &q)) continue;
+  for (int I = g.Ia; I <= g.Ib; ++I) {
+    const GroupRow r = group_row(p, g, I);
+    if (r.ja >= r.jb) continue;
     // this row's columns of the chunk, relative to its first column
-    const int lo = (int)((ja > k0 ? ja : k0) - k0);
-    const int hi = (int)((jb < k0 + p.NB ? jb : k0 + p.NB) - k0);
+    const int lo = (int)((r.ja > k0 ? r.ja : k0) - k0);
+    const int hi = (int)((r.jb < k0 + p.NB ? r.jb : k0 + p.NB) - k0);
     if (lo < hi) {
       const T* wc = c.Wc + (long long)I * p.n + k0 + lane;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const int r = lane + 32 * m;
-        if (r >= lo && r < hi) {
+        const int o = lane + 32 * m;
+        if (o >= lo && o < hi) {
           const T t = ld_l2(wc + 32 * m);
           s[m] = has[m] ? Ops<T>::add(s[m], t) : t;
           has[m] = true;
@@ -222,13 +208,16 @@ __device__ __forceinline__ void chunk_part(const Plan& p, const TicketCtx<T>& c,
       }
     }
     if (I == K) {
-      const T* wr = c.Wr + ((long long)K * p.qmax + q) * p.NB + lane;
+#pragma unroll 1
+      for (int q = r.qa; q <= r.qb; ++q) {
+        const T* wr = c.Wr + ((long long)K * p.qmax + q) * p.NB + lane;
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        if (lane + 32 * m < live) {
-          const T t = ld_l2(wr + 32 * m);
-          s[m] = has[m] ? Ops<T>::add(s[m], t) : t;
-          has[m] = true;
+        for (int m = 0; m < M; ++m) {
+          if (lane + 32 * m < live) {
+            const T t = ld_l2(wr + 32 * m);
+            s[m] = has[m] ? Ops<T>::add(s[m], t) : t;
+            has[m] = true;
+          }
         }
       }
     }
@@ -247,30 +236,26 @@ __device__ __forceinline__ void chunk_nan(const Plan& p, const TicketCtx<T>& c, 
     if (lane + 32 * m < live) yk[m * step] = Ops<T>::nan();
 }
 
-// Warp w's link in chunk K's chain, once the ticket names it (or it is the
-// first contributor): add its part into v and pass the ticket to `next`, or,
-// as the last contributor (next < 0), write the chunk's outputs of y.
+// The group's link in chunk K's chain, once the ticket names it (or it is
+// the first contributor): add its part into v and pass the ticket to group
+// `next`, or, as the last contributor (next < 0), write the chunk's outputs.
 template <class T, int M>
 __device__ __forceinline__ void chunk_link(const Plan& p, const TicketCtx<T>& c,
-                                           const WarpRows& rows, int w, int K, bool first,
-                                           int next, int lane) {
+                                           const GroupRows& g, int K, bool first, int next,
+                                           int lane) {
   const long long k0 = (long long)K * p.NB;
   const int live = (int)((long long)p.n - k0 < p.NB ? (long long)p.n - k0 : p.NB);
+  T* vk = c.v + k0 + lane;
   T s[M];
   bool has[M];
-  chunk_part<T, M>(p, c, rows, w, K, lane, s, has);
-  T* vk = c.v + k0 + lane;
-  if (!first) {
-    // the chain so far: v, then this warp's part
+  // the chain so far (v) first, then this group's part: the loads of both
+  // are in flight together
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      if (lane + 32 * m < live && (has[m] || next < 0)) {
-        const T t = ld_l2(vk + 32 * m);
-        s[m] = has[m] ? Ops<T>::add(t, s[m]) : t;
-        has[m] = true;
-      }
-    }
+  for (int m = 0; m < M; ++m) {
+    has[m] = !first && lane + 32 * m < live;
+    s[m] = has[m] ? ld_l2(vk + 32 * m) : Ops<T>::zero();
   }
+  chunk_part<T, M>(p, c, g, K, lane, s, has);
   if (next < 0) {
     T* yk = c.y + (k0 + lane) * c.incy;
     const long long step = 32 * c.incy;
@@ -288,37 +273,48 @@ __device__ __forceinline__ void chunk_link(const Plan& p, const TicketCtx<T>& c,
     return;
   }
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    // the first contributor defines every element of the chunk
-    if (lane + 32 * m < live && (has[m] || first))
-      st_l2(vk + 32 * m, has[m] ? s[m] : Ops<T>::zero());
-  }
+  for (int m = 0; m < M; ++m)
+    if (lane + 32 * m < live) st_l2(vk + 32 * m, has[m] ? s[m] : Ops<T>::zero());
   __threadfence();   // this lane's stores to v are visible before the ticket moves
   __syncwarp();
   if (lane == 0 && !(c.withhold && first))
-    st_release_u64(c.tk + (long long)K * kTkStride, (c.call << kTkWarpBits) | (unsigned)next);
+    st_release_u64(c.tk + (long long)K * kTkStride, (c.call << kTkIdBits) | (unsigned)next);
 }
 
-// The ticket phase of warp w (after it has streamed its share): every chunk
-// it contributed to, up to 32 at a time (lane k polls the k-th), each linked
-// as soon as its ticket names this warp.
+// The ticket phase of group (block) gid after all its warps have streamed
+// their shares: the group's chunks in increasing order, dealt round-robin to
+// its warps (warp `wl` of `nw` takes entries wl, wl + nw, ...); each warp
+// polls up to 32 of its chunks at once (lane k the k-th) and links each as
+// soon as its ticket names the group.
 template <class T, int NB>
-__device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& c, int w,
+__device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& c,
+                                             const GroupRows& g, int gid, int G, int wl, int nw,
                                              int lane) {
   constexpr int M = NB / 32;
-  const WarpRows rows = warp_rows(p, w, lane);
-  const unsigned long long mine = (c.call << kTkWarpBits) | (unsigned)w;
+  const unsigned long long mine = (c.call << kTkIdBits) | (unsigned)gid;
   const long long limit =
       (long long)(c.limit_ns < (1ull << 61) ? c.limit_ns : (1ull << 61)) * 2;   // <= 2 GHz
-  int done_upto = -1;   // chunks <= done_upto are linked
+  int cur = -1;   // the group's chunks <= cur have been dealt
 #pragma unroll 1
   for (;;) {
-    int ck = -1, cnt = 0, cur = done_upto;
+    // this warp's next batch: every nw-th chunk of the group's list
+    int ck = -1, cnt = 0;
 #pragma unroll 1
-    for (; cnt < 32; ++cnt) {
-      const int K = next_chunk(p, rows, w, lane, cur);
-      if (K >= p.nb) break;
-      if (lane == cnt) ck = K;
+    while (cnt < 32) {
+      int K = cur;
+#pragma unroll 1
+      for (int i = 0; i < nw; ++i) {
+        K = next_chunk(p, g, lane, K);
+        if (K >= p.nb) break;
+        if (i == wl) {
+          if (lane == cnt) ck = K;
+          ++cnt;
+        }
+      }
+      if (K >= p.nb) {
+        cur = p.nb;
+        break;
+      }
       cur = K;
     }
     if (cnt == 0) return;
@@ -326,28 +322,32 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
     int first = -1, next = -1;
     bool ready = false;
     if (pending) {
-      first = plan_chain_first(p, ck);
-      next = plan_chain_next(p, ck, w);
-      ready = first == w;
+      first = plan_group_first(p, ck, G);
+      next = plan_group_next(p, ck, gid, G);
+      ready = first == gid;
     }
     long long t0 = clock64();
     int spins = 0;
     bool failed = false;
     while (__any_sync(0xffffffffu, pending)) {
-      if (pending && !ready) ready = ld_acquire_u64(c.tk + (long long)ck * kTkStride) == mine;
+      if (pending && !ready && ld_relaxed_u64(c.tk + (long long)ck * kTkStride) == mine) {
+        fence_acq_rel();   // with the relaxed load that saw it: acquire the link before
+        ready = true;
+      }
       const unsigned rm = __ballot_sync(0xffffffffu, pending && ready);
       if (rm) {
         const int k = __ffs(rm) - 1;
         const int K = __shfl_sync(0xffffffffu, ck, k);
-        const bool f = __shfl_sync(0xffffffffu, first, k) == w;
+        const bool f = __shfl_sync(0xffffffffu, first, k) == gid;
         const int nx = __shfl_sync(0xffffffffu, next, k);
         __syncwarp();   // lane k's acquire orders the other lanes' reads of v
-        chunk_link<T, M>(p, c, rows, w, K, f, nx, lane);
+        chunk_link<T, M>(p, c, g, K, f, nx, lane);
         if (lane == k) pending = false;
         t0 = clock64();
         spins = 0;
         continue;
       }
+      __nanosleep(32);
       if ((++spins & 63) == 0) {
         const bool out = clock64() - t0 > limit || ld_relaxed_int(c.status) == c.epoch;
         if (__any_sync(0xffffffffu, out)) {
@@ -358,7 +358,7 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
     }
     if (failed) {
       if (lane == 0) atomicMax(c.status, c.epoch);
-      // this batch's unlinked chunks, then every later chunk of the warp
+      // this batch's unlinked chunks, then this warp's share of the rest
       unsigned left = __ballot_sync(0xffffffffu, pending);
 #pragma unroll 1
       while (left) {
@@ -366,34 +366,55 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
         chunk_nan<T, M>(p, c, __shfl_sync(0xffffffffu, ck, k), lane);
         left &= left - 1;
       }
+      int K = cur;
 #pragma unroll 1
-      for (int K = next_chunk(p, rows, w, lane, cur); K < p.nb; K = next_chunk(p, rows, w, lane, K))
-        chunk_nan<T, M>(p, c, K, lane);
+      for (int i = 0; (K = next_chunk(p, g, lane, K)) < p.nb; ++i)
+        if (i % nw == wl) chunk_nan<T, M>(p, c, K, lane);
       return;
     }
-    done_upto = cur;
   }
 }
 
-// One launch: dynamic block IDs, the warp's share of the stream (register
-// path, as symv_main), then its links.  ctr: the ticket buffer's counters.
+// One launch: dynamic block IDs, the warps' shares of the stream (register
+// path, as symv_main), then the block's links.  ctr: the ticket buffer's
+// counters.
 template <class T, int VR, int U, int WARPS, bool ALIGNED, int MINB, int R = U>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_ticket(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
             T* Wc, T* Wr, int* ctr, TicketCtx<T> c) {
   constexpr int NB = WarpTile<T, VR, U>::NB;
   __shared__ int s_blk;
+  __shared__ GroupRow s_rows[kTkRows];
   if (threadIdx.x == 0) s_blk = atomicAdd(ctr + kTkStart, 1);
   __syncthreads();
+  const int blk = s_blk;
   const int lane = threadIdx.x & 31;
-  const int w = s_blk * WARPS + (int)(threadIdx.x >> 5);
+  const int wl = (int)(threadIdx.x >> 5);
+  const int w = blk * WARPS + wl;
   if (w < p.W) {
     Ring rg{0u, 0u, 0, 0u, 0u};
     stream_warp<T, VR, U, 1, false, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr,
                                                 c.limit_ns);
-    __syncwarp();   // the warp's workspace writes are visible to all its lanes
-    ticket_phase<T, NB>(p, c, w, lane);
   }
+  // the block's warps act as one contributor: their workspace writes are
+  // visible to the whole block after the barrier
+  GroupRows g;
+  g.w0 = blk * WARPS;
+  g.w1 = g.w0 + WARPS < p.W ? g.w0 + WARPS : p.W;
+  g.sm = s_rows;
+  if (g.w0 < p.W) {
+    g.Ia = plan_row_of(p, plan_wstart(p, g.w0));
+    g.Ib = plan_row_of(p, plan_wstart(p, g.w1) - 1);
+    if ((int)threadIdx.x < kTkRows) {
+      GroupRow r{0, 0, 0, -1};
+      const int I = g.Ia + (int)threadIdx.x;
+      if (I > g.Ib || !plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb, &r.qa, &r.qb))
+        r.ja = r.jb = 0;
+      s_rows[threadIdx.x] = r;
+    }
+  }
+  __syncthreads();
+  if (g.w0 < p.W) ticket_phase<T, NB>(p, c, g, blk, WARPS, wl, WARPS, lane);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();

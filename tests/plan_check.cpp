@@ -125,23 +125,50 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
     }
   }
   if (p.W >= (1 << 24)) return fail("warp bits", n, NB, upper, Wmax, cd, cg);
-  for (int w = 0; w < p.W; ++w) {
-    const int Ia = plan_row_of(p, plan_wstart(p, w));
-    const int Ib = plan_row_of(p, plan_wstart(p, w + 1) - 1);
-    std::vector<int> got;
-    for (int K = plan_warp_next_chunk(p, w, Ia, Ib, -1); K < nb;
-         K = plan_warp_next_chunk(p, w, Ia, Ib, K))
-      got.push_back(K);
-    if (got != std::vector<int>(chunks_of[w].begin(), chunks_of[w].end()))
-      return fail("warp chunks", n, NB, upper, Wmax, cd, cg);
-    for (int I = Ia; I <= Ib; ++I) {
-      long long ja, jb;
-      const bool has = plan_warp_cols(p, w, I, &ja, &jb);
-      const bool want = std::find(row_warps[I].begin(), row_warps[I].end(), w) != row_warps[I].end();
-      if (has != want) return fail("warp cols", n, NB, upper, Wmax, cd, cg);
-      for (long long c = 0; has && c < (long long)own[I].size(); ++c) {
-        const long long j = plan_colbase(p, I) + c;
-        if ((own[I][c] == w) != (j >= ja && j < jb)) return fail("warp cols range", n, NB, upper, Wmax, cd, cg);
+  // the same chains between groups of G consecutive warps (thread blocks)
+  for (int G : {1, 3, 8}) {
+    const int ng = (p.W + G - 1) / G;
+    for (int K = 0; K < nb; ++K) {
+      std::set<int> gs;
+      for (int w : contrib[K]) gs.insert(w / G);
+      const std::vector<int> v(gs.begin(), gs.end());
+      if (plan_group_first(p, K, G) != v[0]) return fail("group first", n, NB, upper, Wmax, cd, cg);
+      for (size_t k = 0; k < v.size(); ++k) {
+        const int want_next = k + 1 < v.size() ? v[k + 1] : -1;
+        if (plan_group_next(p, K, v[k], G) != want_next)
+          return fail("group next", n, NB, upper, Wmax, cd, cg);
+      }
+    }
+    for (int g = 0; g < ng; ++g) {
+      const int w0 = g * G, w1 = std::min(p.W, w0 + G);
+      const int Ia = plan_row_of(p, plan_wstart(p, w0));
+      const int Ib = plan_row_of(p, plan_wstart(p, w1) - 1);
+      std::set<int> want;
+      for (int w = w0; w < w1; ++w) want.insert(chunks_of[w].begin(), chunks_of[w].end());
+      std::vector<int> got;
+      for (int K = plan_group_next_chunk(p, w0, w1, Ia, Ib, -1); K < nb;
+           K = plan_group_next_chunk(p, w0, w1, Ia, Ib, K))
+        got.push_back(K);
+      if (got != std::vector<int>(want.begin(), want.end()))
+        return fail("group chunks", n, NB, upper, Wmax, cd, cg);
+      for (int I = Ia; I <= Ib; ++I) {
+        long long ja, jb;
+        int qa, qb;
+        const bool has = plan_group_cols(p, w0, w1, I, &ja, &jb, &qa, &qb);
+        // the group's columns are the union of its warps' columns, and its
+        // slots are exactly the slots of its warps that own columns there
+        std::vector<int> slots;
+        for (int w : row_warps[I])
+          if (w >= w0 && w < w1) slots.push_back(w - plan_first_owner(p, I));
+        if (has != !slots.empty()) return fail("group cols", n, NB, upper, Wmax, cd, cg);
+        if (!has) continue;
+        if (qa != slots.front() || qb != slots.back() || (int)slots.size() != qb - qa + 1)
+          return fail("group slots", n, NB, upper, Wmax, cd, cg);
+        for (long long c = 0; c < (long long)own[I].size(); ++c) {
+          const long long j = plan_colbase(p, I) + c;
+          const bool mine = own[I][c] >= w0 && own[I][c] < w1;
+          if (mine != (j >= ja && j < jb)) return fail("group cols range", n, NB, upper, Wmax, cd, cg);
+        }
       }
     }
   }
