@@ -1,6 +1,7 @@
 // Host runtime of the xsymv library: stream selection, workspace cache,
 // launch counter, event timing, status strings and variant overrides.
 // The five compute entry points live in xsymv_{s,d,c,z,w}.cu.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -222,6 +223,76 @@ void* ticket_buffer(size_t bytes, cudaStream_t stream, int* status, unsigned lon
   }
   *call = ++t->call;
   return t->ptr;
+}
+
+namespace {
+struct TabEntry {
+  int device;
+  cudaStream_t stream;
+  void* ptr;
+  size_t bytes;
+  std::vector<unsigned char> key;   // the plan whose tables the buffer holds (empty: none)
+};
+std::vector<TabEntry> g_tab;
+
+TabEntry* tab_entry(int d, cudaStream_t stream) {
+  for (TabEntry& t : g_tab)
+    if (t.device == d && t.stream == stream) return &t;
+  return nullptr;
+}
+}  // namespace
+
+void* plan_tables(size_t bytes, cudaStream_t stream, const void* key, size_t key_bytes,
+                  bool* ready, int* status) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    *status = XSYMV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  TabEntry* t = tab_entry(d, stream);
+  if (t == nullptr) {
+    g_tab.push_back(TabEntry{d, stream, nullptr, 0, {}});
+    t = &g_tab.back();
+  }
+  if (t->bytes < bytes) {
+    t->key.clear();
+    if (t->ptr != nullptr) {
+      // the old buffer may still be in use by work queued on `stream`
+      e = cudaStreamSynchronize(stream);
+      if (e == cudaSuccess) e = cudaFree(t->ptr);
+      t->ptr = nullptr;
+      t->bytes = 0;
+      if (e != cudaSuccess) {
+        record_cuda_error(e);
+        *status = XSYMV_ERR_CUDA;
+        return nullptr;
+      }
+      bytes += bytes / 8;
+    }
+    e = cudaMalloc(&t->ptr, bytes);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      cudaGetLastError();
+      t->ptr = nullptr;
+      *status = XSYMV_ERR_ALLOC;
+      return nullptr;
+    }
+    t->bytes = bytes;
+  }
+  const unsigned char* k = static_cast<const unsigned char*>(key);
+  *ready = t->key.size() == key_bytes && std::equal(t->key.begin(), t->key.end(), k);
+  if (!*ready) t->key.assign(k, k + key_bytes);
+  return t->ptr;
+}
+
+void plan_tables_forget(cudaStream_t stream) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (TabEntry* t = tab_entry(d, stream)) t->key.clear();
 }
 
 unsigned long long wait_limit_ns() { return g_wait_limit.load(); }

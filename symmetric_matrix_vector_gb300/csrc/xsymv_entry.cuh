@@ -54,6 +54,9 @@ struct MainArgs {
   int mode;                   // kFull or kBetaZero
   T* y0;                      // logical element 0 of y
   long long incy;
+  // the plan's warp and row tables (built before the launch)
+  const int4* wt;
+  const int2* rt;
 };
 
 // One compiled configuration of the main kernel.
@@ -93,10 +96,10 @@ cudaError_t launch_main(const MainArgs<T>& a) {
   const uint32_t extra = test_extra_tx();
   if (a.aligned)
     symv_main<T, VR, U, S, P, WARPS, true, MB, R><<<grid, WARPS * 32, smem, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, extra);
   else
     symv_main<T, VR, U, S, P, WARPS, false, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.status, a.epoch, limit, extra);
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, extra);
   return cudaGetLastError();
 }
 
@@ -142,10 +145,10 @@ cudaError_t launch_ticket(const MainArgs<T>& a) {
   int* ctr = static_cast<int*>(a.tk);
   if (a.aligned)
     symv_ticket<T, VR, U, WARPS, true, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, ctr, c);
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, ctr, c);
   else
     symv_ticket<T, VR, U, WARPS, false, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, ctr, c);
+        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, ctr, c);
   return cudaGetLastError();
 }
 
@@ -206,8 +209,8 @@ int ctas_per_sm_ticket() {
   }
 
 template <class T>
-cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, T alpha, T beta, int mode,
-                            T* y0, long long incy, const int* status, int epoch,
+cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, const int2* rt, T alpha,
+                            T beta, int mode, T* y0, long long incy, const int* status, int epoch,
                             cudaStream_t st) {
   // programmatic dependent launch: the launch overlaps the tail of the main
   // kernel, whose completion the finaliser awaits with griddepcontrol.wait
@@ -221,8 +224,53 @@ cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, T alpha, T 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, symv_finalize<T>, p, Wc, Wr, alpha, beta, mode, y0, incy,
+  return cudaLaunchKernelEx(&cfg, symv_finalize<T>, p, Wc, Wr, rt, alpha, beta, mode, y0, incy,
                             status, epoch);
+}
+
+// ----------------------------------------------------------- plan tables --
+// The bytes that identify a plan's tables (all ints: no padding).
+struct TablesKey {
+  int n, NB, upper, cd, cg, W;
+};
+
+inline TablesKey tables_key(const Plan& p) { return TablesKey{p.n, p.NB, p.upper, p.cd, p.cg, p.W}; }
+
+// bytes of the warp table (int4 per warp) followed by the row table (int2
+// per block row)
+inline long long tables_bytes(const Plan& p) {
+  return ((long long)p.W * 16 + 255) / 256 * 256 + (long long)p.nb * 8;
+}
+
+inline cudaError_t launch_plan_tables(const Plan& p, void* buf, cudaStream_t st) {
+  const long long m = p.W > p.nb ? p.W : p.nb;
+  symv_plan_tables<<<(unsigned)((m + 255) / 256), 256, 0, st>>>(
+      p, static_cast<int4*>(buf),
+      reinterpret_cast<int2*>(static_cast<char*>(buf) + ((long long)p.W * 16 + 255) / 256 * 256));
+  return cudaGetLastError();
+}
+
+// Point *wt, *rt at the tables of plan p for this stream, building them
+// first (one small launch) if the stream's table buffer holds another plan's.
+inline int ensure_tables(const Plan& p, cudaStream_t st, const int4** wt, const int2** rt) {
+  const TablesKey key = tables_key(p);
+  bool ready = false;
+  int status = XSYMV_OK;
+  void* buf = plan_tables((size_t)tables_bytes(p), st, &key, sizeof(key), &ready, &status);
+  if (!buf) return status;
+  if (!ready) {
+    cudaError_t e = launch_plan_tables(p, buf, st);
+    if (e != cudaSuccess) {
+      plan_tables_forget(st);
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+  }
+  *wt = static_cast<const int4*>(buf);
+  *rt = reinterpret_cast<const int2*>(static_cast<char*>(buf) +
+                                      ((long long)p.W * 16 + 255) / 256 * 256);
+  return XSYMV_OK;
 }
 
 // ---------------------------------------------------------------- checks --
@@ -307,8 +355,8 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     Plan p = plan_make(n, 32, upper, 1);
     timing_begin(st);
     timing_mid(st);
-    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, alpha, beta, bz ? kZero : kAlphaZero,
-                                       y0, incy, nullptr, 0, st);
+    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, nullptr, alpha, beta,
+                                       bz ? kZero : kAlphaZero, y0, incy, nullptr, 0, st);
     timing_end(st);
     if (e != cudaSuccess) {
       record_cuda_error(e);
@@ -329,6 +377,8 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
                 (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
                     (((long long)lda * (long long)sizeof(T)) % 16 == 0),
                 st};
+  status = ensure_tables(wl.plan, st, &m.wt, &m.rt);
+  if (status) return status;
   if (wl.variant->accum == kAccumTickets) {
     // one launch: the kernel also applies y = alpha*s + beta*y
     const long long tk_bytes = kTkHeaderBytes + (long long)wl.plan.nb * kTkStride * 8;
@@ -355,8 +405,8 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {
     timing_mid(st);
-    e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, alpha, beta, bz ? kBetaZero : kFull, y0, incy,
-                           m.status, epoch, st);
+    e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, alpha, beta, bz ? kBetaZero : kFull, y0,
+                           incy, m.status, epoch, st);
   }
   timing_end(st);
   if (e != cudaSuccess) {

@@ -129,8 +129,8 @@ int gemv_entry(const GemvVariant<T>* table, int count, int tindex, int n, T alph
     Plan p = plan_make(n, 32, 1, 1);
     timing_begin(st);
     timing_mid(st);
-    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, alpha, beta, bz ? kZero : kAlphaZero,
-                                       y0, incy, nullptr, 0, st);
+    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, nullptr, alpha, beta,
+                                       bz ? kZero : kAlphaZero, y0, incy, nullptr, 0, st);
     timing_end(st);
     if (e != cudaSuccess) {
       record_cuda_error(e);

@@ -490,40 +490,48 @@ struct WarpTile {
 };
 
 // ----------------------------------------------------------------------------
+// the plan's warp and row tables (see xsymv_plan.h), once per plan
+// ----------------------------------------------------------------------------
+static __global__ void symv_plan_tables(Plan p, int4* __restrict__ wt, int2* __restrict__ rt) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < p.W) {
+    int Ia, Ib;
+    long long ja, jb;
+    plan_warp_entry(p, (int)t, &Ia, &Ib, &ja, &jb);
+    wt[t] = make_int4(Ia, Ib, (int)ja, (int)jb);
+  }
+  if (t < p.nb) rt[t] = make_int2(plan_first_owner(p, (int)t), plan_nq(p, (int)t));
+}
+
+// ----------------------------------------------------------------------------
 // one warp's share of the triangle
 // ----------------------------------------------------------------------------
-// For every block row I in which warp w owns columns: the columns of the
-// diagonal tile (masked), then the off-diagonal ones (through the ring when
-// RING, else straight into registers), column partials to Wc[I*n + j], then
-// the row partial to the warp's slot of row I in Wr.  Returns false if a
-// bounded wait of the ring ran out (the warp then stops at once).
+// For every block row I in which warp w owns columns (from the plan's warp
+// table wt; row table rt): the columns of the diagonal tile (masked), then
+// the off-diagonal ones (through the ring when RING, else straight into
+// registers), column partials to Wc[I*n + j], then the row partial to the
+// warp's slot of row I in Wr.  Returns false if a bounded wait of the ring
+// ran out (the warp then stops at once).
 template <class T, int VR, int U, int STAGES, bool RING, bool ALIGNED, int R>
 __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int lane, Ring& rg,
                                             const T* __restrict__ A, long long lda,
                                             const T* __restrict__ x, int incx,
                                             T* __restrict__ Wc, T* __restrict__ Wr,
+                                            const int4* __restrict__ wt,
+                                            const int2* __restrict__ rt,
                                             unsigned long long limit_ns) {
   using Tile = WarpTile<T, VR, U>;
   constexpr int VPL = Tile::VPL;
   constexpr int NB = Tile::NB;
-  // this warp's cost range [cs, ce); it owns the columns whose first cost
-  // unit lies in it
-  const long long ce = plan_wstart(p, w + 1);
-  long long cs = plan_wstart(p, w);
-  int I = plan_row_of(p, cs);
+  const int4 d = __ldg(wt + w);   // rows d.x .. d.y, from column d.z to column d.w
   const long long n = p.n;
   Tile t;
 
-  for (; cs < ce && I < p.nb; ++I) {
-    const long long rcs = plan_rowstart(p, I);
-    const long long rce = rcs + plan_rowcost(p, I);
-    const long long c0 = plan_cols_before(p, I, cs - rcs);
-    const long long c1 = plan_cols_before(p, I, (ce < rce ? ce : rce) - rcs);
-    cs = rce;
-    if (c0 >= c1) continue;   // no column of this row starts in the range
+  for (int I = d.x; I <= d.y; ++I) {
     const long long cb = plan_colbase(p, I);
-    const long long ja = cb + c0;
-    const long long jb = cb + c1;
+    const long long ja = I == d.x ? (long long)d.z : cb;
+    const long long jb = I == d.y ? (long long)d.w : cb + plan_rowlen(p, I);
+    if (ja >= jb) continue;   // no column of this row starts in the range
     const long long r0 = (long long)I * NB;
 
 #pragma unroll
@@ -562,7 +570,7 @@ __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int lane, Ring
 
     // the row partial goes to slot q of block row I, q = this warp's index
     // among the warps owning columns of the row
-    const int q = w - plan_first_owner(p, I);
+    const int q = w - __ldg(&rt[I].x);
     T* wr = Wr + ((long long)I * p.qmax + q) * NB;
 #pragma unroll
     for (int v = 0; v < VR; ++v)
@@ -584,8 +592,9 @@ template <class T, int VR, int U, int STAGES, int PIPE, int WARPS, bool ALIGNED,
           int R = U>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
-          T* __restrict__ Wc, T* __restrict__ Wr, int* status, int epoch,
-          unsigned long long limit_ns, uint32_t extra_tx) {
+          T* __restrict__ Wc, T* __restrict__ Wr, const int4* __restrict__ wt,
+          const int2* __restrict__ rt, int* status, int epoch, unsigned long long limit_ns,
+          uint32_t extra_tx) {
   using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
   constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
   // let the finaliser (launched as a programmatic dependent) get scheduled as
@@ -610,7 +619,7 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     __syncwarp();
   }
   if (!stream_warp<T, VR, U, STAGES, RING, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr,
-                                                       limit_ns))
+                                                       wt, rt, limit_ns))
     if (lane == 0) atomicMax(status, epoch);
 }
 
@@ -631,8 +640,9 @@ constexpr int kFinCols = 32;    // output elements per block
 // only on (n, NB, W), never on timing.
 template <class T>
 __global__ void __launch_bounds__(kFinParts * kFinCols)
-symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alpha, T beta,
-              int mode, T* __restrict__ y, long long incy, const int* status, int epoch) {
+symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
+              const int2* __restrict__ rt, T alpha, T beta, int mode, T* __restrict__ y,
+              long long incy, const int* status, int epoch) {
   __shared__ T part[kFinParts][kFinCols];
   // wait until the preceding grid on the stream (the main kernel) has
   // completed and its writes are visible (no-op without a programmatic launch)
@@ -652,7 +662,7 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr, T alph
     const int jj = (int)(j - (long long)K * p.NB);
     const int I0 = p.upper ? 0 : K;
     const int I1 = p.upper ? K : p.nb - 1;
-    const int nq = plan_nq(p, K);
+    const int nq = __ldg(&rt[K].y);
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
     const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
     const T* wc = Wc + j;

@@ -162,6 +162,40 @@ inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int 
   return p;
 }
 
+// columns [ja, jb) of block row I whose first cost unit lies in [cs, ce);
+// false if there are none
+XSYMV_HD bool plan_cost_cols(const Plan& p, long long cs, long long ce, int I, long long* ja,
+                             long long* jb) {
+  const long long rcs = plan_rowstart(p, I), rce = rcs + plan_rowcost(p, I);
+  const long long lo = cs > rcs ? cs : rcs, hi = ce < rce ? ce : rce;
+  if (lo >= hi) return false;
+  const long long c0 = plan_cols_before(p, I, lo - rcs), c1 = plan_cols_before(p, I, hi - rcs);
+  if (c0 >= c1) return false;
+  *ja = plan_colbase(p, I) + c0;
+  *jb = plan_colbase(p, I) + c1;
+  return true;
+}
+
+// The warp and row tables of a plan: built once per plan on the device (by
+// symv_plan_tables) and kept with the workspace, so that the kernels find
+// their work without 64-bit divisions.
+//   warp table, one int4 per warp w: x, y = the first and last block row its
+//     cost range touches; z = its first column in row x; w = the end of its
+//     columns in row y (rows strictly between are wholly its own).  A row
+//     whose share holds no column start gets an empty range (z or w at the
+//     row's other end).
+//   row table, one int2 per block row I: x = the owner of its first column
+//     (row-partial slot q of warp w is w - x), y = the number of warps that
+//     own columns of the row (slots 0 .. y-1).
+XSYMV_HD void plan_warp_entry(const Plan& p, int w, int* Ia, int* Ib, long long* ja, long long* jb) {
+  const long long cs = plan_wstart(p, w), ce = plan_wstart(p, w + 1);
+  *Ia = plan_row_of(p, cs);
+  *Ib = plan_row_of(p, ce - 1);
+  long long a, b;
+  *ja = plan_cost_cols(p, cs, ce, *Ia, &a, &b) ? a : plan_colbase(p, *Ia) + plan_rowlen(p, *Ia);
+  *jb = plan_cost_cols(p, cs, ce, *Ib, &a, &b) ? b : plan_colbase(p, *Ib);
+}
+
 // workspace elements: Wc (nb*n) followed by Wr (nb*qmax*NB)
 inline long long plan_wc_elems(const Plan& p) { return (long long)p.nb * p.n; }
 inline long long plan_wr_elems(const Plan& p) { return (long long)p.nb * p.qmax * p.NB; }
@@ -182,20 +216,6 @@ inline long long plan_wr_elems(const Plan& p) { return (long long)p.nb * p.qmax 
 // The ranges are sorted (their first and last warps never decrease with t),
 // so ordering the contributors by warp index orders them by block row, and a
 // warp waits only for warps with smaller indices.
-
-// columns [ja, jb) of block row I whose first cost unit lies in [cs, ce);
-// false if there are none
-XSYMV_HD bool plan_cost_cols(const Plan& p, long long cs, long long ce, int I, long long* ja,
-                             long long* jb) {
-  const long long rcs = plan_rowstart(p, I), rce = rcs + plan_rowcost(p, I);
-  const long long lo = cs > rcs ? cs : rcs, hi = ce < rce ? ce : rce;
-  if (lo >= hi) return false;
-  const long long c0 = plan_cols_before(p, I, lo - rcs), c1 = plan_cols_before(p, I, hi - rcs);
-  if (c0 >= c1) return false;
-  *ja = plan_colbase(p, I) + c0;
-  *jb = plan_colbase(p, I) + c1;
-  return true;
-}
 
 // columns [ja, jb) of block row I owned by warp w; false if it owns none
 XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long long* jb) {

@@ -29,6 +29,17 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
 // buffer) that the kernel's tickets carry.  nullptr and *status set on failure.
 void* ticket_buffer(size_t bytes, cudaStream_t stream, int* status, unsigned long long* call);
 
+// buffer of at least `bytes` on (current device, stream) for a plan's warp
+// and row tables (see xsymv_plan.h).  *ready is true when the buffer already
+// holds the tables of `key` (compared bytewise); either way the buffer is
+// recorded as holding them, so the caller must enqueue their construction
+// on `stream` when *ready is false, or call plan_tables_forget() if it
+// cannot.  A buffer that had to grow holds no tables.  nullptr and *status
+// set on failure.
+void* plan_tables(size_t bytes, cudaStream_t stream, const void* key, size_t key_bytes,
+                  bool* ready, int* status);
+void plan_tables_forget(cudaStream_t stream);
+
 // time limit of every bounded wait in the kernels
 unsigned long long wait_limit_ns();
 // extra bytes announced on every ring barrier: 0, except when a test makes

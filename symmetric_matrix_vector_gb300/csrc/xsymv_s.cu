@@ -79,7 +79,9 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
 //   bounded wait runs out) must start at zero; the first call on a device
 //   clears them with cudaMemsetAsync on its stream.  Every other workspace
 //   slot the finaliser reads is written by the main kernel of the same
-//   call.  The array keeps the last call's contents.
+//   call.  The array keeps the last call's contents, among them the plan's
+//   warp and row tables: a call rebuilds them (one extra small launch) only
+//   when its plan differs from the previous call's on the device.
 // * All calls share the one array: calls that overlap on the GPU (on
 //   different streams, or from different host threads) race and corrupt
 //   each other's results.  Order them, e.g. on one stream.
@@ -91,13 +93,15 @@ struct NoallocDevice {
   int device;
   void* scratch;
   int epoch;   // last call number on this device
+  xsymv::TablesKey tables;   // the plan whose tables the array holds (n = -1: none)
 };
 std::mutex g_noalloc_mu;
 std::vector<NoallocDevice> g_noalloc_devices;
 
 // device address of g_noalloc_scratch on the current device and a fresh call
-// number; the first call on a device clears the status header on `stream`
-int noalloc_scratch(void** out, int* epoch, cudaStream_t stream) {
+// number; the first call on a device clears the status header on `stream`.
+// *dev_index: the device's entry (for the tables record).
+int noalloc_scratch(void** out, int* epoch, cudaStream_t stream, size_t* dev_index) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) {
@@ -105,13 +109,16 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream) {
     return XSYMV_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  for (NoallocDevice& s : g_noalloc_devices)
+  for (size_t i = 0; i < g_noalloc_devices.size(); ++i) {
+    NoallocDevice& s = g_noalloc_devices[i];
     if (s.device == d) {
       s.epoch = (s.epoch >= 0x7ffffffe) ? 1 : s.epoch + 1;
       *out = s.scratch;
       *epoch = s.epoch;
+      *dev_index = i;
       return XSYMV_OK;
     }
+  }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e == cudaSuccess && p != nullptr) e = cudaMemsetAsync(p, 0, 256, stream);
@@ -119,9 +126,10 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream) {
     xsymv::record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  g_noalloc_devices.push_back(NoallocDevice{d, p, 1});
+  g_noalloc_devices.push_back(NoallocDevice{d, p, 1, xsymv::TablesKey{-1, 0, 0, 0, 0, 0}});
   *out = p;
   *epoch = 1;
+  *dev_index = g_noalloc_devices.size() - 1;
   return XSYMV_OK;
 }
 }  // namespace
@@ -142,12 +150,13 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   const float* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
   void* scratch = nullptr;
   int epoch = 0;
-  int status = noalloc_scratch(&scratch, &epoch, st);
+  size_t dev_index = 0;
+  int status = noalloc_scratch(&scratch, &epoch, st, &dev_index);
   if (status) return status;
 
   if (az) {  // y := beta*y, no workspace needed
     Plan p = plan_make(n, 32, upper, 1);
-    cudaError_t e = launch_finalize<float>(p, nullptr, nullptr, alpha, beta,
+    cudaError_t e = launch_finalize<float>(p, nullptr, nullptr, nullptr, alpha, beta,
                                            bz ? kZero : kAlphaZero, y0, incy, nullptr, 0, st);
     if (e != cudaSuccess) {
       record_cuda_error(e);
@@ -163,20 +172,36 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   if (status) return status;
   // the ordered-ticket kernels keep state in a second, allocated buffer
   if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;
-  if (wl.bytes > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
+  // the plan's tables follow the workspace in the same array
+  const long long tab_off = align_up(wl.bytes, 256);
+  if (tab_off + tables_bytes(wl.plan) > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
   char* ws = static_cast<char*>(scratch);
   MainArgs<float> m{wl.plan, A, lda, x0, incx, reinterpret_cast<float*>(ws + wl.wc_off),
                     reinterpret_cast<float*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
                     (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (((long long)lda * 4) % 16 == 0),
                     st};
-  cudaError_t e = wl.variant->launch(m);
+  m.wt = reinterpret_cast<const int4*>(ws + tab_off);
+  m.rt = reinterpret_cast<const int2*>(ws + tab_off + ((long long)wl.plan.W * 16 + 255) / 256 * 256);
+  int launches = 2;
+  cudaError_t e = cudaSuccess;
+  {
+    const TablesKey key = tables_key(wl.plan);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    TablesKey& have = g_noalloc_devices[dev_index].tables;
+    if (memcmp(&have, &key, sizeof(key)) != 0) {
+      e = launch_plan_tables(wl.plan, ws + tab_off, st);
+      have = e == cudaSuccess ? key : TablesKey{-1, 0, 0, 0, 0, 0};
+      ++launches;
+    }
+  }
+  if (e == cudaSuccess) e = wl.variant->launch(m);
   if (e == cudaSuccess)
-    e = launch_finalize<float>(wl.plan, m.Wc, m.Wr, alpha, beta, bz ? kBetaZero : kFull, y0,
+    e = launch_finalize<float>(wl.plan, m.Wc, m.Wr, m.rt, alpha, beta, bz ? kBetaZero : kFull, y0,
                                incy, m.status, epoch, st);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  note_launches(2);
+  note_launches(launches);
   return XSYMV_OK;
 }

@@ -381,7 +381,8 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
 template <class T, int VR, int U, int WARPS, bool ALIGNED, int MINB, int R = U>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_ticket(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
-            T* Wc, T* Wr, int* ctr, TicketCtx<T> c) {
+            T* Wc, T* Wr, const int4* __restrict__ wt, const int2* __restrict__ rt, int* ctr,
+            TicketCtx<T> c) {
   constexpr int NB = WarpTile<T, VR, U>::NB;
   __shared__ int s_blk;
   __shared__ GroupRow s_rows[kTkRows];
@@ -393,7 +394,7 @@ symv_ticket(Plan p, const T* __restrict__ A, long long lda, const T* __restrict_
   const int w = blk * WARPS + wl;
   if (w < p.W) {
     Ring rg{0u, 0u, 0, 0u, 0u};
-    stream_warp<T, VR, U, 1, false, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr,
+    stream_warp<T, VR, U, 1, false, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr, wt, rt,
                                                 c.limit_ns);
   }
   // the block's warps act as one contributor: their workspace writes are

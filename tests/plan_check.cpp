@@ -7,6 +7,7 @@
 // in increasing warp order.
 #include <cstdio>
 #include <algorithm>
+#include <cstdint>
 #include <cstdlib>
 #include <set>
 #include <vector>
@@ -125,6 +126,22 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
     }
   }
   if (p.W >= (1 << 24)) return fail("warp bits", n, NB, upper, Wmax, cd, cg);
+  // the warp table: rows Ia..Ib, first column ja in row Ia, end jb in row Ib,
+  // whole rows between; read this way it gives exactly the owned columns
+  for (int w = 0; w < p.W; ++w) {
+    int Ia, Ib;
+    long long ja, jb;
+    plan_warp_entry(p, w, &Ia, &Ib, &ja, &jb);
+    for (int I = 0; I < nb; ++I) {
+      const long long cb = plan_colbase(p, I), len = plan_rowlen(p, I);
+      const long long a = I == Ia ? ja : cb, b = I == Ib ? jb : cb + len;
+      for (long long c = 0; c < len; ++c) {
+        const bool mine = I >= Ia && I <= Ib && cb + c >= a && cb + c < b;
+        if (mine != (own[I][c] == w)) return fail("warp table", n, NB, upper, Wmax, cd, cg);
+      }
+    }
+    if (ja > INT32_MAX || jb > INT32_MAX) return fail("warp table range", n, NB, upper, Wmax, cd, cg);
+  }
   // the same chains between groups of G consecutive warps (thread blocks)
   for (int G : {1, 3, 8}) {
     const int ng = (p.W + G - 1) / G;

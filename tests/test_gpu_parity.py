@@ -256,9 +256,12 @@ def test_non_default_stream(o):
 
 
 def test_launch_count_and_timing(lib):
-    """every call launches exactly the main kernel and the finaliser"""
+    """every call launches exactly the main kernel and the finaliser (plus,
+    on the first call of a plan, the kernel that builds its tables)"""
     p = inputs.make_problem("s", "U", 1000, alpha=1.0, beta=0.5, seed=1)
     dp = DeviceProblem(p)
+    st, _ = dp.run()    # a new plan: its warp and row tables are built once (one more launch)
+    assert st == 0
     c0 = lib.xsymv_launch_count()
     lib.xsymv_timing_enable(True)
     for _ in range(5):

@@ -167,6 +167,8 @@ def test_ticket_single_launch(lib):
     p = inputs.make_problem("s", "U", 1000, alpha=1.0, beta=0.5, seed=1)
     dp = DeviceProblem(p)
     with forced(lib, "s", ticket_variants(lib, "s")[0]):
+        st, _ = dp.run()    # a new plan: its tables are built once (one more launch)
+        assert st == 0
         c0 = lib.xsymv_launch_count()
         for _ in range(5):
             st, _ = dp.run()
