@@ -63,6 +63,8 @@ def parse_args():
     ap.add_argument("--no-tickets", action="store_true",
                     help="skip the ordered-ticket versus workspace comparison")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--variant", default="",
+                    help="time this compiled SSYMV variant (by name) instead of the tuned choice")
     return ap.parse_args()
 
 
@@ -185,6 +187,24 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def host_link_gbs(torch, nbytes=1 << 30, reps=5):
+    """Host-to-device bandwidth of this machine's CPU-GPU link: the best of a few
+    copies of a pinned host buffer to the device (CUDA events)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None or ms < best else best
+    del h, d
+    return nbytes / (best * 1e-3) / 1e9
 
 
 def max_over_ranks(value: float, dist, device="cuda") -> float:
@@ -468,6 +488,11 @@ def run_ours(args):
             dist.barrier()
 
     n = args.n
+    if args.variant:
+        names = [xs.xsymv_variant_name("s", i) for i in range(xs.xsymv_variant_count("s"))]
+        if args.variant not in names:
+            raise SystemExit("unknown SSYMV variant %r; compiled: %s" % (args.variant, names))
+        xs.check(xs.xsymv_set_variant("s", names.index(args.variant)))
     prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
     A, x, y = prob["A"], prob["x"], prob["y"]
     lda = prob["lda"]
@@ -612,10 +637,15 @@ def run_ours(args):
         barrier()
         ems = max_over_ranks(e0.elapsed_time(e1) / esteps, dist)
         h2d, d2h = xs.xsymv_host_traffic()
+        link = host_link_gbs(torch)
+        moved = (h2d + d2h) / (ems * 1e-3) / 1e9
         e2e = {"value": replica_rate(world, flops(n), ems), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
                "steps": esteps,
-               "api": "xsymv_s_host on pinned host buffers (read in place over the host link)"}
+               "api": "xsymv_s_host on pinned host buffers (read in place over the host link)",
+               "roofline": {"bound": "host link", "achieved": moved, "peak": link, "unit": "GB/s",
+                            "frac": moved / link,
+                            "peak_source": "pinned host -> device copy of 1 GiB, same run"}}
 
     kinds = []
     if rank == 0 and not args.no_kinds and probes:

@@ -14,32 +14,32 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1820.0 GB/s at n=4096
-    {'s', 1, 12288, 14},   // vr1_u2_r0_w8_b0_g9 3658.8 GB/s at n=8192
-    {'s', 1, 20480, 13},   // vr1_u2_r0_w8_b6_g11 5352.9 GB/s at n=16384
-    {'s', 1, 28672, 11},   // vr1_u2_r0_w8_b6_g7 5934.3 GB/s at n=24576
-    {'s', 1, 2147483647, 11},   // vr1_u2_r0_w8_b6_g7 6205.6 GB/s at n=32768
-    {'s', 0, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1802.7 GB/s at n=4096
-    {'s', 0, 12288, 14},   // vr1_u2_r0_w8_b0_g9 3643.9 GB/s at n=8192
-    {'s', 0, 20480, 12},   // vr1_u2_r0_w8_b6_g9 5393.9 GB/s at n=16384
-    {'s', 0, 28672, 15},   // vr1_u2_r0_w8_b6_g14 5891.7 GB/s at n=24576
-    {'s', 0, 2147483647, 12},   // vr1_u2_r0_w8_b6_g9 6170.8 GB/s at n=32768
-    {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1781.4 GB/s at n=8192
-    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2164.6 GB/s at n=24576
-    {'d', 0, 16384, 12},   // vr4_u2_r0_w8_b0_g5_c4 1777.6 GB/s at n=8192
-    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2167.5 GB/s at n=24576
-    {'c', 1, 12288, 9},   // vr1_u4_r0_w8_b0_g7 4789.0 GB/s at n=8192
-    {'c', 1, 2147483647, 10},   // vr2_u2_r0_w8_b0_g7 6085.4 GB/s at n=16384
-    {'c', 0, 12288, 9},   // vr1_u4_r0_w8_b0_g7 4800.6 GB/s at n=8192
-    {'c', 0, 2147483647, 10},   // vr2_u2_r0_w8_b0_g7 6092.8 GB/s at n=16384
-    {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1054.9 GB/s at n=8192
-    {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1096.2 GB/s at n=16384
-    {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1048.3 GB/s at n=8192
-    {'z', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1098.5 GB/s at n=16384
-    {'w', 1, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 113.3 GB/s at n=4096
-    {'w', 1, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 129.4 GB/s at n=8192
-    {'w', 0, 6144, 9},   // vr4_u2_r0_w8_b0_g4_c4 112.7 GB/s at n=4096
-    {'w', 0, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 129.3 GB/s at n=8192
+    {'s', 1, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1817.7 GB/s at n=4096
+    {'s', 1, 12288, 12},   // vr1_u2_r0_w8_b6_g9 3972.4 GB/s at n=8192
+    {'s', 1, 20480, 12},   // vr1_u2_r0_w8_b6_g9 5979.0 GB/s at n=16384
+    {'s', 1, 28672, 13},   // vr1_u2_r0_w8_b6_g11 6291.7 GB/s at n=24576
+    {'s', 1, 2147483647, 11},   // vr1_u2_r0_w8_b6_g7 6560.3 GB/s at n=32768
+    {'s', 0, 6144, 11},   // vr1_u2_r0_w8_b6_g7 1638.8 GB/s at n=4096
+    {'s', 0, 12288, 15},   // vr1_u2_r0_w8_b6_g14 4092.5 GB/s at n=8192
+    {'s', 0, 20480, 15},   // vr1_u2_r0_w8_b6_g14 5898.5 GB/s at n=16384
+    {'s', 0, 28672, 15},   // vr1_u2_r0_w8_b6_g14 6295.9 GB/s at n=24576
+    {'s', 0, 2147483647, 11},   // vr1_u2_r0_w8_b6_g7 6544.3 GB/s at n=32768
+    {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1593.2 GB/s at n=8192
+    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2173.8 GB/s at n=24576
+    {'d', 0, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1558.5 GB/s at n=8192
+    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2171.3 GB/s at n=24576
+    {'c', 1, 12288, 9},   // vr1_u4_r0_w8_b0_g7 4080.6 GB/s at n=8192
+    {'c', 1, 2147483647, 10},   // vr2_u2_r0_w8_b0_g7 6331.9 GB/s at n=16384
+    {'c', 0, 12288, 5},   // vr1_u2_r0_w8_b5 3955.5 GB/s at n=8192
+    {'c', 0, 2147483647, 10},   // vr2_u2_r0_w8_b0_g7 6322.0 GB/s at n=16384
+    {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1054.8 GB/s at n=8192
+    {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1095.9 GB/s at n=16384
+    {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1047.4 GB/s at n=8192
+    {'z', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1097.4 GB/s at n=16384
+    {'w', 1, 6144, 9},   // vr4_u2_r0_w8_b0_g4_c4 116.8 GB/s at n=4096
+    {'w', 1, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 130.5 GB/s at n=8192
+    {'w', 0, 6144, 9},   // vr4_u2_r0_w8_b0_g4_c4 117.2 GB/s at n=4096
+    {'w', 0, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 130.5 GB/s at n=8192
 };
 // END TUNED TABLE
 

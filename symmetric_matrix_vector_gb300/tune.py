@@ -29,9 +29,15 @@ DEFAULT_N = {"s": [4096, 8192, 16384, 24576, 32768], "d": [8192, 24576], "c": [8
              "z": [8192, 16384], "w": [4096, 8192]}
 TUNED_H = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "xsymv_tuned.h")
 INT_MAX = 2147483647
+L2_BYTES = 129e6          # GB300's L2
+COLD_BELOW = 4 * L2_BYTES  # smaller stored triangles are timed with L2 flushed before each call
 
 
-def measure(xs, kind, uplo, n, variant, reps, prob):
+def measure(xs, kind, uplo, n, variant, reps, prob, cold=False):
+    """median ms of one call.  Back-to-back calls, or, with cold=True, each
+    call after writing a 512 MB buffer and reading another (nothing of the
+    problem left in L2, and no dirty lines left to write back during the
+    call) -- the protocol the benchmark uses for triangles near L2's size."""
     import torch
 
     assert xs.xsymv_set_variant(kind, variant) == 0
@@ -42,6 +48,21 @@ def measure(xs, kind, uplo, n, variant, reps, prob):
         for _ in range(3):
             xs.check(xs.symv(kind, uplo, n, alpha, A, lda, x, 1, beta, y, 1))
         torch.cuda.synchronize()
+        if cold:
+            flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+            clean = torch.zeros(64 << 20, dtype=torch.int64, device="cuda")
+            evs = []
+            for _ in range(max(20, min(reps, 60))):
+                flush.fill_(1)
+                clean.sum()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                xs.check(xs.symv(kind, uplo, n, alpha, A, lda, x, 1, beta, y, 1))
+                e1.record()
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs)
         times = []
         for _ in range(3):
             e0 = torch.cuda.Event(enable_timing=True)
@@ -70,7 +91,7 @@ def load_results(path):
     return done
 
 
-def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9):
+def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9, only=None):
     import torch
 
     import symmetric_matrix_vector_gb300 as xs
@@ -86,6 +107,8 @@ def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9):
                 prob = None
                 for v in range(xs.xsymv_variant_count(kind)):
                     name = xs.xsymv_variant_name(kind, v)
+                    if only and name not in only:
+                        continue
                     if (kind, uplo, n, name) in done:
                         continue
                     if prob is None:
@@ -95,9 +118,10 @@ def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9):
                                                      seed=n)
                     tri = n * (n + 1) / 2 * es[kind]
                     reps = int(max(5, min(500, reps_bytes / tri)))
-                    ms = measure(xs, kind, uplo, n, v, reps, prob)
+                    ms = measure(xs, kind, uplo, n, v, reps, prob, cold=tri < COLD_BELOW)
                     rec = {"kind": kind, "uplo": uplo, "n": n, "variant": v, "variant_name": name,
                            "ms": ms, "gbs": tri / (ms * 1e-3) / 1e9,
+                           "l2": "flushed" if tri < COLD_BELOW else "back-to-back",
                            "gpu": torch.cuda.get_device_name()}
                     done[(kind, uplo, n, name)] = rec
                     if out:
@@ -169,13 +193,16 @@ def main():
     ap.add_argument("--uplo", default="U,L")
     ap.add_argument("--results", default="tune_results.jsonl")
     ap.add_argument("--write-header", default="", help="write the tuned header here")
+    ap.add_argument("--variants", default="",
+                    help="comma-separated variant names: time only these (default: all)")
     args = ap.parse_args()
     kinds = [k for k in args.kinds.split(",") if k]
     sizes = {}
     if args.n:
         ns = [int(v) for v in args.n.split(",")]
         sizes = {k: ns for k in kinds}
-    done = sweep(kinds, sizes, args.uplo.split(","), args.results)
+    only = set(v for v in args.variants.split(",") if v)
+    done = sweep(kinds, sizes, args.uplo.split(","), args.results, only=only or None)
     if args.write_header:
         import symmetric_matrix_vector_gb300 as xs
 
