@@ -18,6 +18,9 @@ static const Variant<c32> kVariants_c[] = {
     XSYMV_REG_GC(c32, 2, 2, 8, 0, 7, 8),
     XSYMV_REG_GC(c32, 1, 4, 8, 0, 7, 8),
     XSYMV_TICKET(c32, 2, 2, 8, 0, 7, 2),
+    XSYMV_REG_G(c32, 2, 2, 8, 4, 7),
+    XSYMV_REG_G(c32, 2, 2, 8, 4, 9),
+    XSYMV_REG_G(c32, 2, 2, 8, 4, 11),
 };
 static_assert(sizeof(c32) == sizeof(xsymv_c32), "C-ABI type layout");
 }  // namespace xsymv

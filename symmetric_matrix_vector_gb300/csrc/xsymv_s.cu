@@ -26,6 +26,10 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_TICKET(float, 1, 2, 8, 0, 9, 2),
     XSYMV_TICKET(float, 2, 2, 8, 0, 6, 2),
     XSYMV_TICKET(float, 2, 2, 8, 4, 6, 2),
+    XSYMV_REG_G(float, 2, 2, 8, 4, 9),
+    XSYMV_REG_G(float, 2, 2, 8, 4, 11),
+    XSYMV_REG_G(float, 2, 2, 8, 4, 13),
+    XSYMV_REG_G(float, 2, 1, 8, 5, 6),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv
