@@ -74,8 +74,8 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
 //
 // * The array holds kNoallocScratchBytes (16 MiB) on every GPU that loads
 //   this library, until the process exits.  Problems whose workspace does
-//   not fit (roughly n > 17000 for single precision on GB300) are rejected
-//   with XSYMV_ERR_TOO_LARGE before anything is enqueued.
+//   not fit (roughly n > 21000 with the tuned kernels on GB300) are
+//   rejected with XSYMV_ERR_TOO_LARGE before anything is enqueued.
 // * The first call on a device looks up the array's device address
 //   (cudaGetSymbolAddress, with that device current) and caches it; make
 //   that first call before any stream capture.
