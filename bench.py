@@ -94,14 +94,18 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the files that define the main kernel's device code (the compiled variant
+# is identified separately, by its name)
+KERNEL_SOURCES = ("xsymv_kernels.cuh", "xsymv_plan.h", "xsymv_scalar.cuh")
+
+
 def kernel_source_digest() -> str:
     csrc = os.path.join(ROOT, "symmetric_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")) and f != "xsymv_tuned.h":
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
