@@ -47,6 +47,12 @@
  * default stream) and runs asynchronously: when a call returns XSYMV_OK the
  * result is ready once that stream has reached it.  Two calls on the same
  * stream are ordered; calls on different streams use different workspaces.
+ * Issue the calls that share a stream from one host thread at a time: a call
+ * enqueues two or three kernels that share the stream's workspace, and two
+ * threads interleaving their launches on one stream would mix them.
+ * The first call of a new problem shape (kind, uplo, n, variant) on a stream
+ * also enqueues a small kernel that tabulates the work partition; later
+ * calls of that shape on that stream reuse the table.
  *
  * Status (return value):
  *   0                 success.
