@@ -115,7 +115,7 @@ XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int l
  * and status codes as xsymv_s; it never allocates.  Its workspace is one
  * fixed 16 MiB device array in the library, held on every GPU that loads the
  * library until the process exits; a problem whose workspace does not fit
- * (roughly n > 21000 with the tuned kernels) returns XSYMV_ERR_TOO_LARGE with nothing enqueued.
+ * (roughly n > 31000 with the tuned kernels) returns XSYMV_ERR_TOO_LARGE with nothing enqueued.
  * The first call on a device looks up the array's address on that device;
  * make that call before any stream capture.  It also clears the array's
  * 256-byte status header, the only part that must start at zero.  All calls

@@ -142,6 +142,7 @@ cudaError_t launch_ticket(const MainArgs<T>& a) {
   c.mode = a.mode;
   c.y = a.y0;
   c.incy = a.incy;
+  c.rt = a.rt;
   int* ctr = static_cast<int*>(a.tk);
   if (a.aligned)
     symv_ticket<T, VR, U, WARPS, true, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
@@ -231,10 +232,12 @@ cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, const int2*
 // ----------------------------------------------------------- plan tables --
 // The bytes that identify a plan's tables (all ints: no padding).
 struct TablesKey {
-  int n, NB, upper, cd, cg, W;
+  int n, NB, upper, cd, cg, W, G;
 };
 
-inline TablesKey tables_key(const Plan& p) { return TablesKey{p.n, p.NB, p.upper, p.cd, p.cg, p.W}; }
+inline TablesKey tables_key(const Plan& p) {
+  return TablesKey{p.n, p.NB, p.upper, p.cd, p.cg, p.W, p.G};
+}
 
 // bytes of the warp table (int4 per warp) followed by the row table (int2
 // per block row)
@@ -320,7 +323,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
   const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n)];
   const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps * v->waves;
-  out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost);
+  out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost, v->warps);
   out->variant = v;
   out->wc_off = kHeaderBytes;
   out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);

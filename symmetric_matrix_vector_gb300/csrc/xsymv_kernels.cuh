@@ -500,25 +500,88 @@ static __global__ void symv_plan_tables(Plan p, int4* __restrict__ wt, int2* __r
     plan_warp_entry(p, (int)t, &Ia, &Ib, &ja, &jb);
     wt[t] = make_int4(Ia, Ib, (int)ja, (int)jb);
   }
-  if (t < p.nb) rt[t] = make_int2(plan_first_owner(p, (int)t), plan_nq(p, (int)t));
+  if (t < p.nb) rt[t] = make_int2(plan_first_owner(p, (int)t) / p.G, plan_nq(p, (int)t));
+}
+
+// ----------------------------------------------------------------------------
+// row partials: one slot per thread block and block row
+// ----------------------------------------------------------------------------
+// A warp's row partials of its first and last block rows go to its two
+// shared-memory buffers; the row partials of the rows strictly between (rows
+// no other warp touches) go straight to the block's slot.  After the block's
+// warps are done, the block adds the buffers of each row in warp order and
+// writes the sum to its slot (row_partials_combine).
+template <class T, int NB, int WARPS>
+struct RowBuffers {
+  T buf[WARPS][2][NB];   // [warp][first / last row][row within the block row]
+  int row[WARPS][2];     // block row held by each buffer, -1: none
+};
+
+// block b's slot of block row I (first block of the row: rt[I].x)
+template <class T>
+__device__ __forceinline__ T* row_slot(const Plan& p, T* Wr, const int2* __restrict__ rt, int b,
+                                       int I) {
+  return Wr + ((long long)I * p.qmax + (b - __ldg(&rt[I].x))) * p.NB;
+}
+
+// All threads of the block, after a barrier that follows every warp's
+// stream: the rows of the buffers, in increasing order, each summed over the
+// warps in warp order and written to block b's slot.
+template <class T, int NB, int WARPS>
+__device__ __forceinline__ void row_partials_combine(const Plan& p, T* Wr,
+                                                     const int2* __restrict__ rt, int b,
+                                                     const RowBuffers<T, NB, WARPS>& rb) {
+  int lo = 0x7fffffff, hi = -1;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int I = rb.row[w][k];
+      if (I >= 0) {
+        lo = I < lo ? I : lo;
+        hi = I > hi ? I : hi;
+      }
+    }
+  for (int I = lo; I <= hi; ++I) {
+    T* slot = nullptr;
+    for (int r = threadIdx.x; r < NB; r += blockDim.x) {
+      T s = Ops<T>::zero();
+      bool has = false;
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (rb.row[w][k] == I) {
+            const T v = rb.buf[w][k][r];
+            s = has ? Ops<T>::add(s, v) : v;
+            has = true;
+          }
+      if (has) {
+        if (slot == nullptr) slot = row_slot(p, Wr, rt, b, I);
+        slot[r] = s;
+      }
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------
 // one warp's share of the triangle
 // ----------------------------------------------------------------------------
-// For every block row I in which warp w owns columns (from the plan's warp
-// table wt; row table rt): the columns of the diagonal tile (masked), then
-// the off-diagonal ones (through the ring when RING, else straight into
-// registers), column partials to Wc[I*n + j], then the row partial to the
-// warp's slot of row I in Wr.  Returns false if a bounded wait of the ring
-// ran out (the warp then stops at once).
-template <class T, int VR, int U, int STAGES, bool RING, bool ALIGNED, int R>
-__device__ __forceinline__ bool stream_warp(const Plan& p, int w, int lane, Ring& rg,
-                                            const T* __restrict__ A, long long lda,
+// For every block row I in which warp w (warp wl of block b) owns columns
+// (from the plan's warp table wt; row table rt): the columns of the diagonal
+// tile (masked), then the off-diagonal ones (through the ring when RING,
+// else straight into registers), column partials to Wc[I*n + j], then the
+// row partial: to the warp's buffer in rb for its first and last rows, to
+// block b's slot in Wr for the rows between.  Returns false if a bounded
+// wait of the ring ran out (the warp then stops at once).
+template <class T, int VR, int U, int STAGES, bool RING, bool ALIGNED, int R, int WARPS>
+__device__ __forceinline__ bool stream_warp(const Plan& p, int w, int wl, int b, int lane,
+                                            Ring& rg, const T* __restrict__ A, long long lda,
                                             const T* __restrict__ x, int incx,
                                             T* __restrict__ Wc, T* __restrict__ Wr,
                                             const int4* __restrict__ wt,
                                             const int2* __restrict__ rt,
+                                            RowBuffers<T, WarpTile<T, VR, U>::NB, WARPS>& rb,
                                             unsigned long long limit_ns) {
   using Tile = WarpTile<T, VR, U>;
   constexpr int VPL = Tile::VPL;
@@ -568,14 +631,16 @@ __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int lane, Ring
       }
     }
 
-    // the row partial goes to slot q of block row I, q = this warp's index
-    // among the warps owning columns of the row
-    const int q = w - __ldg(&rt[I].x);
-    T* wr = Wr + ((long long)I * p.qmax + q) * NB;
+    // the row partial: rows between the first and the last are this warp's
+    // alone (straight to the block's slot); the first and last rows are
+    // shared with other warps (to this warp's buffers, combined later)
+    const int k = I == d.x ? 0 : (I == d.y ? 1 : -1);
+    T* wr = k < 0 ? row_slot(p, Wr, rt, b, I) : rb.buf[wl][k];
 #pragma unroll
     for (int v = 0; v < VR; ++v)
 #pragma unroll
-      for (int k = 0; k < VPL; ++k) wr[Tile::lane_row(v, lane, k)] = t.racc[v][k];
+      for (int kk = 0; kk < VPL; ++kk) wr[Tile::lane_row(v, lane, kk)] = t.racc[v][kk];
+    if (k >= 0 && lane == 0) rb.row[wl][k] = I;
   }
   return true;
 }
@@ -597,16 +662,18 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
           uint32_t extra_tx) {
   using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
   constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
+  __shared__ RowBuffers<T, WarpTile<T, VR, U>::NB, WARPS> rb;
   // let the finaliser (launched as a programmatic dependent) get scheduled as
   // blocks of this grid retire; it waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int wl = threadIdx.x >> 5;
   const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
-  if (w >= p.W) return;
+  if (lane < 2) rb.row[wl][lane] = -1;
+  __syncwarp();
 
   Ring rg{0u, 0u, 0, 0u, extra_tx};
-  if (RING) {
+  if (RING && w < p.W) {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* base = smem + (size_t)wl * Lay::WARP_BYTES;
     rg.data = smem_addr(base);
@@ -618,9 +685,14 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     }
     __syncwarp();
   }
-  if (!stream_warp<T, VR, U, STAGES, RING, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr,
-                                                       wt, rt, limit_ns))
-    if (lane == 0) atomicMax(status, epoch);
+  bool ok = true;
+  if (w < p.W)
+    ok = stream_warp<T, VR, U, STAGES, RING, ALIGNED, R, WARPS>(p, w, wl, blockIdx.x, lane, rg, A,
+                                                                lda, x, incx, Wc, Wr, wt, rt, rb,
+                                                                limit_ns);
+  if (!ok && lane == 0) atomicMax(status, epoch);   // (its row buffers are incomplete: y is NaN)
+  __syncthreads();
+  row_partials_combine<T, WarpTile<T, VR, U>::NB, WARPS>(p, Wr, rt, blockIdx.x, rb);
 }
 
 // ----------------------------------------------------------------------------

@@ -13,17 +13,17 @@
 // it, so every column has exactly one owner.
 //
 // Deterministic cross-warp accumulation (the role the report's ordered
-// tickets play, "CUDA-xSYMV の実装と評価" §2.1, figure "Atomic"): a warp
-// writes
-//   * one column partial per column it owns, to Wc[I*n + j], and
-//   * one row partial per block row in which it owns columns, to slot q of
-//     that row, Wr[(I*qmax + q)*NB + r], q = w - (owner of the row's first
-//     column);
+// tickets play, "CUDA-xSYMV の実装と評価" §2.1, figure "Atomic"):
+//   * a warp writes one column partial per column it owns, to Wc[I*n + j];
+//   * the G warps of a thread block (warps b*G .. b*G+G-1) add their row
+//     partials of block row I in warp order, and the block writes the sum to
+//     slot q of that row, Wr[(I*qmax + q)*NB + r], q = b - (block of the
+//     owner of the row's first column);
 // a second kernel then sums those slots for every output element in a fixed
 // order, so results are bit-identical from run to run.  Warp ranges are at
 // least max(cd, cg) units long, so every warp between the owners of a row's
-// first and last columns owns columns in that row: no slot a finaliser reads
-// is left unwritten.
+// first and last columns owns columns in that row, hence every block between
+// their blocks does: no slot a finaliser reads is left unwritten.
 #pragma once
 
 #ifdef __CUDACC__
@@ -43,7 +43,8 @@ struct Plan {
   int cg;           // cost of a diagonal-tile column
   long long SC;     // total cost
   int W;            // warps sharing the cost (1 <= W <= SC / max(cd, cg))
-  int qmax;         // most warps that touch one block row
+  int G;            // warps per thread block: row partials are written per block
+  int qmax;         // most blocks that touch one block row
 };
 
 XSYMV_HD long long plan_rowlen(const Plan& p, int I) {
@@ -122,7 +123,10 @@ XSYMV_HD int plan_first_owner(const Plan& p, int I) { return plan_owner(p, plan_
 XSYMV_HD int plan_last_owner(const Plan& p, int I) {
   return plan_owner(p, plan_rowstart(p, I) + plan_col_cost(p, I, plan_rowlen(p, I) - 1));
 }
-XSYMV_HD int plan_nq(const Plan& p, int I) { return plan_last_owner(p, I) - plan_first_owner(p, I) + 1; }
+// row-partial slots of block row I: the blocks owning its columns
+XSYMV_HD int plan_nq(const Plan& p, int I) {
+  return plan_last_owner(p, I) / p.G - plan_first_owner(p, I) / p.G + 1;
+}
 
 // block row containing cost unit s (binary search)
 XSYMV_HD int plan_row_of(const Plan& p, long long s) {
@@ -136,13 +140,14 @@ XSYMV_HD int plan_row_of(const Plan& p, long long s) {
 
 XSYMV_HD long long plan_total_cost(int n, int NB, int upper, int cd, int cg) {
   if (n <= 0) return 0;
-  Plan p{n, NB, (n + NB - 1) / NB, upper, cd, cg, 0, 1, 1};
+  Plan p{n, NB, (n + NB - 1) / NB, upper, cd, cg, 0, 1, 1, 1};
   return plan_rowstart(p, p.nb - 1) + plan_rowcost(p, p.nb - 1);
 }
 
-// Build the plan for n, NB, uplo with at most Wmax warps; a dense column
-// costs cd units and a diagonal-tile column cg units (cd, cg >= 1).
-inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int cg = 1) {
+// Build the plan for n, NB, uplo with at most Wmax warps in blocks of G; a
+// dense column costs cd units and a diagonal-tile column cg units (cd, cg >= 1).
+inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int cg = 1,
+                      int G = 1) {
   Plan p{};
   p.n = n;
   p.NB = NB;
@@ -154,6 +159,7 @@ inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int 
   const long long unit = cd > cg ? cd : cg;
   long long W = Wmax < p.SC / unit ? Wmax : p.SC / unit;
   p.W = (int)(W < 1 ? 1 : W);
+  p.G = G < 1 ? 1 : G;
   p.qmax = 1;
   for (int I = 0; I < p.nb; ++I) {
     int q = plan_nq(p, I);
@@ -184,9 +190,9 @@ XSYMV_HD bool plan_cost_cols(const Plan& p, long long cs, long long ce, int I, l
 //     columns in row y (rows strictly between are wholly its own).  A row
 //     whose share holds no column start gets an empty range (z or w at the
 //     row's other end).
-//   row table, one int2 per block row I: x = the owner of its first column
-//     (row-partial slot q of warp w is w - x), y = the number of warps that
-//     own columns of the row (slots 0 .. y-1).
+//   row table, one int2 per block row I: x = the thread block of the owner
+//     of its first column (block b's row-partial slot in the row is b - x),
+//     y = the number of blocks that own columns of the row (slots 0 .. y-1).
 XSYMV_HD void plan_warp_entry(const Plan& p, int w, int* Ia, int* Ib, long long* ja, long long* jb) {
   const long long cs = plan_wstart(p, w), ce = plan_wstart(p, w + 1);
   *Ia = plan_row_of(p, cs);
@@ -223,14 +229,9 @@ XSYMV_HD bool plan_warp_cols(const Plan& p, int w, int I, long long* ja, long lo
 }
 
 // columns of block row I owned by warps w0 .. w1-1 (a contiguous run,
-// their union) and those warps' row-partial slots qa .. qb in the row
-XSYMV_HD bool plan_group_cols(const Plan& p, int w0, int w1, int I, long long* ja, long long* jb,
-                              int* qa, int* qb) {
-  if (!plan_cost_cols(p, plan_wstart(p, w0), plan_wstart(p, w1), I, ja, jb)) return false;
-  const int f = plan_first_owner(p, I), l = plan_last_owner(p, I);
-  *qa = (w0 > f ? w0 : f) - f;
-  *qb = (w1 - 1 < l ? w1 - 1 : l) - f;
-  return true;
+// their union)
+XSYMV_HD bool plan_group_cols(const Plan& p, int w0, int w1, int I, long long* ja, long long* jb) {
+  return plan_cost_cols(p, plan_wstart(p, w0), plan_wstart(p, w1), I, ja, jb);
 }
 
 // number of link ranges of chunk K

@@ -74,7 +74,7 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
 //
 // * The array holds kNoallocScratchBytes (16 MiB) on every GPU that loads
 //   this library, until the process exits.  Problems whose workspace does
-//   not fit (roughly n > 21000 with the tuned kernels on GB300) are
+//   not fit (roughly n > 31000 with the tuned kernels on GB300) are
 //   rejected with XSYMV_ERR_TOO_LARGE before anything is enqueued.
 // * The first call on a device looks up the array's device address
 //   (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -130,7 +130,7 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream, size_t* dev_ind
     xsymv::record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  g_noalloc_devices.push_back(NoallocDevice{d, p, 1, xsymv::TablesKey{-1, 0, 0, 0, 0, 0}});
+  g_noalloc_devices.push_back(NoallocDevice{d, p, 1, xsymv::TablesKey{-1, 0, 0, 0, 0, 0, 0}});
   *out = p;
   *epoch = 1;
   *dev_index = g_noalloc_devices.size() - 1;
@@ -194,7 +194,7 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
     TablesKey& have = g_noalloc_devices[dev_index].tables;
     if (memcmp(&have, &key, sizeof(key)) != 0) {
       e = launch_plan_tables(wl.plan, ws + tab_off, st);
-      have = e == cudaSuccess ? key : TablesKey{-1, 0, 0, 0, 0, 0};
+      have = e == cudaSuccess ? key : TablesKey{-1, 0, 0, 0, 0, 0, 0};
       ++launches;
     }
   }

@@ -126,27 +126,28 @@ struct TicketCtx {
   int mode;                   // kFull or kBetaZero
   T* y;                       // logical element 0 of y
   long long incy;
+  const int2* rt;             // the plan's row table
 };
 
 // A block's share of one block row: the columns [ja, jb) its warps own
-// (ja >= jb: none) and their row-partial slots qa .. qb.
+// (ja >= jb: none).
 struct GroupRow {
   long long ja, jb;
-  int qa, qb;
 };
 
 // the group's rows Ia..Ib; rows Ia .. Ia+kTkRows-1 are in shared memory,
 // later ones (only when a block's share spans more block rows) recomputed
 struct GroupRows {
   int w0, w1;          // warps of the group
+  int gid;             // the group's (block's) index: its row-partial slots
   int Ia, Ib;
   const GroupRow* sm;  // kTkRows entries
 };
 
 __device__ __forceinline__ GroupRow group_row(const Plan& p, const GroupRows& g, int I) {
   if (I - g.Ia < kTkRows) return g.sm[I - g.Ia];
-  GroupRow r{0, 0, 0, -1};
-  if (!plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb, &r.qa, &r.qb)) r.ja = r.jb = 0;
+  GroupRow r{0, 0};
+  if (!plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb)) r.ja = r.jb = 0;
   return r;
 }
 
@@ -180,7 +181,7 @@ __device__ __forceinline__ int next_chunk(const Plan& p, const GroupRows& g, int
 
 // The group's partial sums of chunk K, added to s[m] (lane l holds outputs
 // K*NB + l + 32m, m < M): column partials of its rows in increasing row
-// order, then, in row K, the row partials of its slots in slot order.
+// order, then, in row K, the group's row partial (its slot of the row).
 // has[m] is false where there was no term yet.  Offsets are 32-bit.
 template <class T, int M>
 __device__ __forceinline__ void chunk_part(const Plan& p, const TicketCtx<T>& c,
@@ -208,16 +209,13 @@ __device__ __forceinline__ void chunk_part(const Plan& p, const TicketCtx<T>& c,
       }
     }
     if (I == K) {
-#pragma unroll 1
-      for (int q = r.qa; q <= r.qb; ++q) {
-        const T* wr = c.Wr + ((long long)K * p.qmax + q) * p.NB + lane;
+      const T* wr = c.Wr + ((long long)K * p.qmax + (g.gid - __ldg(&c.rt[K].x))) * p.NB + lane;
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          if (lane + 32 * m < live) {
-            const T t = ld_l2(wr + 32 * m);
-            s[m] = has[m] ? Ops<T>::add(s[m], t) : t;
-            has[m] = true;
-          }
+      for (int m = 0; m < M; ++m) {
+        if (lane + 32 * m < live) {
+          const T t = ld_l2(wr + 32 * m);
+          s[m] = has[m] ? Ops<T>::add(s[m], t) : t;
+          has[m] = true;
         }
       }
     }
@@ -386,20 +384,25 @@ symv_ticket(Plan p, const T* __restrict__ A, long long lda, const T* __restrict_
   constexpr int NB = WarpTile<T, VR, U>::NB;
   __shared__ int s_blk;
   __shared__ GroupRow s_rows[kTkRows];
+  __shared__ RowBuffers<T, NB, WARPS> rb;
   if (threadIdx.x == 0) s_blk = atomicAdd(ctr + kTkStart, 1);
-  __syncthreads();
-  const int blk = s_blk;
   const int lane = threadIdx.x & 31;
   const int wl = (int)(threadIdx.x >> 5);
+  if (lane < 2) rb.row[wl][lane] = -1;
+  __syncthreads();
+  const int blk = s_blk;
   const int w = blk * WARPS + wl;
   if (w < p.W) {
     Ring rg{0u, 0u, 0, 0u, 0u};
-    stream_warp<T, VR, U, 1, false, ALIGNED, R>(p, w, lane, rg, A, lda, x, incx, Wc, Wr, wt, rt,
-                                                c.limit_ns);
+    stream_warp<T, VR, U, 1, false, ALIGNED, R, WARPS>(p, w, wl, blk, lane, rg, A, lda, x, incx,
+                                                       Wc, Wr, wt, rt, rb, c.limit_ns);
   }
+  __syncthreads();
+  row_partials_combine<T, NB, WARPS>(p, Wr, rt, blk, rb);
   // the block's warps act as one contributor: their workspace writes are
   // visible to the whole block after the barrier
   GroupRows g;
+  g.gid = blk;
   g.w0 = blk * WARPS;
   g.w1 = g.w0 + WARPS < p.W ? g.w0 + WARPS : p.W;
   g.sm = s_rows;
@@ -407,10 +410,9 @@ symv_ticket(Plan p, const T* __restrict__ A, long long lda, const T* __restrict_
     g.Ia = plan_row_of(p, plan_wstart(p, g.w0));
     g.Ib = plan_row_of(p, plan_wstart(p, g.w1) - 1);
     if ((int)threadIdx.x < kTkRows) {
-      GroupRow r{0, 0, 0, -1};
+      GroupRow r{0, 0};
       const int I = g.Ia + (int)threadIdx.x;
-      if (I > g.Ib || !plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb, &r.qa, &r.qb))
-        r.ja = r.jb = 0;
+      if (I > g.Ib || !plan_group_cols(p, g.w0, g.w1, I, &r.ja, &r.jb)) r.ja = r.jb = 0;
       s_rows[threadIdx.x] = r;
     }
   }

@@ -16,13 +16,17 @@
 
 using namespace xsymv;
 
+static int g_G = 1;   // warps per block of the case being checked
+
 static int fail(const char* what, int n, int NB, int upper, long long W, int cd, int cg) {
-  std::printf("FAIL %s n=%d NB=%d upper=%d W=%lld cd=%d cg=%d\n", what, n, NB, upper, W, cd, cg);
+  std::printf("FAIL %s n=%d NB=%d upper=%d W=%lld cd=%d cg=%d G=%d\n", what, n, NB, upper, W, cd,
+              cg, g_G);
   return 1;
 }
 
 static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
-  const Plan p = plan_make(n, NB, upper, Wmax, cd, cg);
+  const Plan p = plan_make(n, NB, upper, Wmax, cd, cg, g_G);
+  const int G = p.G;
   const int nb = p.nb;
   // owners[I][c] = warp owning column c of block row I, from the kernel loop
   std::vector<std::vector<int>> own(nb);
@@ -47,7 +51,8 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
         if (plan_owner(p, rcs + plan_col_cost(p, I, c)) != w)
           return fail("owner rule", n, NB, upper, Wmax, cd, cg);
       }
-      const int q = w - plan_first_owner(p, I);
+      // the row-partial slot of the warp's block
+      const int q = w / G - plan_first_owner(p, I) / G;
       if (q < 0 || q >= plan_nq(p, I) || q >= p.qmax)
         return fail("slot index", n, NB, upper, Wmax, cd, cg);
       row_warps[I].push_back(w);
@@ -58,11 +63,14 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
     for (int o : own[I])
       if (o < 0) return fail("column not owned", n, NB, upper, Wmax, cd, cg);
     total += (long long)own[I].size();
-    // the warps of a row are exactly first_owner .. last_owner, each once
-    const int f = plan_first_owner(p, I), nq = plan_nq(p, I);
-    if ((int)row_warps[I].size() != nq) return fail("slot holes", n, NB, upper, Wmax, cd, cg);
-    for (int k = 0; k < nq; ++k)
+    // the warps of a row are exactly first_owner .. last_owner, each once, so
+    // its blocks are exactly first_owner/G .. last_owner/G: the slots have
+    // no holes
+    const int f = plan_first_owner(p, I), l = plan_last_owner(p, I);
+    if ((int)row_warps[I].size() != l - f + 1) return fail("slot holes", n, NB, upper, Wmax, cd, cg);
+    for (int k = 0; k <= l - f; ++k)
       if (row_warps[I][k] != f + k) return fail("slot order", n, NB, upper, Wmax, cd, cg);
+    if (plan_nq(p, I) != l / G - f / G + 1) return fail("slot count", n, NB, upper, Wmax, cd, cg);
   }
   // total segments = stored columns per block row, as the report's triangle
   long long want = 0;
@@ -141,6 +149,11 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
       }
     }
     if (ja > INT32_MAX || jb > INT32_MAX) return fail("warp table range", n, NB, upper, Wmax, cd, cg);
+    // a row strictly between the warp's first and last rows is its alone:
+    // the kernel writes that row partial straight to the block's slot
+    for (int I = Ia + 1; I < Ib; ++I)
+      if (row_warps[I].size() != 1 || row_warps[I][0] != w)
+        return fail("middle row shared", n, NB, upper, Wmax, cd, cg);
   }
   // the same chains between groups of G consecutive warps (thread blocks)
   for (int G : {1, 3, 8}) {
@@ -170,17 +183,16 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
         return fail("group chunks", n, NB, upper, Wmax, cd, cg);
       for (int I = Ia; I <= Ib; ++I) {
         long long ja, jb;
-        int qa, qb;
-        const bool has = plan_group_cols(p, w0, w1, I, &ja, &jb, &qa, &qb);
-        // the group's columns are the union of its warps' columns, and its
-        // slots are exactly the slots of its warps that own columns there
+        const bool has = plan_group_cols(p, w0, w1, I, &ja, &jb);
+        // the group's columns are the union of the columns of its warps that
+        // own columns there (a contiguous run of warps)
         std::vector<int> slots;
         for (int w : row_warps[I])
           if (w >= w0 && w < w1) slots.push_back(w - plan_first_owner(p, I));
         if (has != !slots.empty()) return fail("group cols", n, NB, upper, Wmax, cd, cg);
         if (!has) continue;
-        if (qa != slots.front() || qb != slots.back() || (int)slots.size() != qb - qa + 1)
-          return fail("group slots", n, NB, upper, Wmax, cd, cg);
+        if ((int)slots.size() != slots.back() - slots.front() + 1)
+          return fail("group warps", n, NB, upper, Wmax, cd, cg);
         for (long long c = 0; c < (long long)own[I].size(); ++c) {
           const long long j = plan_colbase(p, I) + c;
           const bool mine = own[I][c] >= w0 && own[I][c] < w1;
@@ -202,10 +214,12 @@ int main() {
     for (int NB : edges)
       for (int upper = 0; upper < 2; ++upper)
         for (long long W : warps)
-          for (auto& c : costs) {
-            bad += check(n, NB, upper, W, c[0], c[1]);
-            ++cases;
-          }
+          for (auto& c : costs)
+            for (int G : {1, 8}) {
+              g_G = G;
+              bad += check(n, NB, upper, W, c[0], c[1]);
+              ++cases;
+            }
   std::printf("%d cases, %d failures\n", cases, bad);
   return bad ? 1 : 0;
 }

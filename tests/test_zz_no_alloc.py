@@ -70,7 +70,13 @@ def test_noalloc_rejects_too_large():
     _build.build()
     lib = xs.load()
     fn = _noalloc(lib)
-    n = 30000
+    # A below is far smaller than an n-by-n matrix: the call is only safe if
+    # it is rejected before anything is enqueued.  So n is chosen so that the
+    # column partials alone (one per 512 rows or fewer, per column) exceed
+    # the 16 MiB array whatever kernel variant is tuned, and the library's
+    # own workspace estimate is checked first.
+    n = 100000
+    assert xs.xsymv_workspace_bytes("s", "U", n) > (16 << 20)
     y = torch.full((n,), 3.0, device="cuda")
     A = torch.zeros(16, device="cuda")
     st = fn(b"U", n, 1.0, ctypes.c_void_p(A.data_ptr()), n, ctypes.c_void_p(y.data_ptr()), 1, 0.0,
