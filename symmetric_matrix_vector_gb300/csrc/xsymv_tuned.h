@@ -14,32 +14,32 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1820.9 GB/s at n=4096
-    {'s', 1, 12288, 12},   // vr1_u2_r0_w8_b6_g9 3855.5 GB/s at n=8192
-    {'s', 1, 20480, 21},   // vr2_u2_r0_w8_b4_g11 6168.8 GB/s at n=16384
-    {'s', 1, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6580.0 GB/s at n=24576
-    {'s', 1, 2147483647, 20},   // vr2_u2_r0_w8_b4_g9 6802.5 GB/s at n=32768
-    {'s', 0, 6144, 12},   // vr1_u2_r0_w8_b6_g9 1638.8 GB/s at n=4096
-    {'s', 0, 12288, 13},   // vr1_u2_r0_w8_b6_g11 3855.5 GB/s at n=8192
-    {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6114.4 GB/s at n=16384
-    {'s', 0, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6575.7 GB/s at n=24576
-    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6786.6 GB/s at n=32768
-    {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1594.4 GB/s at n=8192
-    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2166.6 GB/s at n=24576
-    {'d', 0, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1572.6 GB/s at n=8192
-    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2169.8 GB/s at n=24576
-    {'c', 1, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4658.3 GB/s at n=8192
-    {'c', 1, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6501.4 GB/s at n=16384
-    {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4500.9 GB/s at n=8192
-    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6547.1 GB/s at n=16384
-    {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1053.5 GB/s at n=8192
-    {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1094.0 GB/s at n=16384
-    {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1050.5 GB/s at n=8192
-    {'z', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1095.9 GB/s at n=16384
-    {'w', 1, 6144, 9},   // vr4_u2_r0_w8_b0_g4_c4 117.0 GB/s at n=4096
+    {'s', 1, 6144, 15},   // vr1_u2_r0_w8_b6_g14 1933.3 GB/s at n=4096
+    {'s', 1, 12288, 14},   // vr1_u2_r0_w8_b0_g9 4025.7 GB/s at n=8192
+    {'s', 1, 20480, 21},   // vr2_u2_r0_w8_b4_g11 6146.2 GB/s at n=16384
+    {'s', 1, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6580.7 GB/s at n=24576
+    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6777.5 GB/s at n=32768
+    {'s', 0, 6144, 15},   // vr1_u2_r0_w8_b6_g14 1978.9 GB/s at n=4096
+    {'s', 0, 12288, 13},   // vr1_u2_r0_w8_b6_g11 3887.7 GB/s at n=8192
+    {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6148.8 GB/s at n=16384
+    {'s', 0, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6600.5 GB/s at n=24576
+    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6833.1 GB/s at n=32768
+    {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1577.0 GB/s at n=8192
+    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2165.1 GB/s at n=24576
+    {'d', 0, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1558.3 GB/s at n=8192
+    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2174.8 GB/s at n=24576
+    {'c', 1, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4660.9 GB/s at n=8192
+    {'c', 1, 2147483647, 16},   // vr2_u2_r0_w8_b4_g9 6484.2 GB/s at n=16384
+    {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4624.9 GB/s at n=8192
+    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6513.8 GB/s at n=16384
+    {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1054.4 GB/s at n=8192
+    {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1097.6 GB/s at n=16384
+    {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1044.2 GB/s at n=8192
+    {'z', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1099.1 GB/s at n=16384
+    {'w', 1, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 119.4 GB/s at n=4096
     {'w', 1, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 130.6 GB/s at n=8192
-    {'w', 0, 6144, 9},   // vr4_u2_r0_w8_b0_g4_c4 117.3 GB/s at n=4096
-    {'w', 0, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 130.4 GB/s at n=8192
+    {'w', 0, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 118.3 GB/s at n=4096
+    {'w', 0, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 131.0 GB/s at n=8192
 };
 // END TUNED TABLE
 
