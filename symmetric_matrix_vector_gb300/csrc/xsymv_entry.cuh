@@ -91,16 +91,28 @@ cudaError_t launch_main(const MainArgs<T>& a) {
     }
     configured = true;
   }
-  const unsigned grid = (unsigned)((a.plan.W + WARPS - 1) / WARPS);
   const unsigned long long limit = wait_limit_ns();
   const uint32_t extra = test_extra_tx();
+  // programmatic dependent launch: the blocks may be scheduled while the
+  // stream's previous kernel finishes; the kernel waits for its completion
+  // (griddepcontrol.wait) before touching global memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.plan.W + WARPS - 1) / WARPS));
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = a.aligned ? smem : 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a.aligned)
-    symv_main<T, VR, U, S, P, WARPS, true, MB, R><<<grid, WARPS * 32, smem, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, extra);
-  else
-    symv_main<T, VR, U, S, P, WARPS, false, MB, R><<<grid, WARPS * 32, 0, a.stream>>>(
-        a.plan, a.A, a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, extra);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, symv_main<T, VR, U, S, P, WARPS, true, MB, R>, a.plan, a.A,
+                              a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch,
+                              limit, extra);
+  return cudaLaunchKernelEx(&cfg, symv_main<T, VR, U, S, P, WARPS, false, MB, R>, a.plan, a.A,
+                            a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit,
+                            extra);
 }
 
 template <class T, int VR, int U, int S, int P, int WARPS, int MB, int R = U>

@@ -685,6 +685,10 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
     }
     __syncwarp();
   }
+  // launched as a programmatic dependent of the stream's previous kernel
+  // (the previous call's finaliser lets it start early): nothing of global
+  // memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   bool ok = true;
   if (w < p.W)
     ok = stream_warp<T, VR, U, STAGES, RING, ALIGNED, R, WARPS>(p, w, wl, blockIdx.x, lane, rg, A,
@@ -716,6 +720,9 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
               const int2* __restrict__ rt, T alpha, T beta, int mode, T* __restrict__ y,
               long long incy, const int* status, int epoch) {
   __shared__ T part[kFinParts][kFinCols];
+  // the next call's main kernel, a programmatic dependent, may be scheduled
+  // once every block of this grid runs; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // wait until the preceding grid on the stream (the main kernel) has
   // completed and its writes are visible (no-op without a programmatic launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
