@@ -100,12 +100,15 @@ KERNEL_SOURCES = ("xsymv_kernels.cuh", "xsymv_plan.h", "xsymv_scalar.cuh")
 
 
 def kernel_source_digest() -> str:
+    """digest of the main kernel's code: its headers without // comments and
+    blank lines, so that a comment edit does not void a traffic record"""
     csrc = os.path.join(ROOT, "symmetric_matrix_vector_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            code = [re.sub(r"//.*$", "", line).rstrip() for line in fh]
+        h.update(f.encode())
+        h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 

@@ -33,9 +33,13 @@
 //                  operation touches data, so results are bit-identical from
 //                  run to run.
 //
-// On GB300 the register path is the faster one for SSYMV/CHEMV: with about
-// 48 registers per thread, 40 warps per SM keep enough 16-byte loads in
-// flight to run near the copy bandwidth.  Every wait of the bulk-copy ring
+// On GB300 the register path is the faster one for SSYMV/CHEMV: what sets
+// the speed is the 16-byte loads in flight per SM, so the tuned variants cap
+// registers (40 per thread and 48 warps per SM with 4 rows per lane; 64 and
+// 32 warps with 8 rows per lane, twice the bytes per warp, at large n).
+// Both kernels are launched as programmatic dependents (main after the
+// stream's previous kernel, finaliser after main) and wait for their
+// predecessor before touching global memory.  Every wait of the bulk-copy ring
 // on an mbarrier has a time limit.  A wait that runs out marks the call
 // failed (status word := the call's epoch), waits (again with a limit) for
 // the warp's copies still in flight and leaves the kernel; the finaliser then

@@ -355,3 +355,36 @@ def test_bounded_wait_reports_timeout(lib):
     lib.xsymv_set_variant("s", -1)
     assert st == 0 and lib.xsymv_sync_status() == 0
     assert bool((again == good).all())
+
+
+@pytest.mark.parametrize("kind", ["s", "d", "z"])
+def test_chained_calls_read_previous_result(lib, kind):
+    """Each call's main kernel may be scheduled while the previous call's
+    finaliser still runs (programmatic launch); it must not read x before
+    that finaliser has written it.  Five calls y_{k+1} := A y_k, each
+    reading the previous call's y as its x, enqueued back to back on one
+    stream, give the same bytes as the same calls with the host waiting for
+    the GPU after each one."""
+    import torch
+
+    n = {"s": 3000, "d": 2000, "z": 1500}[kind]
+    al, _ = SCAL[kind]
+    zero = 0.0
+    p = inputs.make_problem(kind, "U", n, lda=n + 4, alpha=al, beta=zero, seed=77)
+    dp = DeviceProblem(p)
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+
+    def iterate(sync):
+        a, b = dp.x.clone(), dp.x.clone()
+        for _ in range(5):
+            st = lib.symv(kind, "U", n, al, dp.A, p.lda, a, 1, zero, b, 1)
+            assert st == 0
+            if sync:
+                torch.cuda.synchronize()
+            a, b = b, a
+        torch.cuda.synchronize()
+        return a
+
+    chained = iterate(False)
+    waited = iterate(True)
+    assert bool((chained == waited).all())
