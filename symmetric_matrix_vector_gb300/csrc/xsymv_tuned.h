@@ -24,10 +24,12 @@ static const TunedEntry kTuned[] = {
     {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6148.8 GB/s at n=16384
     {'s', 0, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6600.5 GB/s at n=24576
     {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6833.1 GB/s at n=32768
-    {'d', 1, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1577.0 GB/s at n=8192
-    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2165.1 GB/s at n=24576
-    {'d', 0, 16384, 13},   // vr2_u4_r0_w8_b0_g5_c8 1558.3 GB/s at n=8192
-    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2174.8 GB/s at n=24576
+    {'d', 1, 12288, 17},   // vr8_u1_r0_w4_b0_g8_c8 1677.9 GB/s at n=8192
+    {'d', 1, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2113.9 GB/s at n=16384
+    {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2170.2 GB/s at n=24576
+    {'d', 0, 12288, 17},   // vr8_u1_r0_w4_b0_g8_c8 1673.2 GB/s at n=8192
+    {'d', 0, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2093.0 GB/s at n=16384
+    {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2177.1 GB/s at n=24576
     {'c', 1, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4660.9 GB/s at n=8192
     {'c', 1, 2147483647, 16},   // vr2_u2_r0_w8_b4_g9 6484.2 GB/s at n=16384
     {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 4624.9 GB/s at n=8192
@@ -36,10 +38,10 @@ static const TunedEntry kTuned[] = {
     {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1097.6 GB/s at n=16384
     {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1044.2 GB/s at n=8192
     {'z', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1099.1 GB/s at n=16384
-    {'w', 1, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 119.4 GB/s at n=4096
-    {'w', 1, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 130.6 GB/s at n=8192
-    {'w', 0, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 118.3 GB/s at n=4096
-    {'w', 0, 2147483647, 8},   // vr4_u2_r0_w8_b0_g4_c8 131.0 GB/s at n=8192
+    {'w', 1, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 119.3 GB/s at n=4096
+    {'w', 1, 2147483647, 13},   // vr8_u1_r0_w4_b0_g6_c8 132.6 GB/s at n=8192
+    {'w', 0, 6144, 8},   // vr4_u2_r0_w8_b0_g4_c8 118.2 GB/s at n=4096
+    {'w', 0, 2147483647, 13},   // vr8_u1_r0_w4_b0_g6_c8 132.6 GB/s at n=8192
 };
 // END TUNED TABLE
 

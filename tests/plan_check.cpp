@@ -207,7 +207,7 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
 int main() {
   int bad = 0, cases = 0;
   const int sizes[] = {1, 2, 3, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 511, 700, 1025};
-  const int edges[] = {32, 64, 128, 256};
+  const int edges[] = {32, 64, 128, 256, 512};
   const long long warps[] = {1, 2, 3, 7, 64, 300, 1000, 7296, 1000000};
   const int costs[][2] = {{1, 1}, {4, 6}, {4, 3}, {2, 7}, {5, 1}};
   for (int n : sizes)

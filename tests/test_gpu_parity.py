@@ -85,7 +85,7 @@ def test_every_variant(o, lib, kind):
         for v in range(lib.xsymv_variant_count(kind)):
             assert lib.xsymv_set_variant(kind, v) == 0
             for uplo in ("U", "L"):
-                for n in (97, 700):
+                for n in (97, 700, 1300):    # 1300: three block rows of 512
                     p = inputs.make_problem(kind, uplo, n, lda=n + 2, alpha=al, beta=be,
                                             seed=100 + v)
                     run_and_check(o, p)
