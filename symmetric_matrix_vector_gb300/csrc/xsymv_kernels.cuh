@@ -443,11 +443,22 @@ struct WarpTile {
   // Columns [ja, jb) with per-element masks: rows must be < n and, when
   // DIAG, inside the stored triangle (upper: row <= col; lower: row >= col).
   // On the diagonal only the row term is taken (and for a Hermitian matrix
-  // only the real part of the element).  Elements outside the mask are
-  // never read.  U columns per step, like the dense loop, so that diagonal
-  // tiles keep as many loads in flight and do not hold their warps back;
-  // each element address is a running column pointer plus a constant.
-  template <bool DIAG>
+  // only the real part of the element).  U columns per step, like the dense
+  // loop, so that diagonal tiles keep as many loads in flight and do not
+  // hold their warps back; each element address is a running column pointer
+  // plus a constant.
+  //
+  // VEC (16-byte aligned matrices): a lane's VPL consecutive rows that are
+  // all below row n and hold at least one element inside the mask are read
+  // as one 16-byte vector, the way dense columns are; a vector that crosses
+  // the diagonal then also brings the up to VPL - 1 elements beside it on
+  // the other side (in the same 32-byte sector, inside the caller's array:
+  // rows < n <= lda), which are never used.  Per element loads, the
+  // diagonal tiles issued VPL times the requests per byte of the dense
+  // columns, and their warps fell behind when the tiles came from DRAM.
+  // Without VEC, elements outside the mask are never read.  The arithmetic,
+  // and so the rounding, is the same either way.
+  template <bool DIAG, bool VEC = false>
   __device__ __forceinline__ void masked_cols(const T* __restrict__ A, long long lda,
                                               const T* __restrict__ x, int incx, long long r0,
                                               long long ja, long long jb, T* wc_row, int lane,
@@ -460,6 +471,23 @@ struct WarpTile {
       const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
       const int jl0 = (int)(j0 - r0);
       const T xl = (lane < cnt) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
+      // VEC: the step's vectors, all issued before the arithmetic (as in
+      // the dense loop); a vector below row n but wholly outside the mask is
+      // not read (zeros stand in)
+      uint4 raw[VEC ? U : 1][VEC ? VR : 1];
+      if (VEC) {
+        const T* c = col;
+#pragma unroll
+        for (int u = 0; u < U; ++u, c += lda)
+#pragma unroll
+          for (int v = 0; v < VR; ++v) {
+            const int rl0 = lane_row(v, lane, 0);
+            const int jl = jl0 + u;
+            const bool need = u < cnt && rl0 + VPL <= nl &&
+                              (!DIAG || (upper ? rl0 <= jl : rl0 + VPL - 1 >= jl));
+            raw[VEC ? u : 0][VEC ? v : 0] = need ? ldg_stream16(c + rl0) : make_uint4(0u, 0u, 0u, 0u);
+          }
+      }
       T cp[U];
       const T* c = col;
 #pragma unroll
@@ -468,14 +496,17 @@ struct WarpTile {
         const T xj = Ops<T>::shfl(xl, u);
         T cu = Ops<T>::zero();
 #pragma unroll
-        for (int v = 0; v < VR; ++v)
+        for (int v = 0; v < VR; ++v) {
+          T av[VPL];
+          if (VEC) Unpack<T>::run(raw[VEC ? u : 0][VEC ? v : 0], av);
+          const bool whole = VEC && lane_row(v, lane, 0) + VPL <= nl;   // read as a vector
 #pragma unroll
           for (int k = 0; k < VPL; ++k) {
             const int rl = lane_row(v, lane, k);
             bool valid = u < cnt;
             if (DIAG) valid = valid && rl < nl && (upper ? rl <= jl : rl >= jl);
             if (valid) {
-              T a = Ops<T>::load(c + rl);
+              T a = whole ? av[k] : Ops<T>::load(c + rl);
               if (DIAG && rl == jl) {
                 racc[v][k] = Ops<T>::madd(racc[v][k], Ops<T>::diag(a), xj);
               } else {
@@ -484,6 +515,7 @@ struct WarpTile {
               }
             }
           }
+        }
         cp[u] = cu;
       }
       T red = reduce_scatter<T, U>(cp, lane);
@@ -619,13 +651,13 @@ __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int wl, int b,
     const long long a0 = ja > dA ? ja : dA;
     const long long a1 = p.upper ? (jb < dB ? jb : dB) : jb;
     if (a0 < a1)
-      t.template masked_cols<true>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, p.upper);
+      t.template masked_cols<true, ALIGNED>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, p.upper);
     const long long b0 = p.upper ? (ja > dB ? ja : dB) : ja;
     const long long b1 = p.upper ? jb : (jb < dA ? jb : dA);
     if (b0 < b1) {
       if (r0 + NB > n) {
         // a last, incomplete block row (lower storage only): rows masked
-        t.template masked_cols<true>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
+        t.template masked_cols<true, ALIGNED>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
       } else if (RING) {
         if (!t.template dense_cols_ring<(STAGES > 0 ? STAGES : 1)>(rg, A, lda, x, incx, r0, b0, b1,
                                                                    wc_row, lane, limit_ns))
