@@ -46,6 +46,8 @@
 // writes NaN to y and the host can read the status.
 #pragma once
 
+#include <type_traits>
+
 #include "xsymv_plan.h"
 #include "xsymv_scalar.cuh"
 
@@ -443,10 +445,10 @@ struct WarpTile {
   // Columns [ja, jb) with per-element masks: rows must be < n and, when
   // DIAG, inside the stored triangle (upper: row <= col; lower: row >= col).
   // On the diagonal only the row term is taken (and for a Hermitian matrix
-  // only the real part of the element).  U columns per step, like the dense
-  // loop, so that diagonal tiles keep as many loads in flight and do not
-  // hold their warps back; each element address is a running column pointer
-  // plus a constant.
+  // only the real part of the element).  UD columns per step (U, like the
+  // dense loop, unless the caller asks for fewer), so that diagonal tiles
+  // keep loads in flight and do not hold their warps back; each element
+  // address is a running column pointer plus a constant.
   //
   // VEC (16-byte aligned matrices): a lane's VPL consecutive rows that are
   // all below row n and hold at least one element inside the mask are read
@@ -458,7 +460,7 @@ struct WarpTile {
   // columns, and their warps fell behind when the tiles came from DRAM.
   // Without VEC, elements outside the mask are never read.  The arithmetic,
   // and so the rounding, is the same either way.
-  template <bool DIAG, bool VEC = false>
+  template <bool DIAG, bool VEC = false, int UD = U>
   __device__ __forceinline__ void masked_cols(const T* __restrict__ A, long long lda,
                                               const T* __restrict__ x, int incx, long long r0,
                                               long long ja, long long jb, T* wc_row, int lane,
@@ -467,18 +469,18 @@ struct WarpTile {
     // rows and columns relative to r0 fit in 32 bits (|j - r0| < n)
     const int nl = (int)((n - r0) < NB ? (n - r0) : NB);
 #pragma unroll 1
-    for (long long j0 = ja; j0 < jb; j0 += U, col += U * lda) {
-      const int cnt = (int)((jb - j0) < U ? (jb - j0) : U);
+    for (long long j0 = ja; j0 < jb; j0 += UD, col += UD * lda) {
+      const int cnt = (int)((jb - j0) < UD ? (jb - j0) : UD);
       const int jl0 = (int)(j0 - r0);
       const T xl = (lane < cnt) ? Ops<T>::load(x + (j0 + lane) * incx) : Ops<T>::zero();
       // VEC: the step's vectors, all issued before the arithmetic (as in
       // the dense loop); a vector below row n but wholly outside the mask is
       // not read (zeros stand in)
-      uint4 raw[VEC ? U : 1][VEC ? VR : 1];
+      uint4 raw[VEC ? UD : 1][VEC ? VR : 1];
       if (VEC) {
         const T* c = col;
 #pragma unroll
-        for (int u = 0; u < U; ++u, c += lda)
+        for (int u = 0; u < UD; ++u, c += lda)
 #pragma unroll
           for (int v = 0; v < VR; ++v) {
             const int rl0 = lane_row(v, lane, 0);
@@ -488,10 +490,10 @@ struct WarpTile {
             raw[VEC ? u : 0][VEC ? v : 0] = need ? ldg_stream16(c + rl0) : make_uint4(0u, 0u, 0u, 0u);
           }
       }
-      T cp[U];
+      T cp[UD];
       const T* c = col;
 #pragma unroll
-      for (int u = 0; u < U; ++u, c += lda) {
+      for (int u = 0; u < UD; ++u, c += lda) {
         const int jl = jl0 + u;
         const T xj = Ops<T>::shfl(xl, u);
         T cu = Ops<T>::zero();
@@ -518,9 +520,10 @@ struct WarpTile {
         }
         cp[u] = cu;
       }
-      T red = reduce_scatter<T, U>(cp, lane);
-      const int uo = lane >> (5 - H);
-      if ((lane & ((32 >> H) - 1)) == 0 && uo < cnt) wc_row[j0 + uo] = red;
+      T red = reduce_scatter<T, UD>(cp, lane);
+      constexpr int HD = Log2<UD>::v;
+      const int uo = lane >> (5 - HD);
+      if ((lane & ((32 >> HD) - 1)) == 0 && uo < cnt) wc_row[j0 + uo] = red;
     }
   }
 };
@@ -622,6 +625,11 @@ __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int wl, int b,
   using Tile = WarpTile<T, VR, U>;
   constexpr int VPL = Tile::VPL;
   constexpr int NB = Tile::NB;
+  // columns per step in the diagonal tiles: one for the single-precision
+  // kinds read as vectors (with U columns the step's vectors and masks
+  // spilled under those kernels' register caps), U otherwise
+  constexpr bool kSingle = std::is_same<T, float>::value || std::is_same<T, c32>::value;
+  constexpr int UD = (ALIGNED && kSingle) ? 1 : U;
   const int4 d = __ldg(wt + w);   // rows d.x .. d.y, from column d.z to column d.w
   const long long n = p.n;
   Tile t;
@@ -651,13 +659,13 @@ __device__ __forceinline__ bool stream_warp(const Plan& p, int w, int wl, int b,
     const long long a0 = ja > dA ? ja : dA;
     const long long a1 = p.upper ? (jb < dB ? jb : dB) : jb;
     if (a0 < a1)
-      t.template masked_cols<true, ALIGNED>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, p.upper);
+      t.template masked_cols<true, ALIGNED, UD>(A, lda, x, incx, r0, a0, a1, wc_row, lane, n, p.upper);
     const long long b0 = p.upper ? (ja > dB ? ja : dB) : ja;
     const long long b1 = p.upper ? jb : (jb < dA ? jb : dA);
     if (b0 < b1) {
       if (r0 + NB > n) {
         // a last, incomplete block row (lower storage only): rows masked
-        t.template masked_cols<true, ALIGNED>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
+        t.template masked_cols<true, ALIGNED, UD>(A, lda, x, incx, r0, b0, b1, wc_row, lane, n, 0);
       } else if (RING) {
         if (!t.template dense_cols_ring<(STAGES > 0 ? STAGES : 1)>(rg, A, lda, x, incx, r0, b0, b1,
                                                                    wc_row, lane, limit_ns))

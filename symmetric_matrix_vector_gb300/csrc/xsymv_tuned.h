@@ -14,26 +14,26 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 25},   // vr2_u2_r0_w8_b4_g8 1982.7 GB/s at n=4096
-    {'s', 1, 12288, 12},   // vr1_u2_r0_w8_b6_g9 4025.7 GB/s at n=8192
-    {'s', 1, 20480, 21},   // vr2_u2_r0_w8_b4_g11 6122.8 GB/s at n=16384
-    {'s', 1, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6546.1 GB/s at n=24576
-    {'s', 1, 2147483647, 20},   // vr2_u2_r0_w8_b4_g9 6735.2 GB/s at n=32768
-    {'s', 0, 6144, 14},   // vr1_u2_r0_w8_b0_g9 1982.7 GB/s at n=4096
-    {'s', 0, 12288, 12},   // vr1_u2_r0_w8_b6_g9 4029.6 GB/s at n=8192
-    {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6127.3 GB/s at n=16384
-    {'s', 0, 28672, 21},   // vr2_u2_r0_w8_b4_g11 6488.2 GB/s at n=24576
-    {'s', 0, 2147483647, 22},   // vr2_u2_r0_w8_b4_g13 6746.7 GB/s at n=32768
+    {'s', 1, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1940.5 GB/s at n=4096
+    {'s', 1, 12288, 21},   // vr2_u2_r0_w8_b4_g11 4002.7 GB/s at n=8192
+    {'s', 1, 20480, 21},   // vr2_u2_r0_w8_b4_g11 6175.9 GB/s at n=16384
+    {'s', 1, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6529.1 GB/s at n=24576
+    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6741.6 GB/s at n=32768
+    {'s', 0, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1977.1 GB/s at n=4096
+    {'s', 0, 12288, 21},   // vr2_u2_r0_w8_b4_g11 4006.5 GB/s at n=8192
+    {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6190.6 GB/s at n=16384
+    {'s', 0, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6521.8 GB/s at n=24576
+    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6753.9 GB/s at n=32768
     {'d', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1817.5 GB/s at n=8192
     {'d', 1, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2120.0 GB/s at n=16384
     {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2170.6 GB/s at n=24576
     {'d', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1840.6 GB/s at n=8192
     {'d', 0, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2116.3 GB/s at n=16384
     {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2175.2 GB/s at n=24576
-    {'c', 1, 12288, 16},   // vr2_u2_r0_w8_b4_g9 5153.3 GB/s at n=8192
-    {'c', 1, 2147483647, 16},   // vr2_u2_r0_w8_b4_g9 6298.5 GB/s at n=16384
-    {'c', 0, 12288, 15},   // vr2_u2_r0_w8_b4_g7 5185.2 GB/s at n=8192
-    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6494.2 GB/s at n=16384
+    {'c', 1, 12288, 17},   // vr2_u2_r0_w8_b4_g11 5182.0 GB/s at n=8192
+    {'c', 1, 2147483647, 16},   // vr2_u2_r0_w8_b4_g9 6352.0 GB/s at n=16384
+    {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 5182.0 GB/s at n=8192
+    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6527.8 GB/s at n=16384
     {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1060.8 GB/s at n=8192
     {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1096.4 GB/s at n=16384
     {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1061.0 GB/s at n=8192
