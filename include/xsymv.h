@@ -20,8 +20,13 @@
  *   n      order of A, n >= 0.
  *   alpha  scalar, passed by value.
  *   A      DEVICE pointer to the matrix, column-major: A(i,j) at A[i + j*lda].
- *          Only the uplo triangle (diagonal included) is read; for Hermitian
- *          A the imaginary parts of the diagonal are not read either.
+ *          Only the uplo triangle (diagonal included) is used; for Hermitian
+ *          A the imaginary parts of the diagonal are not used either.  On a
+ *          16-byte aligned matrix the diagonal tiles are loaded as 16-byte
+ *          vectors, which may also fetch up to 3 (float) or 1 (double,
+ *          complex float) elements of the other triangle next to the
+ *          diagonal; those values are never used (NaN there is harmless).
+ *          Nothing outside rows and columns 0 .. n-1 is read.
  *   lda    leading dimension, lda >= max(1, n).
  *   x      DEVICE pointer; element i at x[kx + i*incx], kx = 0 if incx > 0,
  *          else (1-n)*incx (negative strides run backwards, as in BLAS).
