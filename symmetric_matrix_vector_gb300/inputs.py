@@ -10,8 +10,8 @@ Layout (host numpy arrays, BLAS column-major):
     row ``j`` is matrix column ``j``, so ``A[j, i]`` is A(i, j).
   * Everything outside the stored triangle — the other triangle, the rows
     ``n..lda-1`` of each column, and for Hermitian matrices the imaginary
-    part of the diagonal — is filled with NaN, so a kernel that reads it
-    produces NaN.
+    part of the diagonal — is filled with NaN, so a kernel that uses any of
+    it in its arithmetic produces NaN.
   * ``x`` / ``y`` are strided vectors of ``1 + (n-1)*|inc|`` elements whose
     gap elements are NaN.
 

@@ -85,8 +85,11 @@ def test_every_variant(o, lib, kind):
         for v in range(lib.xsymv_variant_count(kind)):
             assert lib.xsymv_set_variant(kind, v) == 0
             for uplo in ("U", "L"):
-                for n in (97, 700, 1300):    # 1300: three block rows of 512
-                    p = inputs.make_problem(kind, uplo, n, lda=n + 2, alpha=al, beta=be,
+                # 16-byte aligned columns (vector loads, also in the diagonal
+                # tiles) and unaligned ones (element loads), ragged tails;
+                # 1300: three block rows of 512
+                for n, lda in ((97, 99), (700, 704), (1300, 1302), (1301, 1304)):
+                    p = inputs.make_problem(kind, uplo, n, lda=lda, alpha=al, beta=be,
                                             seed=100 + v)
                     run_and_check(o, p)
     finally:
