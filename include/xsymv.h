@@ -182,6 +182,12 @@ XSYMV_API int xsymv_set_wait_limit(unsigned long long ns);
  * its ticket, so the next calls' waits run out (nothing faults; the kernels
  * return after the time limit).  0 restores normal operation. */
 XSYMV_API int xsymv_test_stall(int on);
+/* Test hook: sets the last call number handed out on the current device and
+ * stream (calls number themselves 1, 2, ... to tag failures in the status
+ * word; after 0x7ffffffe they start again at 1 and the status word is
+ * cleared).  0 <= number <= 0x7ffffffe, and the stream must have a
+ * workspace (one earlier call); else XSYMV_ERR_VALUE, nothing changed. */
+XSYMV_API int xsymv_test_set_call_number(int number);
 
 /* Human-readable text for a status code (static storage). */
 XSYMV_API const char *xsymv_status_string(int status);

@@ -30,6 +30,7 @@ __all__ = [
     "xsymv_workspace_bytes", "XsymvError", "check", "load", "library_path", "ENTRY_POINTS",
     "xsymv_s_host", "xsymv_d_host", "xhemv_c_host", "xhemv_z_host", "xsymv_w_host", "symv_host",
     "xsymv_host_traffic", "xsymv_sync_status", "xsymv_set_wait_limit", "xsymv_test_stall",
+    "xsymv_test_set_call_number",
     "xsymv_probe_peaks", "xgemv_s", "xgemv_d", "gemv", "xgemv_variant_count",
     "xgemv_variant_name", "xgemv_set_variant", "xgemv_selected_variant",
 ]
@@ -91,6 +92,8 @@ def load():
         lib.xsymv_set_wait_limit.restype = c_int
         lib.xsymv_test_stall.argtypes = [c_int]
         lib.xsymv_test_stall.restype = c_int
+        lib.xsymv_test_set_call_number.argtypes = [c_int]
+        lib.xsymv_test_set_call_number.restype = c_int
         lib.xsymv_set_stream.argtypes = [vp]
         lib.xsymv_set_stream.restype = c_int
         lib.xsymv_get_stream.restype = vp
@@ -266,6 +269,10 @@ def xsymv_set_wait_limit(ns: int) -> int:
 
 def xsymv_test_stall(on: bool) -> int:
     return load().xsymv_test_stall(1 if on else 0)
+
+
+def xsymv_test_set_call_number(number: int) -> int:
+    return load().xsymv_test_set_call_number(int(number))
 
 
 def xsymv_probe_peaks():

@@ -158,8 +158,19 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
     }
   }
   if (epoch != nullptr) {
-    w->epoch = (w->epoch >= 0x7ffffffe) ? 1 : w->epoch + 1;
-    *epoch = w->epoch;
+    if (w->epoch >= 0x7ffffffe) {
+      // call numbers start again at 1: clear the status word first (on the
+      // stream, before this call's kernels), or a failure recorded under a
+      // larger old number would hide the failures of the next calls
+      e = cudaMemsetAsync(w->ptr, 0, 256, stream);
+      if (e != cudaSuccess) {
+        record_cuda_error(e);
+        *status = XSYMV_ERR_CUDA;
+        return nullptr;
+      }
+      w->epoch = 0;
+    }
+    *epoch = ++w->epoch;
   }
   return w->ptr;
 }
@@ -443,6 +454,24 @@ XSYMV_API int xsymv_set_wait_limit(unsigned long long ns) {
 XSYMV_API int xsymv_test_stall(int on) {
   g_extra_tx.store(on ? 16u : 0u);
   return XSYMV_OK;
+}
+
+XSYMV_API int xsymv_test_set_call_number(int number) {
+  if (number < 0 || number > 0x7ffffffe) return XSYMV_ERR_VALUE;
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  const cudaStream_t s = g_stream.load();
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (WsEntry& w : g_ws)
+    if (w.device == d && w.stream == s && w.slot == 0 && w.ptr != nullptr) {
+      w.epoch = number;
+      return XSYMV_OK;
+    }
+  return XSYMV_ERR_VALUE;
 }
 
 XSYMV_API int xsymv_host_traffic(long long* h2d_bytes, long long* d2h_bytes) {

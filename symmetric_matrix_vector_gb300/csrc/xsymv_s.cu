@@ -118,7 +118,17 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream, size_t* dev_ind
   for (size_t i = 0; i < g_noalloc_devices.size(); ++i) {
     NoallocDevice& s = g_noalloc_devices[i];
     if (s.device == d) {
-      s.epoch = (s.epoch >= 0x7ffffffe) ? 1 : s.epoch + 1;
+      if (s.epoch >= 0x7ffffffe) {
+        // call numbers start again at 1: clear the status word first (see
+        // the workspace's call numbers)
+        e = cudaMemsetAsync(s.scratch, 0, 256, stream);
+        if (e != cudaSuccess) {
+          xsymv::record_cuda_error(e);
+          return XSYMV_ERR_CUDA;
+        }
+        s.epoch = 0;
+      }
+      ++s.epoch;
       *out = s.scratch;
       *epoch = s.epoch;
       *dev_index = i;

@@ -360,6 +360,41 @@ def test_bounded_wait_reports_timeout(lib):
     assert bool((again == good).all())
 
 
+def test_call_numbers_wrap(lib):
+    """Calls tag failures in the status word with their call number; when the
+    numbers start again at 1 the word is cleared first, so a failure recorded
+    under a large old number does not hide the failures that follow."""
+    import torch
+
+    p = inputs.make_problem("s", "U", 700, lda=700, alpha=1.0, beta=0.0, seed=4)
+    dp = DeviceProblem(p)
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+    tma = [v for v in range(lib.xsymv_variant_count("s")) if "_t" in lib.xsymv_variant_name("s", v)]
+    assert tma and lib.xsymv_set_variant("s", tma[0]) == 0
+    try:
+        st, good = dp.run()
+        assert st == 0 and lib.xsymv_sync_status() == 0
+        assert lib.xsymv_test_set_call_number(0x7ffffffd) == 0
+        lib.xsymv_set_wait_limit(2_000_000)          # 2 ms
+        lib.xsymv_test_stall(True)
+        st, _ = dp.run()                             # call 0x7ffffffe fails
+        assert st == 0 and lib.xsymv_sync_status() == -6
+        lib.xsymv_test_stall(False)
+        st, again = dp.run()                         # call 1: the word is cleared
+        assert st == 0 and lib.xsymv_sync_status() == 0
+        assert bool((again == good).all())
+        lib.xsymv_test_stall(True)
+        st, bad = dp.run()                           # call 2 fails: reported
+        assert st == 0 and lib.xsymv_sync_status() == -6
+        assert np.all(np.isnan(from_device(bad, p.y)))
+    finally:
+        lib.xsymv_test_stall(False)
+        lib.xsymv_set_wait_limit(0)
+        lib.xsymv_set_variant("s", -1)
+    assert lib.xsymv_test_set_call_number(-1) == -4
+    assert lib.xsymv_test_set_call_number(0x7fffffff) == -4
+
+
 @pytest.mark.parametrize("kind", ["s", "d", "z"])
 def test_chained_calls_read_previous_result(lib, kind):
     """Each call's main kernel may be scheduled while the previous call's
