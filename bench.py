@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--n", type=int, default=32768)
-    ap.add_argument("--no-sweep", action="store_true", help="skip the n = 8K..32K sweep")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the n = 4096..32768 sweep")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kinds", action="store_true",
@@ -557,15 +557,13 @@ def run_ours(args):
         roofline["frac_same_run_copy"] = achieved / probes["copy_gbs"]
         roofline["frac_same_run_read"] = achieved / probes["read_gbs"]
 
-    # ---- size sweep (n = 8K..32K), beside the headline
+    # ---- size sweep (the workload's n = 4096 .. 32768 step 4096), beside the headline
     sweep = []
     if not args.no_sweep and rank == 0:
         del prob
-        for m in (8192, 16384, 24576, 32768):
-            if m == n:
-                sweep.append({"n": m, "gflops": flops(m) / (ms_per_step * 1e-3) / 1e9,
-                              "gbs": triangle_bytes(m) / (ms_per_step * 1e-3) / 1e9})
-                continue
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        clean = torch.zeros(64 << 20, dtype=torch.int64, device="cuda")
+        for m in range(4096, 32768 + 1, 4096):
             pm = inputs.device_problem("s", "U", m, lda=m + 32, alpha=1.0, beta=0.0, seed=m)
 
             def call():
@@ -574,44 +572,46 @@ def run_ours(args):
             for _ in range(5):
                 call()
             torch.cuda.synchronize()
-            cold = triangle_bytes(m) < 4 * L2_BYTES
-            if cold:
-                # the triangle could partly stay in the 129 MB L2: before
-                # every call write a 512 MB buffer (evicting everything) and
-                # read another (so that the evicted dirty lines are written
-                # back before the call, not during it).  Nothing synchronises
-                # inside the loop: the host enqueues each call while the
-                # flush runs, so the events time the GPU work only.
-                flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-                clean = torch.zeros(64 << 20, dtype=torch.int64, device="cuda")
-                evs = []
-                for _ in range(20):
-                    flush.fill_(1)
-                    clean.sum()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    call()
-                    e1.record(stream)
-                    evs.append((e0, e1))
-                torch.cuda.synchronize()
-                t = statistics.median(a.elapsed_time(b) for a, b in evs)
-                del flush, clean
-            else:
-                reps = max(10, min(200, int(4e10 / triangle_bytes(m))))
+            # with the L2 flushed before every call: write a 512 MB buffer
+            # (evicting everything) and read another (so that the evicted
+            # dirty lines are written back before the call, not during it).
+            # Nothing synchronises inside the loop: the host enqueues each
+            # call while the flush runs, so the events time the GPU work only.
+            evs = []
+            for _ in range(20):
+                flush.fill_(1)
+                clean.sum()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                for _ in range(reps):
-                    call()
+                call()
                 e1.record(stream)
-                torch.cuda.synchronize()
-                t = e0.elapsed_time(e1) / reps
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            t_cold = statistics.median(a.elapsed_time(b) for a, b in evs)
+            # back to back
+            reps = max(10, min(200, int(4e10 / triangle_bytes(m))))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t_b2b = e0.elapsed_time(e1) / reps
+            # the headline figure of each size: flushed while the triangle
+            # could partly stay in L2 (under 4x its 129 MB), else back to back
+            cold = triangle_bytes(m) < 4 * L2_BYTES
+            t = t_cold if cold else t_b2b
             sweep.append({"n": m, "gflops": flops(m) / (t * 1e-3) / 1e9,
                           "gbs": triangle_bytes(m) / (t * 1e-3) / 1e9,
                           "frac": triangle_bytes(m) / (t * 1e-3) / 1e9 / peak,
                           "l2": "flushed (write 512 MB, read 512 MB) before each call, median of 20"
                           if cold
-                          else "inputs larger than L2, back-to-back calls"})
+                          else "inputs larger than L2, back-to-back calls",
+                          "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
+                          "gbs_back_to_back": triangle_bytes(m) / (t_b2b * 1e-3) / 1e9,
+                          "variant": xs.xsymv_variant_name("s", xs.xsymv_selected_variant("s", "U", m))})
             del pm
+        del flush, clean
         torch.cuda.empty_cache()
         prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
         A, x, y = prob["A"], prob["x"], prob["y"]

@@ -14,16 +14,22 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1940.5 GB/s at n=4096
-    {'s', 1, 12288, 21},   // vr2_u2_r0_w8_b4_g11 4002.7 GB/s at n=8192
-    {'s', 1, 20480, 21},   // vr2_u2_r0_w8_b4_g11 6175.9 GB/s at n=16384
-    {'s', 1, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6529.1 GB/s at n=24576
-    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6741.6 GB/s at n=32768
-    {'s', 0, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1977.1 GB/s at n=4096
-    {'s', 0, 12288, 21},   // vr2_u2_r0_w8_b4_g11 4006.5 GB/s at n=8192
-    {'s', 0, 20480, 22},   // vr2_u2_r0_w8_b4_g13 6190.6 GB/s at n=16384
-    {'s', 0, 28672, 22},   // vr2_u2_r0_w8_b4_g13 6521.8 GB/s at n=24576
-    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6753.9 GB/s at n=32768
+    {'s', 1, 6144, 21},   // vr2_u2_r0_w8_b4_g11 1940.5 GB/s at n=4096
+    {'s', 1, 10240, 22},   // vr2_u2_r0_w8_b4_g13 4029.6 GB/s at n=8192
+    {'s', 1, 14336, 21},   // vr2_u2_r0_w8_b4_g11 5407.0 GB/s at n=12288
+    {'s', 1, 18432, 21},   // vr2_u2_r0_w8_b4_g11 6255.5 GB/s at n=16384
+    {'s', 1, 22528, 22},   // vr2_u2_r0_w8_b4_g13 6468.9 GB/s at n=20480
+    {'s', 1, 26624, 22},   // vr2_u2_r0_w8_b4_g13 6617.2 GB/s at n=24576
+    {'s', 1, 30720, 21},   // vr2_u2_r0_w8_b4_g11 6761.0 GB/s at n=28672
+    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6835.6 GB/s at n=32768
+    {'s', 0, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1982.7 GB/s at n=4096
+    {'s', 0, 10240, 12},   // vr1_u2_r0_w8_b6_g9 4041.2 GB/s at n=8192
+    {'s', 0, 14336, 22},   // vr2_u2_r0_w8_b4_g13 5405.5 GB/s at n=12288
+    {'s', 0, 18432, 22},   // vr2_u2_r0_w8_b4_g13 6261.5 GB/s at n=16384
+    {'s', 0, 22528, 21},   // vr2_u2_r0_w8_b4_g11 6500.1 GB/s at n=20480
+    {'s', 0, 26624, 21},   // vr2_u2_r0_w8_b4_g11 6614.5 GB/s at n=24576
+    {'s', 0, 30720, 21},   // vr2_u2_r0_w8_b4_g11 6790.5 GB/s at n=28672
+    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6831.5 GB/s at n=32768
     {'d', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1817.5 GB/s at n=8192
     {'d', 1, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2120.0 GB/s at n=16384
     {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2170.6 GB/s at n=24576

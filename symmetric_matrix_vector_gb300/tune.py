@@ -25,7 +25,7 @@ import statistics
 
 from . import _build, inputs
 
-DEFAULT_N = {"s": [4096, 8192, 16384, 24576, 32768], "d": [8192, 16384, 24576], "c": [8192, 16384],
+DEFAULT_N = {"s": [4096, 8192, 12288, 16384, 20480, 24576, 28672, 32768], "d": [8192, 16384, 24576], "c": [8192, 16384],
              "z": [8192, 16384], "w": [4096, 8192]}
 TUNED_H = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "xsymv_tuned.h")
 INT_MAX = 2147483647
