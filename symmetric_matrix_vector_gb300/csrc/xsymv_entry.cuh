@@ -21,9 +21,11 @@ constexpr long long kHeaderBytes = 256;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // 2 s
 
 // Partition costs (see xsymv_plan.h): a dense column costs kDenseCost; a
-// diagonal-tile column, read with masked element loads, costs more for the
-// bandwidth-bound types and less for the FP64-bound ones (it holds half a
-// column's elements on average).
+// diagonal-tile column (masked, and stepped one column at a time for the
+// single-precision kinds) costs more for the bandwidth-bound types and less
+// for the FP64-bound ones (it holds half a column's elements on average).
+// These are the defaults of the untuned variants; the tuned ones carry their
+// own cost (_g<G>).
 constexpr int kDenseCost = 4;
 template <class T> struct DiagCost { static constexpr int v = 4; };
 template <> struct DiagCost<float> { static constexpr int v = 6; };

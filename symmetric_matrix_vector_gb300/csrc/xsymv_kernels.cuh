@@ -26,7 +26,8 @@
 //                  arithmetic with a triangle mask: its stored part is read
 //                  once and contributes to both sides, which is what the
 //                  report's mirrored copy in shared memory (part two)
-//                  achieves.
+//                  achieves (on aligned matrices as 16-byte vectors, whose
+//                  few elements across the diagonal are ignored).
 //   symv_finalize  For every output element, sums the workspace slots of its
 //                  row in a fixed order and applies y = alpha*s + beta*y (the
 //                  report's part three and beta scaling).  No atomic
