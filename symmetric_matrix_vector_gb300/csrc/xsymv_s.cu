@@ -32,6 +32,7 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_REG_G(float, 2, 1, 8, 5, 6),
     XSYMV_REG_G(float, 2, 2, 8, 4, 7),
     XSYMV_REG_G(float, 2, 2, 8, 4, 8),
+    XSYMV_REG_G(float, 2, 2, 8, 4, 12),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

@@ -14,32 +14,32 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 6144, 21},   // vr2_u2_r0_w8_b4_g11 1940.5 GB/s at n=4096
-    {'s', 1, 10240, 22},   // vr2_u2_r0_w8_b4_g13 4029.6 GB/s at n=8192
-    {'s', 1, 14336, 21},   // vr2_u2_r0_w8_b4_g11 5407.0 GB/s at n=12288
-    {'s', 1, 18432, 21},   // vr2_u2_r0_w8_b4_g11 6255.5 GB/s at n=16384
-    {'s', 1, 22528, 22},   // vr2_u2_r0_w8_b4_g13 6468.9 GB/s at n=20480
-    {'s', 1, 26624, 22},   // vr2_u2_r0_w8_b4_g13 6617.2 GB/s at n=24576
-    {'s', 1, 30720, 21},   // vr2_u2_r0_w8_b4_g11 6761.0 GB/s at n=28672
-    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6835.6 GB/s at n=32768
-    {'s', 0, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1982.7 GB/s at n=4096
-    {'s', 0, 10240, 12},   // vr1_u2_r0_w8_b6_g9 4041.2 GB/s at n=8192
-    {'s', 0, 14336, 22},   // vr2_u2_r0_w8_b4_g13 5405.5 GB/s at n=12288
-    {'s', 0, 18432, 22},   // vr2_u2_r0_w8_b4_g13 6261.5 GB/s at n=16384
-    {'s', 0, 22528, 21},   // vr2_u2_r0_w8_b4_g11 6500.1 GB/s at n=20480
-    {'s', 0, 26624, 21},   // vr2_u2_r0_w8_b4_g11 6614.5 GB/s at n=24576
-    {'s', 0, 30720, 21},   // vr2_u2_r0_w8_b4_g11 6790.5 GB/s at n=28672
-    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6831.5 GB/s at n=32768
+    {'s', 1, 6144, 13},   // vr1_u2_r0_w8_b6_g11 1978.9 GB/s at n=4096
+    {'s', 1, 10240, 26},   // vr2_u2_r0_w8_b4_g12 4006.5 GB/s at n=8192
+    {'s', 1, 14336, 21},   // vr2_u2_r0_w8_b4_g11 5338.2 GB/s at n=12288
+    {'s', 1, 18432, 21},   // vr2_u2_r0_w8_b4_g11 6161.7 GB/s at n=16384
+    {'s', 1, 22528, 26},   // vr2_u2_r0_w8_b4_g12 6451.4 GB/s at n=20480
+    {'s', 1, 26624, 26},   // vr2_u2_r0_w8_b4_g12 6536.7 GB/s at n=24576
+    {'s', 1, 30720, 21},   // vr2_u2_r0_w8_b4_g11 6697.5 GB/s at n=28672
+    {'s', 1, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6768.2 GB/s at n=32768
+    {'s', 0, 6144, 26},   // vr2_u2_r0_w8_b4_g12 1982.7 GB/s at n=4096
+    {'s', 0, 10240, 22},   // vr2_u2_r0_w8_b4_g13 4029.6 GB/s at n=8192
+    {'s', 0, 14336, 21},   // vr2_u2_r0_w8_b4_g11 5394.7 GB/s at n=12288
+    {'s', 0, 18432, 22},   // vr2_u2_r0_w8_b4_g13 6171.4 GB/s at n=16384
+    {'s', 0, 22528, 21},   // vr2_u2_r0_w8_b4_g11 6437.5 GB/s at n=20480
+    {'s', 0, 26624, 26},   // vr2_u2_r0_w8_b4_g12 6588.4 GB/s at n=24576
+    {'s', 0, 30720, 26},   // vr2_u2_r0_w8_b4_g12 6724.5 GB/s at n=28672
+    {'s', 0, 2147483647, 21},   // vr2_u2_r0_w8_b4_g11 6809.4 GB/s at n=32768
     {'d', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1817.5 GB/s at n=8192
     {'d', 1, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2120.0 GB/s at n=16384
     {'d', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2170.6 GB/s at n=24576
     {'d', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1840.6 GB/s at n=8192
     {'d', 0, 20480, 11},   // vr4_u2_r0_w8_b0_g5_c8 2116.3 GB/s at n=16384
     {'d', 0, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 2175.2 GB/s at n=24576
-    {'c', 1, 12288, 17},   // vr2_u2_r0_w8_b4_g11 5182.0 GB/s at n=8192
-    {'c', 1, 2147483647, 16},   // vr2_u2_r0_w8_b4_g9 6352.0 GB/s at n=16384
-    {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 5182.0 GB/s at n=8192
-    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6527.8 GB/s at n=16384
+    {'c', 1, 12288, 20},   // vr2_u2_r0_w8_b4_g13 5198.0 GB/s at n=8192
+    {'c', 1, 2147483647, 20},   // vr2_u2_r0_w8_b4_g13 6447.7 GB/s at n=16384
+    {'c', 0, 12288, 17},   // vr2_u2_r0_w8_b4_g11 5207.7 GB/s at n=8192
+    {'c', 0, 2147483647, 17},   // vr2_u2_r0_w8_b4_g11 6536.5 GB/s at n=16384
     {'z', 1, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1060.8 GB/s at n=8192
     {'z', 1, 2147483647, 11},   // vr4_u2_r0_w8_b0_g5_c8 1096.4 GB/s at n=16384
     {'z', 0, 12288, 11},   // vr4_u2_r0_w8_b0_g5_c8 1061.0 GB/s at n=8192
