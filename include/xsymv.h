@@ -117,16 +117,20 @@ XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int l
  * a plug-in whose host application owns all device memory and forbids
  * allocating inside the plug-in, or latency-critical code where cudaMalloc /
  * cudaFree would block or synchronise the device.  Same arguments, results
- * and status codes as xsymv_s; it never allocates.  Its workspace is one
- * fixed 16 MiB device array in the library, held on every GPU that loads the
- * library until the process exits; a problem whose workspace does not fit
- * (roughly n > 31000 with the tuned kernels) returns XSYMV_ERR_TOO_LARGE with nothing enqueued.
- * The first call on a device looks up the array's address on that device;
- * make that call before any stream capture.  It also clears the array's
- * 256-byte status header, the only part that must start at zero.  All calls
- * share the array and it keeps the last call's contents: calls that overlap
- * on the GPU, on different streams or from different threads, race on it
- * and corrupt each other's results. */
+ * and status codes as xsymv_s (xsymv_sync_status reports its timeouts too); it
+ * never allocates.  Its workspace is one fixed 16 MiB device array in the
+ * library, held on every GPU that loads the library until the process exits;
+ * a problem whose workspace does not fit (roughly n > 31000 with the tuned
+ * kernels) returns XSYMV_ERR_TOO_LARGE with nothing enqueued and y untouched.
+ * The first call with alpha != 0 on a device looks up the array's address
+ * on that device; make that call before any stream capture.  It also clears
+ * the array's 256-byte status header, the only part that must start at zero.
+ * All calls share the array and it keeps the last call's contents (the
+ * plan's tables among them): calls that overlap on the GPU, on different
+ * streams or from different threads, race on it and corrupt each other's
+ * results.  Each call must start on the GPU only after everything the
+ * previous call enqueued has finished (calls on one stream are; across
+ * streams, wait on an event recorded after the previous call). */
 XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float *A, int lda,
                               const float *x, int incx, float beta, float *y, int incy);
 
@@ -173,7 +177,9 @@ XSYMV_API void *xsymv_get_stream(void);
  * completed keep their results).
  * xsymv_sync_status waits for the current stream and returns
  * XSYMV_ERR_TIMEOUT if the latest call on it (device, stream) failed that
- * way, else 0 (or XSYMV_ERR_CUDA). */
+ * way, else 0 (or XSYMV_ERR_CUDA).  That covers every SYMV entry point,
+ * xsymv_s_noalloc included; a call with nothing that waits (alpha = 0, the
+ * general product) reports 0. */
 XSYMV_API int xsymv_sync_status(void);
 /* Time limit of those waits in ns (0: back to 2 s). */
 XSYMV_API int xsymv_set_wait_limit(unsigned long long ns);
@@ -185,8 +191,10 @@ XSYMV_API int xsymv_test_stall(int on);
 /* Test hook: sets the last call number handed out on the current device and
  * stream (calls number themselves 1, 2, ... to tag failures in the status
  * word; after 0x7ffffffe they start again at 1 and the status word is
- * cleared).  0 <= number <= 0x7ffffffe, and the stream must have a
- * workspace (one earlier call); else XSYMV_ERR_VALUE, nothing changed. */
+ * cleared), and that of xsymv_s_noalloc on the current device.
+ * 0 <= number <= 0x7ffffffe, and the stream must have a workspace or the
+ * device an xsymv_s_noalloc call (one earlier call); else XSYMV_ERR_VALUE,
+ * nothing changed. */
 XSYMV_API int xsymv_test_set_call_number(int number);
 
 /* Human-readable text for a status code (static storage). */

@@ -71,6 +71,15 @@ cudaEvent_t take_event() {
 
 cudaStream_t current_stream() { return g_stream.load(); }
 
+int current_device_index() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
 void record_cuda_error(cudaError_t e) {
   if (e != cudaSuccess) g_last_error.store((int)e);
 }
@@ -173,6 +182,32 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
     *epoch = ++w->epoch;
   }
   return w->ptr;
+}
+
+namespace {
+struct CallStatus {
+  int device;
+  cudaStream_t stream;
+  const int* status;   // nullptr: the latest call has no status word
+  int epoch;
+};
+std::vector<CallStatus> g_call_status;
+}  // namespace
+
+void note_call_status(cudaStream_t stream, const int* status, int epoch) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (CallStatus& c : g_call_status)
+    if (c.device == d && c.stream == stream) {
+      c.status = status;
+      c.epoch = epoch;
+      return;
+    }
+  g_call_status.push_back(CallStatus{d, stream, status, epoch});
 }
 
 namespace {
@@ -426,14 +461,14 @@ XSYMV_API int xsymv_sync_status(void) {
     record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  void* ptr = nullptr;
+  const int* ptr = nullptr;
   int epoch = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    for (WsEntry& w : g_ws)
-      if (w.device == d && w.stream == s && w.slot == 0) {
-        ptr = w.ptr;
-        epoch = w.epoch;
+    for (const CallStatus& c : g_call_status)
+      if (c.device == d && c.stream == s) {
+        ptr = c.status;
+        epoch = c.epoch;
       }
   }
   if (ptr == nullptr || epoch == 0) return XSYMV_OK;
@@ -465,13 +500,14 @@ XSYMV_API int xsymv_test_set_call_number(int number) {
     return XSYMV_ERR_CUDA;
   }
   const cudaStream_t s = g_stream.load();
+  bool found = noalloc_set_call_number(number);
   std::lock_guard<std::mutex> lk(g_mu);
   for (WsEntry& w : g_ws)
     if (w.device == d && w.stream == s && w.slot == 0 && w.ptr != nullptr) {
       w.epoch = number;
-      return XSYMV_OK;
+      found = true;
     }
-  return XSYMV_ERR_VALUE;
+  return found ? XSYMV_OK : XSYMV_ERR_VALUE;
 }
 
 XSYMV_API int xsymv_host_traffic(long long* h2d_bytes, long long* d2h_bytes) {

@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "../../include/xsymv.h"
 #include "xsymv_kernels.cuh"
 #include "xsymv_ticket.cuh"
@@ -84,14 +86,16 @@ constexpr int ring_smem_bytes() {
 template <class T, int VR, int U, int S, int P, int WARPS, int MB, int R = U>
 cudaError_t launch_main(const MainArgs<T>& a) {
   constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
-  static bool configured = false;
-  if (!configured) {
-    if (smem > 48 * 1024) {
+  if (smem > 48 * 1024) {
+    // the attribute is per device: set once on each device this kernel runs on
+    static std::atomic<int> configured[kMaxDevices];
+    const int dev = current_device_index();
+    if (dev < 0 || !configured[dev].load(std::memory_order_relaxed)) {
       cudaError_t e = cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
+      if (dev >= 0) configured[dev].store(1, std::memory_order_relaxed);
     }
-    configured = true;
   }
   const unsigned long long limit = wait_limit_ns();
   const uint32_t extra = test_extra_tx();
@@ -117,23 +121,37 @@ cudaError_t launch_main(const MainArgs<T>& a) {
                             extra);
 }
 
+// resident blocks per SM of one kernel on the current device, computed once
+// per device by `count` (a result < 1 counts as 1)
+template <class F>
+int per_device_count(std::atomic<int> (&cache)[kMaxDevices], F count) {
+  const int dev = current_device_index();
+  int b = dev >= 0 ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (b == 0) {
+    b = count();
+    if (b < 1) {
+      cudaGetLastError();
+      b = 1;
+    }
+    if (dev >= 0) cache[dev].store(b, std::memory_order_relaxed);
+  }
+  return b;
+}
+
 template <class T, int VR, int U, int S, int P, int WARPS, int MB, int R = U>
 int ctas_per_sm() {
-  static int cached = 0;
-  if (!cached) {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device_count(cache, [] {
     constexpr int smem = ring_smem_bytes<T, VR, U, S, P, WARPS>();
     int b = 0;
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_main<T, VR, U, S, P, WARPS, true, MB, R>,
-                                                      WARPS * 32, smem) != cudaSuccess || b < 1) {
-      cudaGetLastError();
-      b = 1;
-    }
-    cached = b;
-  }
-  return cached;
+                                                      WARPS * 32, smem) != cudaSuccess)
+      b = 0;
+    return b;
+  });
 }
 
 // The ordered-ticket kernel (register path): one launch streams the triangle,
@@ -169,17 +187,14 @@ cudaError_t launch_ticket(const MainArgs<T>& a) {
 
 template <class T, int VR, int U, int WARPS, int MB, int R>
 int ctas_per_sm_ticket() {
-  static int cached = 0;
-  if (!cached) {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device_count(cache, [] {
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_ticket<T, VR, U, WARPS, true, MB, R>,
-                                                      WARPS * 32, 0) != cudaSuccess || b < 1) {
-      cudaGetLastError();
-      b = 1;
-    }
-    cached = b;
-  }
-  return cached;
+                                                      WARPS * 32, 0) != cudaSuccess)
+      b = 0;
+    return b;
+  });
 }
 
 // Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>][_tk],
@@ -323,12 +338,28 @@ struct Workload {
   long long bytes;      // total workspace bytes
 };
 
+// The variant a call uses: the forced one, else the tuned entry's variant,
+// looked up by name in this kind's table (once per entry, then cached); 0 if
+// the tuned table names no compiled variant.
 template <class T>
 int pick_variant(const Variant<T>* table, int count, char kind, int upper, int n) {
   int f = forced_variant(kind);
   if (f >= 0 && f < count) return f;
-  int t = tuned_variant(kind, upper, n);
-  return (t >= 0 && t < count) ? t : 0;
+  const int e = tuned_entry(kind, upper, n);
+  if (e < 0) return 0;
+  // resolved[e] = variant index + 1 (0: not looked up yet)
+  static std::atomic<int> resolved[kTunedCount];
+  int r = resolved[e].load(std::memory_order_relaxed);
+  if (r == 0) {
+    r = 1;   // variant 0 unless the name is found
+    for (int i = 0; i < count; ++i)
+      if (strcmp(table[i].name, kTuned[e].variant) == 0) {
+        r = i + 1;
+        break;
+      }
+    resolved[e].store(r, std::memory_order_relaxed);
+  }
+  return r - 1;
 }
 
 template <class T>
@@ -380,6 +411,7 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
       return XSYMV_ERR_CUDA;
     }
     note_launches(1);
+    note_call_status(st, nullptr, 0);
     return XSYMV_OK;
   }
 
@@ -416,6 +448,7 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
       return XSYMV_ERR_CUDA;
     }
     note_launches(1);
+    note_call_status(st, m.status, epoch);
     return XSYMV_OK;
   }
   timing_begin(st);
@@ -431,6 +464,7 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     return XSYMV_ERR_CUDA;
   }
   note_launches(2);
+  note_call_status(st, m.status, epoch);
   return XSYMV_OK;
 }
 

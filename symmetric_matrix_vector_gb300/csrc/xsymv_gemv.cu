@@ -44,17 +44,14 @@ cudaError_t launch_gemv(const GemvArgs<T>& a) {
 
 template <class T, int VR, int U, int WARPS, int MB>
 int gemv_ctas_per_sm() {
-  static int cached = 0;
-  if (!cached) {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device_count(cache, [] {
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gemv_main<T, VR, U, WARPS, true, MB>,
-                                                      WARPS * 32, 0) != cudaSuccess || b < 1) {
-      cudaGetLastError();
-      b = 1;
-    }
-    cached = b;
-  }
-  return cached;
+                                                      WARPS * 32, 0) != cudaSuccess)
+      b = 0;
+    return b;
+  });
 }
 
 // names: vr<VR>_u<U>_r0_w<WARPS>[_b<MINB>], as for the SYMV register path
@@ -137,6 +134,7 @@ int gemv_entry(const GemvVariant<T>* table, int count, int tindex, int n, T alph
       return XSYMV_ERR_CUDA;
     }
     note_launches(1);
+    note_call_status(st, nullptr, 0);
     return XSYMV_OK;
   }
 
@@ -164,6 +162,7 @@ int gemv_entry(const GemvVariant<T>* table, int count, int tindex, int n, T alph
     return XSYMV_ERR_CUDA;
   }
   note_launches(2);
+  note_call_status(st, nullptr, 0);   // nothing in the general product waits
   return XSYMV_OK;
 }
 

@@ -105,19 +105,25 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return r;
 }
 
-// Wait for phase `parity` of the mbarrier, giving up after about limit_ns.
-// The limit is counted in SM clock cycles (at most 2 per ns, i.e. a clock of
-// up to 2 GHz; a slower clock only lengthens the wait), read every 256 tries.
+// The GPU's global nanosecond timer (%globaltimer): the same time base on
+// every SM, independent of the SM clock.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of the mbarrier, giving up once limit_ns have
+// passed on the global timer (read every 256 tries).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  const long long limit = (long long)(limit_ns < (1ull << 61) ? limit_ns : (1ull << 61)) * 2;
+  const unsigned long long t0 = global_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > limit) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

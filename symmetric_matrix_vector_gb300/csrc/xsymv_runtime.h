@@ -11,6 +11,13 @@ namespace xsymv {
 
 cudaStream_t current_stream();
 
+// Kernel attributes and occupancy belong to a device, and one process may
+// drive several GPUs: the kernels' per-device caches have kMaxDevices slots,
+// indexed by current_device_index() (-1 on a CUDA error or a device number
+// beyond the slots; such calls compute afresh every time).
+constexpr int kMaxDevices = 64;
+int current_device_index();
+
 // current device and its multiprocessor count; false if there is no usable
 // device (records the CUDA error)
 bool current_device(int* dev, int* sm_count);
@@ -22,6 +29,17 @@ bool current_device(int* dev, int* sm_count);
 // buffer is allocated, and *epoch receives a fresh call number (> 0) that the
 // kernels write to the status word if they give up on a wait.
 void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch);
+
+// Record where the latest call on (current device, stream) keeps its
+// status word and the call number its kernels write there if a bounded wait
+// runs out; xsymv_sync_status reads it.  status == nullptr: the call has no
+// status word (it launched no kernel that waits).
+void note_call_status(cudaStream_t stream, const int* status, int epoch);
+
+// Set the last call number of the allocation-free entry point on the current
+// device (defined beside it); false if that entry point has not been called
+// on this device yet.
+bool noalloc_set_call_number(int number);
 
 // buffer of at least `bytes` for the ordered-ticket kernels on (current
 // device, stream): zeroed when it is allocated, written by nothing but those

@@ -79,19 +79,21 @@ extern "C" XSYMV_API int xsymv_s_host(char uplo, int n, float alpha, const float
 //   this library, until the process exits.  Problems whose workspace does
 //   not fit (roughly n > 31000 with the tuned kernels on GB300) are
 //   rejected with XSYMV_ERR_TOO_LARGE before anything is enqueued.
-// * The first call on a device looks up the array's device address
-//   (cudaGetSymbolAddress, with that device current) and caches it; make
-//   that first call before any stream capture.
+// * The first call on a device that needs the array (alpha != 0) looks up
+//   its device address (cudaGetSymbolAddress, with that device current) and
+//   caches it; make that first call before any stream capture.
 // * Only the array's first 256 bytes (a status word the kernels set if a
-//   bounded wait runs out) must start at zero; the first call on a device
-//   clears them with cudaMemsetAsync on its stream.  Every other workspace
-//   slot the finaliser reads is written by the main kernel of the same
-//   call.  The array keeps the last call's contents, among them the plan's
-//   warp and row tables: a call rebuilds them (one extra small launch) only
-//   when its plan differs from the previous call's on the device.
+//   bounded wait runs out) must start at zero; that first call clears them
+//   with cudaMemsetAsync on its stream.  Every other workspace slot the
+//   finaliser reads is written by the main kernel of the same call.  The
+//   array keeps the last call's contents, among them the plan's warp and
+//   row tables: a call rebuilds them (one extra small launch) only when its
+//   plan differs from the previous call's on the device.
 // * All calls share the one array: calls that overlap on the GPU (on
 //   different streams, or from different host threads) race and corrupt
-//   each other's results.  Order them, e.g. on one stream.
+//   each other's results.  Order them: each call must start on the GPU only
+//   after everything the previous call enqueued has finished (one stream
+//   does that; with several, an event recorded after the previous call).
 static constexpr long long kNoallocScratchBytes = 16ll << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -151,6 +153,25 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream, size_t* dev_ind
 }
 }  // namespace
 
+namespace xsymv {
+// test hook (xsymv_test_set_call_number): the last call number handed out on
+// the current device
+bool noalloc_set_call_number(int number) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  for (NoallocDevice& s : g_noalloc_devices)
+    if (s.device == d) {
+      s.epoch = number;
+      return true;
+    }
+  return false;
+}
+}  // namespace xsymv
+
 extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float* A, int lda,
                                          const float* x, int incx, float beta, float* y,
                                          int incy) {
@@ -165,11 +186,6 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   cudaStream_t st = current_stream();
   float* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
   const float* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
-  void* scratch = nullptr;
-  int epoch = 0;
-  size_t dev_index = 0;
-  int status = noalloc_scratch(&scratch, &epoch, st, &dev_index);
-  if (status) return status;
 
   if (az) {  // y := beta*y, no workspace needed
     Plan p = plan_make(n, 32, upper, 1);
@@ -180,18 +196,26 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
       return XSYMV_ERR_CUDA;
     }
     note_launches(1);
+    note_call_status(st, nullptr, 0);
     return XSYMV_OK;
   }
 
+  // plan and size check first: a refused call enqueues nothing
   const int count = (int)(sizeof(kVariants_s) / sizeof(kVariants_s[0]));
   Workload<float> wl;
-  status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
+  int status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
   if (status) return status;
   // the ordered-ticket kernels keep state in a second, allocated buffer
   if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;
   // the plan's tables follow the workspace in the same array
   const long long tab_off = align_up(wl.bytes, 256);
   if (tab_off + tables_bytes(wl.plan) > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
+
+  void* scratch = nullptr;
+  int epoch = 0;
+  size_t dev_index = 0;
+  status = noalloc_scratch(&scratch, &epoch, st, &dev_index);
+  if (status) return status;
   char* ws = static_cast<char*>(scratch);
   MainArgs<float> m{wl.plan, A, lda, x0, incx, reinterpret_cast<float*>(ws + wl.wc_off),
                     reinterpret_cast<float*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
@@ -220,5 +244,6 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
     return XSYMV_ERR_CUDA;
   }
   note_launches(launches);
+  note_call_status(st, m.status, epoch);
   return XSYMV_OK;
 }

@@ -290,8 +290,6 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
                                              int lane) {
   constexpr int M = NB / 32;
   const unsigned long long mine = (c.call << kTkIdBits) | (unsigned)gid;
-  const long long limit =
-      (long long)(c.limit_ns < (1ull << 61) ? c.limit_ns : (1ull << 61)) * 2;   // <= 2 GHz
   int cur = -1;   // the group's chunks <= cur have been dealt
 #pragma unroll 1
   for (;;) {
@@ -324,7 +322,7 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
       next = plan_group_next(p, ck, gid, G);
       ready = first == gid;
     }
-    long long t0 = clock64();
+    unsigned long long t0 = global_ns();
     int spins = 0;
     bool failed = false;
     while (__any_sync(0xffffffffu, pending)) {
@@ -341,13 +339,13 @@ __device__ __forceinline__ void ticket_phase(const Plan& p, const TicketCtx<T>& 
         __syncwarp();   // lane k's acquire orders the other lanes' reads of v
         chunk_link<T, M>(p, c, g, K, f, nx, lane);
         if (lane == k) pending = false;
-        t0 = clock64();
+        t0 = global_ns();
         spins = 0;
         continue;
       }
       __nanosleep(32);
       if ((++spins & 63) == 0) {
-        const bool out = clock64() - t0 > limit || ld_relaxed_int(c.status) == c.epoch;
+        const bool out = global_ns() - t0 > c.limit_ns || ld_relaxed_int(c.status) == c.epoch;
         if (__any_sync(0xffffffffu, out)) {
           failed = true;
           break;

@@ -13,7 +13,7 @@ Results are appended to a JSONL file (one line per measurement) and reused on
 a rerun, so an interrupted sweep resumes where it stopped.
 
     python -m symmetric_matrix_vector_gb300.tune --kinds s --n 8192,16384,32768 \\
-        --results gpurun_out/tune.jsonl --write-header csrc_copy.h
+        --results /tmp/tune.jsonl --write-header /tmp/xsymv_tuned.h
 """
 from __future__ import annotations
 
@@ -167,11 +167,11 @@ def render_table(entries, kinds_all="sdczw"):
     have = set()
     for kind, upper, n_max, r in entries:
         have.add(kind)
-        lines.append("    {'%s', %d, %d, %d},   // %s %.1f GB/s at n=%d" % (
-            kind, upper, n_max, r["variant"], r["variant_name"], r["gbs"], r["n"]))
+        lines.append("    {'%s', %d, %d, \"%s\"},   // %.1f GB/s at n=%d" % (
+            kind, upper, n_max, r["variant_name"], r["gbs"], r["n"]))
     for kind in kinds_all:
         if kind not in have:
-            lines.append("    {'%s', -1, %d, 0}," % (kind, INT_MAX))
+            lines.append("    {'%s', -1, %d, \"\"},   // not tuned: variant 0" % (kind, INT_MAX))
     lines.append("};")
     return "\n".join(lines)
 

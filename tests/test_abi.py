@@ -128,3 +128,28 @@ def test_gemv_variants_introspection(lib):
         assert xs.xgemv_set_variant(kind, -1) == 0 and xs.xgemv_selected_variant(kind) == 0
     assert xs.xgemv_variant_count("c") == -4
     assert xs.xgemv_variant_name("c", 0) is None
+
+
+def tuned_entries():
+    """(kind, upper, n_max, variant name) of every row of the tuned table"""
+    src = open(os.path.join(ROOT, "symmetric_matrix_vector_gb300", "csrc", "xsymv_tuned.h")).read()
+    body = src.split("// BEGIN TUNED TABLE", 1)[1].split("// END TUNED TABLE", 1)[0]
+    return [(k, int(u), int(nmax), name) for k, u, nmax, name in
+            re.findall(r"\{'(\w)', (-?\d+), (\d+), \"([^\"]*)\"\}", body)]
+
+
+def test_tuned_table_names_compiled_variants(lib):
+    """Every row of the tuned table names a variant compiled for its kind,
+    and the library resolves a call of that row's largest size to exactly
+    that variant (rows are looked up by name, not by position)."""
+    rows = tuned_entries()
+    assert len(rows) >= 5
+    for kind, upper, n_max, name in rows:
+        compiled = [xs.xsymv_variant_name(kind, i) for i in range(xs.xsymv_variant_count(kind))]
+        if not name:          # an untuned kind: variant 0
+            continue
+        assert name in compiled, (kind, name)
+        for uplo in (("U", "L") if upper < 0 else (("U",) if upper else ("L",))):
+            n = min(n_max, 1 << 20)
+            got = xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))
+            assert got == name, (kind, uplo, n, name, got)

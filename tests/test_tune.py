@@ -33,6 +33,6 @@ def test_choose_maps_names_to_current_indices():
 def test_render_table_fills_missing_kinds():
     done = {("z", "U", 16384, "x"): rec("z", "U", 16384, 3, "x", 1.0)}
     text = tune.render_table(tune.choose(done))
-    assert "{'z', 1, %d, 3}" % tune.INT_MAX in text
+    assert "{'z', 1, %d, \"x\"}" % tune.INT_MAX in text
     for k in "sdcw":
-        assert "{'%s', -1, %d, 0}," % (k, tune.INT_MAX) in text
+        assert "{'%s', -1, %d, \"\"}," % (k, tune.INT_MAX) in text
