@@ -12,13 +12,21 @@ Prints one JSON line: GFLOP/s (2 n^2 flops per call) over the timed steps,
 the main kernel's achieved HBM bandwidth against the measured copy bandwidth
 (roofline), the end-to-end rate through the host-buffer entry point with the
 host<->device copies inside the timed region, SM clocks sampled during the
-timed region, the number of kernels launched, and the CPU oracle timed on a
-bounded sample (cpu_baseline).  ``--impl reference`` times the CPU oracle
-alone on a sample of the same workload.
+timed region (and, so that short runs get samples too, while the same steps
+continue for at least a second after it), the number of kernels launched,
+and the CPU oracle timed on a bounded sample of the same workload's data
+(cpu_baseline).  Beside the headline: the size sweep (n = 4096 .. 32768),
+small sizes (n = 512 .. 4096, the n = 1024 lower-triangle workload among
+them), the other kinds, SYMV against GEMV, tickets against the workspace
+reduction, and the block-column split run shard by shard on the one GPU.
+``--impl reference`` times the CPU oracle alone on the same workload.
 
-Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
-the problem (the call does not shard); ``value`` is the total over ranks
-divided by the slowest rank's time.
+Multi-GPU (torchrun, one rank per GPU): the call is split by block columns
+(each rank streams its panel of the stored triangle into a partial vector;
+the partial vectors are all-gathered and added in rank order), a strong-
+scaling workload: ``value`` is the one problem's flops per step over the
+slowest rank's time.  ``--replicas`` runs one independent copy per rank
+instead (weak scaling).
 """
 from __future__ import annotations
 
@@ -65,6 +73,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--variant", default="",
                     help="time this compiled SSYMV variant (by name) instead of the tuned choice")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with several ranks: independent replicas instead of the block-column split")
+    ap.add_argument("--no-shards", action="store_true",
+                    help="skip the block-column split run shard by shard on one GPU")
+    ap.add_argument("--no-small", action="store_true", help="skip the small sizes n = 512 .. 4096")
     return ap.parse_args()
 
 
@@ -76,10 +89,16 @@ def triangle_bytes(n: int, es: int = 4) -> float:
     return n * (n + 1) / 2.0 * es
 
 
-def workload_config(n: int) -> dict:
-    return {"workload": "ssymv n=%d uplo=U lda=n+32 alpha=1 beta=0 U(-1,1) seed=%d" % (n, n),
-            "kernel_variant": None, "l2": "inputs larger than L2 (triangle %.2f GB vs 129 MB L2), "
-            "no flush" % (triangle_bytes(n) / 1e9)}
+def workload_config(n: int, world: int = 1, replicas: bool = False) -> dict:
+    """The workload, the same in both arms (kernel variant and samples are
+    reported beside it, not in it)."""
+    cfg = {"workload": "ssymv n=%d uplo=U lda=n+32 alpha=1 beta=0 U(-1,1) seed=%d" % (n, n),
+           "l2": "inputs larger than L2 (triangle %.2f GB vs 129 MB L2), "
+           "no flush" % (triangle_bytes(n) / 1e9)}
+    if world > 1:
+        cfg["parallelism"] = ("replicas x%d" % world if replicas
+                              else "block-column split x%d (rank-order reduction)" % world)
+    return cfg
 
 
 # ----------------------------------------------------------------- helpers --
@@ -131,7 +150,7 @@ def recorded_traffic(n: int, variant: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -147,7 +166,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -410,27 +429,50 @@ def dist_info():
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def cpu_oracle_rate(n: int, seconds: float):
-    """Run the CPU oracle's SSYMV on an n-by-n instance of the workload's
-    recipe until ``seconds`` have passed; returns (GFLOP/s, calls, seconds)."""
-    import oracle
-    from symmetric_matrix_vector_gb300 import inputs
+def oracle_block_call(o, A, lda, x, y, ns):
+    """One oracle SSYMV (the report's three-part algorithm, binary64
+    accumulator) on the leading ns-by-ns principal block of the workload's
+    matrix: the same array, lda and vectors (a principal block of a
+    symmetric matrix is itself the stored triangle of one)."""
+    info, _, _, _ = o.symv("s", "U", ns, 1.0, A[:ns], lda, x, 1, 0.0, y, 1)
+    assert info == 0
 
-    p = inputs.workload("ssymv_sweep", n=n)
+
+def oracle_block_size(o, A, lda, x, y, n, seconds_per_call):
+    """the largest leading block (a multiple of 256, at most n) one oracle
+    call finishes in about seconds_per_call, from a timed call on n=1024"""
+    m = min(n, 1024)
+    t0 = time.perf_counter()
+    oracle_block_call(o, A, lda, x, y, m)
+    rate = flops(m) / max(time.perf_counter() - t0, 1e-6)
+    ns = int((seconds_per_call * rate / 2.0) ** 0.5)
+    return n if ns >= n else max(256, ns // 256 * 256)
+
+
+def cpu_oracle_rate(A, lda, x, y, n, seconds):
+    """The CPU oracle on the workload's own data (host arrays), single-
+    threaded, repeated until ``seconds`` have passed: each call on the whole
+    matrix, or on its leading principal block if one call would take more
+    than a third of the time.  Returns (GFLOP/s, calls, seconds, block)."""
+    import oracle
+
     o = oracle.get()
+    ns = oracle_block_size(o, A, lda, x, y, n, seconds / 3.0)
     calls, t0 = 0, time.perf_counter()
     while True:
-        info, _, _, _ = o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
-        assert info == 0
+        oracle_block_call(o, A, lda, x, y, ns)
         calls += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return flops(n) * calls / el / 1e9, calls, el
+    return flops(ns) * calls / el / 1e9, calls, el, ns
 
 
 def run_reference(args):
-    """The CPU oracle, timed step by step on a sample of the workload."""
+    """The CPU oracle, timed step by step on the benchmark's workload: one
+    step = one oracle call on the whole n=32768 matrix (host recipe of the
+    same workload), or on its leading principal block when K + W whole calls
+    would not end within about 90 s."""
     world, rank, _ = dist_info()
     if rank != 0:
         return
@@ -438,30 +480,31 @@ def run_reference(args):
     from symmetric_matrix_vector_gb300 import inputs
 
     o = oracle.get()
-    # size the per-step sample so the whole run stays within ~90 s
-    budget = 90.0 / max(1, args.steps + args.warmup)
-    p0 = inputs.workload("ssymv_sweep", n=1024)
-    t0 = time.perf_counter()
-    o.symv("s", p0.uplo, p0.n, p0.alpha, p0.A, p0.lda, p0.x, 1, p0.beta, p0.y, 1)
-    rate = flops(1024) / max(time.perf_counter() - t0, 1e-6)
-    ns = int((budget * rate / 2.0) ** 0.5) // 256 * 256
-    ns = max(256, min(ns, 8192))
-    p = inputs.workload("ssymv_sweep", n=ns)
+    n = args.n
+    t_gen = time.perf_counter()
+    p = inputs.workload("ssymv_sweep", n=n)
+    t_gen = time.perf_counter() - t_gen
+    ns = oracle_block_size(o, p.A, p.lda, p.x, p.y, n, 90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+        oracle_block_call(o, p.A, p.lda, p.x, p.y, ns)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        o.symv("s", p.uplo, p.n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+        oracle_block_call(o, p.A, p.lda, p.x, p.y, ns)
     el = time.perf_counter() - t0
     value = flops(ns) * args.steps / el / 1e9
-    sample = ("each step: the oracle's three-part SSYMV (binary64 accumulator) on n=%d of the "
-              "same recipe (uplo=U, lda=n+32, alpha=1, beta=0), single-threaded" % ns)
+    what = ("the whole matrix" if ns == n else
+            "its leading %d-by-%d principal block (a bounded sample)" % (ns, ns))
+    sample = ("each step: the oracle's three-part SSYMV (binary64 accumulator), single-threaded, "
+              "on %s of the workload's matrix (host recipe: numpy PCG64, seed n; generated in "
+              "%.1f s before the timed steps)" % (what, t_gen))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "strong" if (world > 1 and not args.replicas) else "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(args.n),
+        "config": workload_config(n, world, args.replicas),
+        "sample_n": ns,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -470,6 +513,285 @@ def run_reference(args):
 
 
 # -------------------------------------------------------------- our arm ----
+
+def l2_flush_buffers(torch):
+    """a 512 MB buffer to write and a 512 MB one to read: evicts the L2 and
+    has the evicted dirty lines written back before the next timed call"""
+    return (torch.empty(512 << 20, dtype=torch.uint8, device="cuda"),
+            torch.zeros(64 << 20, dtype=torch.int64, device="cuda"))
+
+
+def time_flushed(torch, stream, fn, flush, reps=20):
+    """median ms of fn() with the L2 flushed before each call (nothing
+    synchronises inside the loop, so the events time the GPU work only)"""
+    evs = []
+    for _ in range(reps):
+        flush[0].fill_(1)
+        flush[1].sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def time_back_to_back(torch, stream, fn, reps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_sweep(xs, inputs, torch, stream, peak, flush):
+    """The workload's size sweep n = 4096 .. 32768 step 4096, each size
+    timed with the L2 flushed and back to back."""
+    sweep = []
+    for m in range(4096, 32768 + 1, 4096):
+        pm = inputs.device_problem("s", "U", m, lda=m + 32, alpha=1.0, beta=0.0, seed=m)
+
+        def call():
+            xs.check(xs.xsymv_s("U", m, 1.0, pm["A"], m + 32, pm["x"], 1, 0.0, pm["y"], 1))
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        t_cold = time_flushed(torch, stream, call, flush)
+        t_b2b = time_back_to_back(torch, stream, call, max(10, min(200, int(4e10 / triangle_bytes(m)))))
+        # the headline figure of each size: flushed while the triangle
+        # could partly stay in L2 (under 4x its 129 MB), else back to back
+        cold = triangle_bytes(m) < 4 * L2_BYTES
+        t = t_cold if cold else t_b2b
+        sweep.append({"n": m, "gflops": flops(m) / (t * 1e-3) / 1e9,
+                      "gbs": triangle_bytes(m) / (t * 1e-3) / 1e9,
+                      "frac": triangle_bytes(m) / (t * 1e-3) / 1e9 / peak,
+                      "l2": "flushed (write 512 MB, read 512 MB) before each call, median of 20"
+                      if cold else "inputs larger than L2, back-to-back calls",
+                      "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
+                      "gbs_back_to_back": triangle_bytes(m) / (t_b2b * 1e-3) / 1e9,
+                      "variant": xs.xsymv_variant_name("s", xs.xsymv_selected_variant("s", "U", m))})
+        del pm
+    torch.cuda.empty_cache()
+    return sweep
+
+
+def measure_small(xs, inputs, torch, stream, peak, flush):
+    """Small sizes, whose triangle fits the L2 (n <= 4096: at most 34 MB):
+    the n = 1024 lower-triangle workload (lda = n, alpha = 1.25, beta = 0.5)
+    and upper triangles n = 512 .. 4096 (lda = n + 32), each call's time
+    with the L2 flushed before it (median of 20) and back to back."""
+    cases = [("ssymv n=1024 uplo=L lda=n alpha=1.25 beta=0.5 seed=0", "L", 1024, 1024, 1.25, 0.5, 0)]
+    cases += [("ssymv n=%d uplo=U lda=n+32 alpha=1 beta=0 seed=%d" % (m, m), "U", m, m + 32, 1.0,
+               0.0, m) for m in (512, 1024, 2048, 3072, 4096)]
+    out = []
+    for name, uplo, m, lda, al, be, seed in cases:
+        pm = inputs.device_problem("s", uplo, m, lda=lda, alpha=al, beta=be, seed=seed)
+
+        def call():
+            xs.check(xs.xsymv_s(uplo, m, al, pm["A"], lda, pm["x"], 1, be, pm["y"], 1))
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        t_cold = time_flushed(torch, stream, call, flush)
+        t_b2b = time_back_to_back(torch, stream, call, 200)
+        out.append({"workload": name, "n": m, "uplo": uplo,
+                    "us_l2_flushed": t_cold * 1e3, "us_back_to_back": t_b2b * 1e3,
+                    "gflops_l2_flushed": flops(m) / (t_cold * 1e-3) / 1e9,
+                    "gflops_back_to_back": flops(m) / (t_b2b * 1e-3) / 1e9,
+                    "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
+                    "gbs_back_to_back": triangle_bytes(m) / (t_b2b * 1e-3) / 1e9,
+                    "frac_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9 / peak,
+                    "variant": xs.xsymv_variant_name("s", xs.xsymv_selected_variant("s", uplo, m))})
+        del pm
+    torch.cuda.empty_cache()
+    return out
+
+
+def panel_elements(uplo, n, c0, c1):
+    """stored elements of the columns c0 .. c1-1"""
+    if uplo == "U":
+        return (c1 * (c1 + 1) - c0 * (c0 + 1)) // 2
+    return (c1 - c0) * n - (c1 * (c1 - 1) - c0 * (c0 - 1)) // 2
+
+
+def measure_shards_one_gpu(xs, inputs, torch, stream, n, peak, flush):
+    """The block-column split of the headline workload run on this one GPU,
+    shard after shard (each panel in its own allocation, as on its own GPU):
+    each shard call's time with the L2 flushed before it, and the rank-order
+    reduction of the N partial vectors.  A rank's step would be its shard,
+    an all-gather of N vectors of n elements, and the reduction; the slowest
+    shard plus the reduction is that step without the all-gather."""
+    from symmetric_matrix_vector_gb300 import sharded
+
+    prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
+    A, x = prob["A"], prob["x"]
+    y = torch.empty_like(prob["y"])
+    out = []
+    for N in (2, 4, 8):
+        panels = sharded.split("U", n, N)
+        parts = torch.empty((N, n), dtype=torch.float32, device="cuda")
+        shards = []
+        for r, (c0, c1) in enumerate(panels):
+            panel, ldp = sharded.extract_panel(torch, A, "s", "U", n, n + 32, c0, c1)
+
+            def call(panel=panel, ldp=ldp, c0=c0, c1=c1, r=r):
+                xs.check(xs.xsymv_s_shard("U", n, c0, c1, panel, ldp, x, 1, parts[r]))
+
+            for _ in range(3):
+                call()
+            ms = time_flushed(torch, stream, call, flush, reps=10)
+            el = panel_elements("U", n, c0, c1)
+            shards.append({"cols": [c0, c1], "ms": ms, "gbs": el * 4 / (ms * 1e-3) / 1e9,
+                           "variant": xs.xsymv_variant_name(
+                               "s", xs.xsymv_selected_variant("s", "U", int((2 * el) ** 0.5)))})
+            del panel
+        red = time_flushed(torch, stream,
+                           lambda: xs.check(xs.xsymv_s_reduce(n, N, 1.0, parts, n, 0.0, y, 1)),
+                           flush, reps=10)
+        worst = max(sh["ms"] for sh in shards)
+        out.append({"ranks": N, "shards": shards, "max_shard_ms": worst, "reduce_ms": red,
+                    "step_ms_without_gather": worst + red,
+                    "gflops_without_gather": flops(n) / ((worst + red) * 1e-3) / 1e9,
+                    "slowest_shard_frac_of_hbm": max(sh["gbs"] for sh in shards if sh["ms"] == worst)
+                    / peak})
+        del parts
+        torch.cuda.empty_cache()
+    del prob, A, x, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def soak_for_clocks(torch, clocks, step, seconds=1.0):
+    """keep running the same steps (untimed) until `seconds` have passed
+    since the timed region began, so that the clock record has samples
+    however short the timed region is"""
+    while time.perf_counter() - clocks.t_start < seconds:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    clocks.mark_stop()
+
+
+def clocks_summary(clocks, timed_s):
+    c = clocks.summary()
+    c["window"] = ("the timed region (%.4f s) and the same steps continued after it, %.2f s in "
+                   "all" % (timed_s, (clocks.t_stop or 0) - (clocks.t_start or 0)))
+    return c
+
+
+def run_sharded(args, xs, inputs, torch, dist, world, rank, dev):
+    """N ranks, one GPU each: the block-column split of the workload (strong
+    scaling: the same one problem per step whatever N)."""
+    from symmetric_matrix_vector_gb300 import sharded
+
+    n = args.n
+    lda = n + 32
+    c0, c1 = sharded.split("U", n, world)[rank]
+    prob = inputs.device_problem("s", "U", n, lda=lda, alpha=1.0, beta=0.0, seed=n)
+    panel, ldp = sharded.extract_panel(torch, prob["A"], "s", "U", n, lda, c0, c1)
+    x, y = prob["x"], prob["y"]
+    del prob
+    torch.cuda.empty_cache()
+    job = sharded.ShardedSymv(torch, dist, "s", "U", n, c0, c1, panel, ldp, x, 1, world)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        job.step(1.0, 0.0, y, 1)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = xs.xsymv_launch_count()
+    clocks.mark_start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    timed_s = time.perf_counter() - clocks.t_start
+    launches = xs.xsymv_launch_count() - l0
+    soak_for_clocks(torch, clocks, step)
+    dist.barrier()
+    clocks.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
+    ms_per_step = ms / args.steps
+    value = flops(n) / (ms_per_step * 1e-3) / 1e9
+    launches_all = int(max_over_ranks(float(launches), dist) * world)
+
+    # this rank's shard kernel (library events), the slowest rank's figure
+    xs.xsymv_timing_enable(True)
+    for _ in range(args.steps):
+        xs.check(xs.xsymv_s_shard("U", n, c0, c1, panel, ldp, x, 1, job.partial))
+    calls, main_ms, call_ms = xs.xsymv_timing_read()
+    xs.xsymv_timing_enable(False)
+    main_avg = main_ms / max(calls, 1)
+    alg = panel_elements("U", n, c0, c1) * 4.0
+    rate = alg / (main_avg * 1e-3) / 1e9
+    slowest_main = max_over_ranks(main_avg, dist)
+    peak, peak_src = measured_peak()
+    rate_min = -max_over_ranks(-rate, dist)
+
+    # end to end: this rank's panel and x from pinned host memory, y back
+    hp = torch.empty(panel.shape, dtype=panel.dtype, pin_memory=True)
+    hp.copy_(panel)
+    hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    hx.copy_(x)
+    hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+
+    def estep():
+        panel.copy_(hp, non_blocking=True)
+        x.copy_(hx, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        estep()
+    esteps = max(3, min(args.steps, 50))
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(esteps):
+        estep()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ems = max_over_ranks(e0.elapsed_time(e1) / esteps, dist)
+    h2d = max_over_ranks(float(hp.numel() * hp.element_size() + hx.numel() * 4), dist) * world
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(n, world, False),
+            "kernel_variant": xs.xsymv_variant_name(
+                "s", xs.xsymv_selected_variant("s", "U", int((2 * alg / 4) ** 0.5))),
+            "roofline": {"bound": "hbm", "achieved": rate_min, "peak": peak, "unit": "GB/s",
+                         "frac": rate_min / peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": KERNEL, "main_kernel_ms_slowest_rank": slowest_main,
+                         "note": "the slowest rank's shard kernel over its panel's stored bytes"},
+            "e2e": {"value": flops(n) / (ems * 1e-3) / 1e9, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n * 4 * world,
+                    "ms_per_step": ems, "steps": esteps,
+                    "api": "per rank: panel and x copied from pinned host memory, shard, "
+                           "all-gather, reduce, y copied back"},
+            "cpu_baseline": None, "clocks": clocks_summary(clocks, timed_s),
+            "gpu_launches": launches_all,
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+
 
 def run_ours(args):
     import torch
@@ -489,6 +811,8 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     _build.build()
     xs.load()
+    if world > 1 and not args.replicas:
+        return run_sharded(args, xs, inputs, torch, dist, world, rank, dev)
 
     def barrier():
         if dist is not None:
@@ -526,9 +850,10 @@ def run_ours(args):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    clocks.mark_stop()
-    barrier()
+    timed_s = time.perf_counter() - clocks.t_start
     launches = xs.xsymv_launch_count() - l0
+    soak_for_clocks(torch, clocks, step)
+    barrier()
     clocks.stop()
     ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
     ms_per_step = ms / args.steps
@@ -557,67 +882,26 @@ def run_ours(args):
         roofline["frac_same_run_copy"] = achieved / probes["copy_gbs"]
         roofline["frac_same_run_read"] = achieved / probes["read_gbs"]
 
-    # ---- size sweep (the workload's n = 4096 .. 32768 step 4096), beside the headline
-    sweep = []
-    if not args.no_sweep and rank == 0:
-        del prob
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-        clean = torch.zeros(64 << 20, dtype=torch.int64, device="cuda")
-        for m in range(4096, 32768 + 1, 4096):
-            pm = inputs.device_problem("s", "U", m, lda=m + 32, alpha=1.0, beta=0.0, seed=m)
-
-            def call():
-                xs.check(xs.xsymv_s("U", m, 1.0, pm["A"], m + 32, pm["x"], 1, 0.0, pm["y"], 1))
-
-            for _ in range(5):
-                call()
-            torch.cuda.synchronize()
-            # with the L2 flushed before every call: write a 512 MB buffer
-            # (evicting everything) and read another (so that the evicted
-            # dirty lines are written back before the call, not during it).
-            # Nothing synchronises inside the loop: the host enqueues each
-            # call while the flush runs, so the events time the GPU work only.
-            evs = []
-            for _ in range(20):
-                flush.fill_(1)
-                clean.sum()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                call()
-                e1.record(stream)
-                evs.append((e0, e1))
-            torch.cuda.synchronize()
-            t_cold = statistics.median(a.elapsed_time(b) for a, b in evs)
-            # back to back
-            reps = max(10, min(200, int(4e10 / triangle_bytes(m))))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                call()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            t_b2b = e0.elapsed_time(e1) / reps
-            # the headline figure of each size: flushed while the triangle
-            # could partly stay in L2 (under 4x its 129 MB), else back to back
-            cold = triangle_bytes(m) < 4 * L2_BYTES
-            t = t_cold if cold else t_b2b
-            sweep.append({"n": m, "gflops": flops(m) / (t * 1e-3) / 1e9,
-                          "gbs": triangle_bytes(m) / (t * 1e-3) / 1e9,
-                          "frac": triangle_bytes(m) / (t * 1e-3) / 1e9 / peak,
-                          "l2": "flushed (write 512 MB, read 512 MB) before each call, median of 20"
-                          if cold
-                          else "inputs larger than L2, back-to-back calls",
-                          "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
-                          "gbs_back_to_back": triangle_bytes(m) / (t_b2b * 1e-3) / 1e9,
-                          "variant": xs.xsymv_variant_name("s", xs.xsymv_selected_variant("s", "U", m))})
-            del pm
-        del flush, clean
+    # ---- beside the headline: sweep, small sizes, the split on one GPU
+    sweep, small, shards = [], [], []
+    if rank == 0 and not (args.no_sweep and args.no_small and (args.no_shards or world > 1)):
+        del prob, A, x, y
+        torch.cuda.empty_cache()
+        flush = l2_flush_buffers(torch)
+        if not args.no_sweep:
+            sweep = measure_sweep(xs, inputs, torch, stream, peak, flush)
+        if not args.no_small:
+            small = measure_small(xs, inputs, torch, stream, peak, flush)
+        if not args.no_shards and world == 1:
+            shards = measure_shards_one_gpu(xs, inputs, torch, stream, n, peak, flush)
+        del flush
         torch.cuda.empty_cache()
         prob = inputs.device_problem("s", "U", n, lda=n + 32, alpha=1.0, beta=0.0, seed=n)
         A, x, y = prob["A"], prob["x"], prob["y"]
 
     # ---- end to end through the host-buffer entry point
     e2e = None
+    hA = hx = hy = None
     if not args.no_e2e:
         hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
         hA.copy_(A)
@@ -669,24 +953,28 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, calls_c, el = cpu_oracle_rate(8192, args.cpu_seconds)
+        if hA is None:           # the workload's data on the host
+            hA, hx, hy = A.cpu(), x.cpu(), y.cpu()
+        rate, calls_c, el, ns = cpu_oracle_rate(hA.numpy(), lda, hx.numpy(), hy.numpy(), n,
+                                                args.cpu_seconds)
+        what = ("the whole n=%d matrix" % n if ns == n else
+                "the leading %d-by-%d principal block of the n=%d matrix" % (ns, ns, n))
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "the oracle's three-part SSYMV (binary64 accumulator), single-threaded, "
-                         "on n=8192 of the same recipe (uplo=U, lda=n+32, alpha=1, beta=0): "
-                         "%d calls in %.1f s" % (calls_c, el)}
+                         "on %s of this run's own data (copied from the GPU): %d calls in %.1f s"
+                         % (what, calls_c, el)}
 
     if rank == 0:
-        cfg = workload_config(n)
-        cfg["kernel_variant"] = variant
-        cfg["parallelism"] = "replicas" if world > 1 else "single-gpu"
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": cfg,
+            "data": "synthetic", "config": workload_config(n, world, True),
+            "kernel_variant": variant,
             "hbm_gbs": triangle_bytes(n) / (ms_per_step * 1e-3) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks.summary(), "gpu_launches": launches, "sweep": sweep,
+            "clocks": clocks_summary(clocks, timed_s), "gpu_launches": launches, "sweep": sweep,
+            "small_n": small, "shards_one_gpu": shards,
             "kinds": kinds, "gemv_vs_symv": gemv_cmp, "tickets_vs_workspace": tickets,
         }
         print(json.dumps(line), flush=True)

@@ -134,6 +134,80 @@ XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd *A, int l
 XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const float *A, int lda,
                               const float *x, int incx, float beta, float *y, int incy);
 
+/* ---- the product split across GPUs by block columns -------------------
+ * The report cites Level-2 BLAS on multi-GPU systems (its reference [7],
+ * KBLAS, in §1) but describes no split of its own; the plainest reading,
+ * taken here: the stored triangle is split by block columns, each GPU holds
+ * a panel of consecutive columns, streams it once and produces a
+ * full-length partial vector (the row terms of its elements and the column
+ * terms of its columns); the partial vectors are then added and merged with
+ * beta*y.  These calls are the two steps.  A caller with N GPUs runs one
+ * shard per GPU, gathers the N partial vectors (plain copies, e.g. an NCCL
+ * all-gather) and runs the reduction; the sum is taken in rank order, so
+ * the result is bit-identical from run to run for a fixed N and split.
+ *
+ * xsymv_shard_bounds: column boundaries of an even split of the stored
+ *   triangle of order n into nparts panels: panel r is columns
+ *   bounds[r] .. bounds[r+1]-1 (bounds has nparts + 1 entries; bounds[0] = 0,
+ *   bounds[nparts] = n, nondecreasing; a panel may be empty).  Each panel
+ *   holds about 1/nparts of the stored elements; inner boundaries are
+ *   multiples of 16 columns (or n).  Host only (no CUDA call).  Returns 0, or the
+ *   position of the first bad argument (1 uplo, 2 n < 0, 3 nparts < 1,
+ *   4 bounds NULL).
+ *
+ * x<sy|he>mv_<k>_shard(uplo, n, col_begin, col_end, A, lda, x, incx, partial):
+ *   the panel of stored columns col_begin <= j < col_end (0 <= col_begin <=
+ *   col_end <= n) of the symmetric / Hermitian matrix of order n.
+ *   A      DEVICE pointer to the panel alone, column-major with leading
+ *          dimension lda: element (i, j) (matrix indices) at
+ *          A[(i - r0) + (j - col_begin)*lda], with r0 = 0 for uplo 'U' (the
+ *          panel has rows 0 .. col_end-1) and r0 = col_begin for 'L' (rows
+ *          col_begin .. n-1).  Only the stored triangle's elements are used
+ *          (as for xsymv_s: on a 16-byte aligned panel whose boundaries are
+ *          multiples of 16 bytes, vectors in diagonal tiles may also fetch a
+ *          few unused elements beside the diagonal, inside the panel).
+ *   lda    >= max(1, panel rows): col_end for 'U', n - col_begin for 'L'.
+ *   x      DEVICE pointer to all of x (n elements, stride incx != 0).
+ *   partial DEVICE pointer to n contiguous elements, all written: the
+ *          panel's contribution to A*x (no alpha, no beta; zero for an empty
+ *          panel and for rows the panel does not reach).
+ *   Returns 0, the position of the first bad argument (1 uplo, 2 n,
+ *   3 col_begin, 4 col_end, 6 lda, 8 incx; nothing enqueued), or XSYMV_ERR_*
+ *   (XSYMV_ERR_VALUE for a forced "_tk" variant).  Uses the stream's
+ *   workspace like the other calls; asynchronous on the library's stream.
+ *
+ * x<sy|he>mv_<k>_reduce(n, nparts, alpha, partials, ldp, beta, y, incy):
+ *   y := alpha * (P_0 + P_1 + ... + P_{nparts-1}) + beta * y, where P_r is
+ *   the n contiguous elements at partials + r*ldp (DEVICE), added left to
+ *   right in r order.  y: DEVICE, stride incy (negative: BLAS order), only
+ *   y(0..n-1) written; beta = 0: y not read; alpha = 0: partials not read;
+ *   alpha = 0 and beta = 1: nothing touched.  Returns 0, the position of the
+ *   first bad argument (1 n < 0, 2 nparts < 1, 5 ldp < max(1, n), 8 incy = 0;
+ *   nothing enqueued) or XSYMV_ERR_CUDA. */
+XSYMV_API int xsymv_shard_bounds(char uplo, int n, int nparts, int *bounds);
+
+XSYMV_API int xsymv_s_shard(char uplo, int n, int col_begin, int col_end, const float *A,
+                            int lda, const float *x, int incx, float *partial);
+XSYMV_API int xsymv_d_shard(char uplo, int n, int col_begin, int col_end, const double *A,
+                            int lda, const double *x, int incx, double *partial);
+XSYMV_API int xhemv_c_shard(char uplo, int n, int col_begin, int col_end, const xsymv_c32 *A,
+                            int lda, const xsymv_c32 *x, int incx, xsymv_c32 *partial);
+XSYMV_API int xhemv_z_shard(char uplo, int n, int col_begin, int col_end, const xsymv_c64 *A,
+                            int lda, const xsymv_c64 *x, int incx, xsymv_c64 *partial);
+XSYMV_API int xsymv_w_shard(char uplo, int n, int col_begin, int col_end, const xsymv_dd *A,
+                            int lda, const xsymv_dd *x, int incx, xsymv_dd *partial);
+
+XSYMV_API int xsymv_s_reduce(int n, int nparts, float alpha, const float *partials,
+                             long long ldp, float beta, float *y, int incy);
+XSYMV_API int xsymv_d_reduce(int n, int nparts, double alpha, const double *partials,
+                             long long ldp, double beta, double *y, int incy);
+XSYMV_API int xhemv_c_reduce(int n, int nparts, xsymv_c32 alpha, const xsymv_c32 *partials,
+                             long long ldp, xsymv_c32 beta, xsymv_c32 *y, int incy);
+XSYMV_API int xhemv_z_reduce(int n, int nparts, xsymv_c64 alpha, const xsymv_c64 *partials,
+                             long long ldp, xsymv_c64 beta, xsymv_c64 *y, int incy);
+XSYMV_API int xsymv_w_reduce(int n, int nparts, xsymv_dd alpha, const xsymv_dd *partials,
+                             long long ldp, xsymv_dd beta, xsymv_dd *y, int incy);
+
 /* ---- host-buffer variants ----------------------------------------------
  * Same arguments, semantics and status codes as the five calls above, but A,
  * x and y are HOST pointers (device pointers also work).  When all three are

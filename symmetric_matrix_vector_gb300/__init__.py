@@ -33,9 +33,15 @@ __all__ = [
     "xsymv_test_set_call_number",
     "xsymv_probe_peaks", "xgemv_s", "xgemv_d", "gemv", "xgemv_variant_count",
     "xgemv_variant_name", "xgemv_set_variant", "xgemv_selected_variant",
+    "ELEM_BYTES_BY_KIND", "SHARD_ENTRY_POINTS", "REDUCE_ENTRY_POINTS", "symv_shard", "symv_reduce", "xsymv_shard_bounds",
+    "xsymv_s_shard", "xsymv_d_shard", "xhemv_c_shard", "xhemv_z_shard", "xsymv_w_shard",
+    "xsymv_s_reduce", "xsymv_d_reduce", "xhemv_c_reduce", "xhemv_z_reduce", "xsymv_w_reduce",
 ]
 
 ENTRY_POINTS = {"s": "xsymv_s", "d": "xsymv_d", "c": "xhemv_c", "z": "xhemv_z", "w": "xsymv_w"}
+ELEM_BYTES_BY_KIND = {"s": 4, "d": 8, "c": 8, "z": 16, "w": 16}
+SHARD_ENTRY_POINTS = {k: v + "_shard" for k, v in ENTRY_POINTS.items()}
+REDUCE_ENTRY_POINTS = {k: v + "_reduce" for k, v in ENTRY_POINTS.items()}
 
 
 class C32(ctypes.Structure):
@@ -83,6 +89,15 @@ def load():
                 fn = getattr(lib, nm)
                 fn.argtypes = [c_char, c_int, scal[k], vp, c_int, vp, c_int, scal[k], vp, c_int]
                 fn.restype = c_int
+        for k in ENTRY_POINTS:
+            fn = getattr(lib, SHARD_ENTRY_POINTS[k])
+            fn.argtypes = [c_char, c_int, c_int, c_int, vp, c_int, vp, c_int, vp]
+            fn.restype = c_int
+            fn = getattr(lib, REDUCE_ENTRY_POINTS[k])
+            fn.argtypes = [c_int, c_int, scal[k], vp, ctypes.c_longlong, scal[k], vp, c_int]
+            fn.restype = c_int
+        lib.xsymv_shard_bounds.argtypes = [c_char, c_int, c_int, ctypes.POINTER(c_int)]
+        lib.xsymv_shard_bounds.restype = c_int
         lib.xsymv_host_traffic.argtypes = [ctypes.POINTER(ctypes.c_longlong)] * 2
         lib.xsymv_host_traffic.restype = c_int
         lib.xsymv_sync_status.restype = c_int
@@ -248,6 +263,63 @@ def symv_host(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None)
     """Host-buffer variant of ``symv``: A, x, y are host arrays (numpy arrays,
     CPU tensors or raw addresses); y holds the result on return."""
     return _call(kind.lower(), uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=True)
+
+
+# ------------------------------------------- the block-column split -------
+
+def xsymv_shard_bounds(uplo, n, nparts):
+    """Column boundaries [b_0 = 0, ..., b_nparts = n] of an even split of the
+    stored triangle into nparts panels (panel r: columns b_r .. b_{r+1}-1).
+    Host only.  Raises XsymvError on a bad argument."""
+    nparts = int(nparts)
+    if nparts < 1:
+        raise XsymvError(3, "invalid argument 3 (nparts): must be >= 1")
+    out = (ctypes.c_int * (nparts + 1))()
+    check(load().xsymv_shard_bounds(_uplo(uplo), int(n), nparts, out))
+    return list(out)
+
+
+def symv_shard(kind, uplo, n, col_begin, col_end, A, lda, x, incx, partial, stream=None) -> int:
+    """One shard of the block-column split: the panel of stored columns
+    col_begin .. col_end-1 (A: the panel alone, device memory) writes its
+    n-element partial vector to ``partial`` (device).  See include/xsymv.h."""
+    kind = kind.lower()
+    lib = load()
+    _set_stream(lib, stream)
+    return getattr(lib, SHARD_ENTRY_POINTS[kind])(
+        _uplo(uplo), int(n), int(col_begin), int(col_end), ctypes.c_void_p(_ptr(A)), int(lda),
+        ctypes.c_void_p(_ptr(x)), int(incx), ctypes.c_void_p(_ptr(partial)))
+
+
+def symv_reduce(kind, n, nparts, alpha, partials, ldp, beta, y, incy, stream=None) -> int:
+    """y := alpha * (sum of the nparts partial vectors, in rank order) + beta * y
+    (partial r at partials + r*ldp elements; device memory)."""
+    kind = kind.lower()
+    lib = load()
+    _set_stream(lib, stream)
+    return getattr(lib, REDUCE_ENTRY_POINTS[kind])(
+        int(n), int(nparts), _scalar(kind, alpha), ctypes.c_void_p(_ptr(partials)), int(ldp),
+        _scalar(kind, beta), ctypes.c_void_p(_ptr(y)), int(incy))
+
+
+def _shard_fn(kind):
+    def f(uplo, n, col_begin, col_end, A, lda, x, incx, partial, stream=None):
+        return symv_shard(kind, uplo, n, col_begin, col_end, A, lda, x, incx, partial, stream)
+    f.__name__ = SHARD_ENTRY_POINTS[kind]
+    return f
+
+
+def _reduce_fn(kind):
+    def f(n, nparts, alpha, partials, ldp, beta, y, incy, stream=None):
+        return symv_reduce(kind, n, nparts, alpha, partials, ldp, beta, y, incy, stream)
+    f.__name__ = REDUCE_ENTRY_POINTS[kind]
+    return f
+
+
+xsymv_s_shard, xsymv_d_shard, xhemv_c_shard, xhemv_z_shard, xsymv_w_shard = (
+    _shard_fn(k) for k in "sdczw")
+xsymv_s_reduce, xsymv_d_reduce, xhemv_c_reduce, xhemv_z_reduce, xsymv_w_reduce = (
+    _reduce_fn(k) for k in "sdczw")
 
 
 def xsymv_host_traffic():

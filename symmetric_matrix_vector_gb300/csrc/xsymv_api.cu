@@ -11,6 +11,10 @@
 
 namespace xsymv {
 
+// Shard boundaries are multiples of this many columns (except n), so that
+// every kind's panels keep the 16-byte grid of the whole matrix.
+constexpr long long kShardAlign = 16;
+
 namespace {
 
 std::atomic<cudaStream_t> g_stream{nullptr};
@@ -558,6 +562,35 @@ XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n) {
     case 4: return workspace_bytes_w(uplo, n);
   }
   return XSYMV_ERR_VALUE;
+}
+
+XSYMV_API int xsymv_shard_bounds(char uplo, int n, int nparts, int* bounds) {
+  if (uplo != 'U' && uplo != 'u' && uplo != 'L' && uplo != 'l') return 1;
+  if (n < 0) return 2;
+  if (nparts < 1) return 3;
+  if (bounds == nullptr) return 4;
+  const bool upper = (uplo == 'U' || uplo == 'u');
+  // stored elements in the columns before c
+  auto before = [&](long long c) -> long long {
+    return upper ? c * (c + 1) / 2 : c * (long long)n - c * (c - 1) / 2;
+  };
+  const long long total = before(n);
+  bounds[0] = 0;
+  for (int r = 1; r < nparts; ++r) {
+    // the first column c at which the share of parts 0 .. r-1 is reached
+    const long long want = (long long)((__int128)total * r / nparts);
+    long long lo = 0, hi = n;
+    while (lo < hi) {
+      const long long mid = (lo + hi) / 2;
+      if (before(mid) >= want) hi = mid; else lo = mid + 1;
+    }
+    long long c = (lo + kShardAlign / 2) / kShardAlign * kShardAlign;   // nearest multiple
+    if (c > n) c = n;
+    if (c < bounds[r - 1]) c = bounds[r - 1];
+    bounds[r] = (int)c;
+  }
+  bounds[nparts] = n;
+  return XSYMV_OK;
 }
 
 XSYMV_API int xsymv_set_variant(char kind, int index) {

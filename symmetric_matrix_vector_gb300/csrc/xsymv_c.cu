@@ -29,6 +29,7 @@ static_assert(sizeof(c32) == sizeof(xsymv_c32), "C-ABI type layout");
 }  // namespace xsymv
 
 XSYMV_DEFINE_INTROSPECTION(c, xsymv::c32, kVariants_c)
+XSYMV_DEFINE_SHARDS(xhemv_c_shard, xhemv_c_reduce, 'c', xsymv_c32, xsymv::c32, xsymv::kVariants_c)
 
 extern "C" XSYMV_API int xhemv_c(char uplo, int n, xsymv_c32 alpha, const xsymv_c32* A, int lda, const xsymv_c32* x,
                                 int incx, xsymv_c32 beta, xsymv_c32* y, int incy) {

@@ -26,6 +26,7 @@ static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");
 }  // namespace xsymv
 
 XSYMV_DEFINE_INTROSPECTION(d, double, kVariants_d)
+XSYMV_DEFINE_SHARDS(xsymv_d_shard, xsymv_d_reduce, 'd', double, double, xsymv::kVariants_d)
 
 extern "C" XSYMV_API int xsymv_d(char uplo, int n, double alpha, const double* A, int lda, const double* x,
                                 int incx, double beta, double* y, int incy) {

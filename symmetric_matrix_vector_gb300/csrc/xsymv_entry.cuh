@@ -3,6 +3,7 @@
 // kernel and finaliser, or the one ordered-ticket kernel).
 #pragma once
 
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -261,11 +262,11 @@ cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, const int2*
 // ----------------------------------------------------------- plan tables --
 // The bytes that identify a plan's tables (all ints: no padding).
 struct TablesKey {
-  int n, NB, upper, cd, cg, W, G;
+  int n, NB, upper, cd, cg, W, G, c0, c1;
 };
 
 inline TablesKey tables_key(const Plan& p) {
-  return TablesKey{p.n, p.NB, p.upper, p.cd, p.cg, p.W, p.G};
+  return TablesKey{p.n, p.NB, p.upper, p.cd, p.cg, p.W, p.G, p.c0, p.c1};
 }
 
 // bytes of the warp table (int4 per warp) followed by the row table (int2
@@ -362,13 +363,17 @@ int pick_variant(const Variant<T>* table, int count, char kind, int upper, int n
   return r - 1;
 }
 
+// The plan of a call: the whole triangle, or only its stored columns
+// c0 <= j < c1 (a shard; c1 < 0: n).  The variant is the one tuned for a
+// whole triangle of order n_pick (default n).
 template <class T>
-int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, Workload<T>* out) {
+int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, Workload<T>* out,
+              int c0 = 0, int c1 = -1, int n_pick = -1) {
   int dev = 0, sms = 0;
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
-  const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n)];
+  const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n_pick < 0 ? n : n_pick)];
   const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps * v->waves;
-  out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost, v->warps);
+  out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost, v->warps, c0, c1);
   out->variant = v;
   out->wc_off = kHeaderBytes;
   out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
@@ -577,6 +582,125 @@ int symv_host_entry(const Variant<T>* table, int count, char kind, char uplo, in
   return XSYMV_OK;
 }
 
+// ------------------------------------------------------ sharded product --
+// One shard of y := alpha*A*x + beta*y split by block columns: the stored
+// columns c0 <= j < c1 of A (the shard's panel, in its own array), streamed
+// by the same main kernel restricted to that column window; the finaliser
+// writes the panel's partial vector s (n elements, contiguous: row terms of
+// the panel's elements and column terms of its columns) without alpha or
+// beta.  symv_reduce_entry then adds the shards' vectors in rank order.
+//
+// Panel layout: element (i, j) (matrix indices, i in the stored part of
+// column j) at A[(i - r0) + (j - c0) * lda], r0 = 0 for upper storage (the
+// panel holds rows 0 .. c1-1) and r0 = c0 for lower (rows c0 .. n-1).
+inline int check_shard_args(char uplo, int n, int c0, int c1, int lda, int incx) {
+  if (uplo != 'U' && uplo != 'u' && uplo != 'L' && uplo != 'l') return 1;
+  if (n < 0) return 2;
+  if (c0 < 0 || c0 > n) return 3;
+  if (c1 < c0 || c1 > n) return 4;
+  const int rows = (uplo == 'U' || uplo == 'u') ? c1 : n - c0;
+  if (lda < (rows > 1 ? rows : 1)) return 6;
+  if (incx == 0) return 8;
+  return 0;
+}
+
+template <class T>
+int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, int n, int c0,
+                     int c1, const T* A, int lda, const T* x, int incx, T* partial) {
+  int info = check_shard_args(uplo, n, c0, c1, lda, incx);
+  if (info) return info;
+  if (n == 0) return XSYMV_OK;
+  const int upper = (uplo == 'U' || uplo == 'u');
+  cudaStream_t st = current_stream();
+  const T one = T{}, zero = T{};   // unused by the partial and zero modes
+  if (c0 == c1) {  // an empty panel: its partial vector is zero
+    int dev = 0, sms = 0;
+    if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
+    Plan p = plan_make(n, 32, upper, 1);
+    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, nullptr, one, zero, kZero, partial, 1,
+                                       nullptr, 0, st);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+    note_call_status(st, nullptr, 0);
+    return XSYMV_OK;
+  }
+  const T* x0 = x + (incx < 0 ? (long long)(1 - n) * incx : 0);
+  // the variant tuned for a whole triangle with as many stored elements
+  const long long elems =
+      upper ? ((long long)c1 * (c1 + 1) - (long long)c0 * (c0 + 1)) / 2
+            : (long long)(c1 - c0) * n - ((long long)c1 * (c1 - 1) - (long long)c0 * (c0 - 1)) / 2;
+  long long n_pick = (long long)((sqrt(8.0 * (double)elems + 1.0) - 1.0) / 2.0);
+  while (n_pick * (n_pick + 1) / 2 < elems) ++n_pick;
+  while (n_pick > 1 && (n_pick - 1) * n_pick / 2 >= elems) --n_pick;
+  Workload<T> wl;
+  int status = plan_call(table, count, kind, upper, n, &wl, c0, c1, (int)n_pick);
+  if (status) return status;
+  if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;   // no ticket shards
+  int epoch = 0;
+  char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status, 0, &epoch));
+  if (!ws) return status;
+  // the kernels address A(i, j) at A_k + i + j*lda (matrix indices)
+  const long long r0 = upper ? 0 : c0;
+  const uintptr_t a_addr = reinterpret_cast<uintptr_t>(A) -
+                           (uintptr_t)((r0 + (long long)c0 * lda) * (long long)sizeof(T));
+  const T* Ak = reinterpret_cast<const T*>(a_addr);
+  // 16-byte vectors only when every vector a column's stored rows need lies
+  // inside the panel: the window's edges on the 16-byte grid too
+  const bool aligned = a_addr % 16 == 0 && ((long long)lda * (long long)sizeof(T)) % 16 == 0 &&
+                       ((long long)c0 * (long long)sizeof(T)) % 16 == 0 &&
+                       (c1 == n || ((long long)c1 * (long long)sizeof(T)) % 16 == 0);
+  MainArgs<T> m{wl.plan, Ak, lda, x0, incx, reinterpret_cast<T*>(ws + wl.wc_off),
+                reinterpret_cast<T*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch, aligned,
+                st};
+  status = ensure_tables(wl.plan, st, &m.wt, &m.rt);
+  if (status) return status;
+  timing_begin(st);
+  cudaError_t e = wl.variant->launch(m);
+  if (e == cudaSuccess) {
+    timing_mid(st);
+    e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, one, zero, kPartial, partial, 1, m.status,
+                           epoch, st);
+  }
+  timing_end(st);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_launches(2);
+  note_call_status(st, m.status, epoch);
+  return XSYMV_OK;
+}
+
+// y := alpha * (P_0 + ... + P_{N-1}) + beta * y, the parts added in rank
+// order (P_r at P + r*ldp, n contiguous elements each).
+template <class T>
+int symv_reduce_entry(int n, int nparts, T alpha, const T* P, long long ldp, T beta, T* y,
+                      int incy) {
+  if (n < 0) return 1;
+  if (nparts < 1) return 2;
+  if (ldp < (n > 1 ? n : 1)) return 5;
+  if (incy == 0) return 8;
+  if (n == 0) return XSYMV_OK;
+  const bool az = is_zero(alpha), bz = is_zero(beta);
+  if (az && is_one(beta)) return XSYMV_OK;
+  cudaStream_t st = current_stream();
+  T* y0 = y + (incy < 0 ? (long long)(1 - n) * incy : 0);
+  const int mode = az ? (bz ? kZero : kAlphaZero) : (bz ? kBetaZero : kFull);
+  symv_reduce<T><<<(unsigned)((n + kReduceThreads - 1) / kReduceThreads), kReduceThreads, 0, st>>>(
+      n, nparts, P, ldp, alpha, beta, mode, y0, incy);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_launches(1);
+  note_call_status(st, nullptr, 0);
+  return XSYMV_OK;
+}
+
 template <class T>
 long long workspace_bytes(const Variant<T>* table, int count, char kind, char uplo, int n) {
   if (check_args(uplo, n, n > 1 ? n : 1, 1, 1)) return XSYMV_ERR_VALUE;
@@ -587,6 +711,28 @@ long long workspace_bytes(const Variant<T>* table, int count, char kind, char up
 }
 
 }  // namespace xsymv
+
+// The sharded product's two C entry points of one kind (see include/xsymv.h):
+// SHARD(uplo, n, col_begin, col_end, A, lda, x, incx, partial) and
+// REDUCE(n, nparts, alpha, partials, ldp, beta, y, incy).
+#define XSYMV_DEFINE_SHARDS(SHARD, REDUCE, KIND, CT, T, TABLE)                                \
+  extern "C" XSYMV_API int SHARD(char uplo, int n, int col_begin, int col_end, const CT* A,   \
+                                 int lda, const CT* x, int incx, CT* partial) {               \
+    static_assert(sizeof(CT) == sizeof(T), "C-ABI type layout");                              \
+    return xsymv::symv_shard_entry<T>(TABLE, (int)(sizeof(TABLE) / sizeof(TABLE[0])), KIND,   \
+                                      uplo, n, col_begin, col_end,                            \
+                                      reinterpret_cast<const T*>(A), lda,                     \
+                                      reinterpret_cast<const T*>(x), incx,                    \
+                                      reinterpret_cast<T*>(partial));                         \
+  }                                                                                           \
+  extern "C" XSYMV_API int REDUCE(int n, int nparts, CT alpha, const CT* partials,            \
+                                  long long ldp, CT beta, CT* y, int incy) {                  \
+    T a, b;                                                                                   \
+    memcpy(&a, &alpha, sizeof(T));                                                            \
+    memcpy(&b, &beta, sizeof(T));                                                             \
+    return xsymv::symv_reduce_entry<T>(n, nparts, a, reinterpret_cast<const T*>(partials),    \
+                                       ldp, b, reinterpret_cast<T*>(y), incy);                \
+  }
 
 // Per-kind tables and introspection functions (defined in each xsymv_<k>.cu).
 #define XSYMV_DEFINE_INTROSPECTION(KIND, T, TABLE)                                          \

@@ -546,7 +546,10 @@ static __global__ void symv_plan_tables(Plan p, int4* __restrict__ wt, int2* __r
     plan_warp_entry(p, (int)t, &Ia, &Ib, &ja, &jb);
     wt[t] = make_int4(Ia, Ib, (int)ja, (int)jb);
   }
-  if (t < p.nb) rt[t] = make_int2(plan_first_owner(p, (int)t) / p.G, plan_nq(p, (int)t));
+  if (t < p.nb) {
+    const int nq = plan_nq(p, (int)t);   // 0: a row outside the column window
+    rt[t] = make_int2(nq > 0 ? plan_first_owner(p, (int)t) / p.G : 0, nq);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -753,7 +756,21 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
 // ----------------------------------------------------------------------------
 // finalize: y := alpha * (fixed-order sum of the workspace slots) + beta * y
 // ----------------------------------------------------------------------------
-enum FinalMode { kFull = 0, kBetaZero = 1, kAlphaZero = 2, kZero = 3 };
+// What the final merge writes: y = alpha*s + beta*y (kFull), alpha*s
+// (kBetaZero), beta*y (kAlphaZero), 0 (kZero), or the sum s itself
+// (kPartial: one shard's partial vector, merged later by symv_reduce).
+enum FinalMode { kFull = 0, kBetaZero = 1, kAlphaZero = 2, kZero = 3, kPartial = 4 };
+
+// the merged output of one element (shared by the finaliser and the
+// reduction of shards, so both round alike)
+template <class T>
+__device__ __forceinline__ T final_value(int mode, T alpha, T s, T beta, T y_old) {
+  if (mode == kFull) return Ops<T>::add(Ops<T>::mul(alpha, s), Ops<T>::mul(beta, y_old));
+  if (mode == kBetaZero) return Ops<T>::mul(alpha, s);
+  if (mode == kAlphaZero) return Ops<T>::mul(beta, y_old);
+  if (mode == kPartial) return s;
+  return Ops<T>::zero();
+}
 
 constexpr int kFinParts = 8;    // partial sums per output element (the combination order
                                 // below depends on it: changing it changes the rounding)
@@ -787,11 +804,13 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
   const bool need_y = live && pp == 0 && (mode == kFull || mode == kAlphaZero);
   const T y_old = need_y ? *yj : Ops<T>::zero();
   T s = Ops<T>::zero();
-  if (live && (mode == kFull || mode == kBetaZero)) {
+  if (live && (mode == kFull || mode == kBetaZero || mode == kPartial)) {
     const int K = (int)(j / p.NB);
     const int jj = (int)(j - (long long)K * p.NB);
+    // column partials exist only for the window's columns
+    const bool in_window = j >= p.c0 && j < p.c1;
     const int I0 = p.upper ? 0 : K;
-    const int I1 = p.upper ? K : p.nb - 1;
+    const int I1 = !in_window ? I0 - 1 : (p.upper ? K : p.nb - 1);
     const int nq = __ldg(&rt[K].y);
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
     const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
@@ -826,17 +845,42 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
   s = part[0][c];
 #pragma unroll
   for (int k = 1; k < kFinParts; ++k) s = Ops<T>::add(s, part[k][c]);
-  T out;
-  if (mode == kFull)
-    out = Ops<T>::add(Ops<T>::mul(alpha, s), Ops<T>::mul(beta, y_old));
-  else if (mode == kBetaZero)
-    out = Ops<T>::mul(alpha, s);
-  else if (mode == kAlphaZero)
-    out = Ops<T>::mul(beta, y_old);
-  else
-    out = Ops<T>::zero();
+  T out = final_value(mode, alpha, s, beta, y_old);
   if (status != nullptr && *status == epoch) out = Ops<T>::nan();   // the main kernel gave up
   *yj = out;
+}
+
+// ----------------------------------------------------------------------------
+// reduce: the shards' partial vectors summed in rank order, then merged
+// ----------------------------------------------------------------------------
+// y(i) := alpha * (P_0(i) + P_1(i) + ... + P_{N-1}(i)) + beta * y(i), the sum
+// taken left to right in part (rank) order, P_r(i) at P[r*ldp + i]: the
+// block-column split of the stored triangle across GPUs reduced in one fixed
+// order, so the result is bit-identical from run to run.  One thread per
+// output element; the parts' loads are issued 8 at a time.
+constexpr int kReduceThreads = 256;
+
+template <class T>
+__global__ void __launch_bounds__(kReduceThreads)
+symv_reduce(int n, int nparts, const T* __restrict__ P, long long ldp, T alpha, T beta, int mode,
+            T* __restrict__ y, long long incy) {
+  const long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x;
+  if (i >= n) return;
+  T* yi = y + i * incy;
+  const T y_old = (mode == kFull || mode == kAlphaZero) ? *yi : Ops<T>::zero();
+  T s = Ops<T>::zero();
+  if (mode == kFull || mode == kBetaZero) {
+    for (int r0 = 0; r0 < nparts; r0 += 8) {
+      T v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = r0 + k < nparts ? P[(long long)(r0 + k) * ldp + i] : Ops<T>::zero();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (r0 + k < nparts) s = (r0 + k == 0) ? v[k] : Ops<T>::add(s, v[k]);
+    }
+  }
+  *yi = final_value(mode, alpha, s, beta, y_old);
 }
 
 }  // namespace xsymv

@@ -45,30 +45,75 @@ struct Plan {
   int W;            // warps sharing the cost (1 <= W <= SC / max(cd, cg))
   int G;            // warps per thread block: row partials are written per block
   int qmax;         // most blocks that touch one block row
+  int c0, c1;       // column window: only the stored columns c0 <= j < c1
+                    // are streamed (0, n: the whole triangle)
 };
 
+// The window: block row I holds the stored columns of its rows that lie in
+// [c0, c1).  Upper: [max(I*NB, c0), c1); lower: [c0, min((I+1)*NB, n, c1)).
+// Rows with no such column hold nothing and cost nothing; they are the last
+// rows (upper) or the first ones (lower), so the rows that hold columns are
+// consecutive.  With the whole triangle (c0 = 0, c1 = n) every row holds
+// columns.
+
+// first column (matrix index) of block row I's columns
+XSYMV_HD long long plan_colbase(const Plan& p, int I) {
+  if (!p.upper) return p.c0;
+  const long long s = (long long)I * p.NB;
+  return s > p.c0 ? s : (long long)p.c0;
+}
+
 XSYMV_HD long long plan_rowlen(const Plan& p, int I) {
-  if (p.upper) return (long long)p.n - (long long)I * p.NB;
-  long long e = (long long)(I + 1) * p.NB;
-  return e < p.n ? e : (long long)p.n;
+  if (p.upper) {
+    const long long s = plan_colbase(p, I);
+    return p.c1 > s ? p.c1 - s : 0;
+  }
+  long long e = ((long long)I + 1) * p.NB;
+  if (e > p.n) e = p.n;
+  if (e > p.c1) e = p.c1;
+  return e > p.c0 ? e - p.c0 : 0;
 }
 
 // columns of block row I that lie in its diagonal tile
 XSYMV_HD long long plan_dlen(const Plan& p, int I) {
-  long long r = (long long)p.n - (long long)I * p.NB;
-  return r < p.NB ? r : (long long)p.NB;
+  long long s = (long long)I * p.NB, e = s + p.NB;
+  if (e > p.n) e = p.n;
+  if (e > p.c1) e = p.c1;
+  if (s < p.c0) s = p.c0;
+  return e > s ? e - s : 0;
 }
 
-// column segments in block rows before I
+// sum of floor(j / NB) over 0 <= j < m
+XSYMV_HD long long plan_floor_sum(long long m, int NB) {
+  const long long q = m / NB, r = m % NB;
+  return (long long)NB * q * (q - 1) / 2 + q * r;
+}
+
+// column segments in block rows before I (0 <= I <= nb).  Column j of the
+// window lies in block rows I' <= j/NB (upper) or I' >= j/NB (lower), so
+// this is the sum over the window of min(I, j/NB + 1) (upper) or
+// max(0, I - j/NB) (lower), in closed form.
 XSYMV_HD long long plan_segstart(const Plan& p, int I) {
-  if (p.upper) return (long long)I * p.n - (long long)p.NB * I * (I - 1) / 2;
-  return (long long)p.NB * I * (I + 1) / 2;
+  const long long a = p.c0, b = p.c1;
+  long long m = (long long)I * p.NB;   // columns below m lie in a row's diagonal tile or later
+  m = m < a ? a : (m > b ? b : m);
+  const long long fs = plan_floor_sum(m, p.NB) - plan_floor_sum(a, p.NB);
+  if (p.upper) return (m - a) + fs + (long long)I * (b - m);
+  return (long long)I * (m - a) - fs;
 }
 
-// first cost unit of block row I (0 <= I <= nb-1)
+// diagonal-tile columns in block rows before I: the window's columns below
+// min(I*NB, n) (each column lies in exactly one diagonal tile)
+XSYMV_HD long long plan_diag_before(const Plan& p, int I) {
+  long long e = (long long)I * p.NB;
+  if (e > p.n) e = p.n;
+  if (e > p.c1) e = p.c1;
+  return e > p.c0 ? e - p.c0 : 0;
+}
+
+// first cost unit of block row I (0 <= I <= nb; I = nb gives the total)
 XSYMV_HD long long plan_rowstart(const Plan& p, int I) {
-  // every block row before I has a full diagonal tile of NB columns
-  return (long long)p.cd * plan_segstart(p, I) + (long long)(p.cg - p.cd) * p.NB * I;
+  return (long long)p.cd * plan_segstart(p, I) + (long long)(p.cg - p.cd) * plan_diag_before(p, I);
 }
 
 XSYMV_HD long long plan_rowcost(const Plan& p, int I) {
@@ -109,26 +154,27 @@ XSYMV_HD long long plan_col_cost(const Plan& p, int I, long long c) {
   return c < len1 ? (long long)u1 * c : (long long)u1 * len1 + (long long)u2 * (c - len1);
 }
 
-// first column (matrix index) of block row I's columns
-XSYMV_HD long long plan_colbase(const Plan& p, int I) { return p.upper ? (long long)I * p.NB : 0; }
-
 // first cost unit of warp w (w = W gives SC)
 XSYMV_HD long long plan_wstart(const Plan& p, int w) { return (long long)w * p.SC / p.W; }
 
 // the warp whose range contains cost unit s
 XSYMV_HD int plan_owner(const Plan& p, long long s) { return (int)(((s + 1) * p.W - 1) / p.SC); }
 
-// warps owning the first and the last column of block row I
+// warps owning the first and the last column of block row I (a row that
+// holds columns)
 XSYMV_HD int plan_first_owner(const Plan& p, int I) { return plan_owner(p, plan_rowstart(p, I)); }
 XSYMV_HD int plan_last_owner(const Plan& p, int I) {
   return plan_owner(p, plan_rowstart(p, I) + plan_col_cost(p, I, plan_rowlen(p, I) - 1));
 }
-// row-partial slots of block row I: the blocks owning its columns
+// row-partial slots of block row I: the blocks owning its columns (none for
+// a row outside the window)
 XSYMV_HD int plan_nq(const Plan& p, int I) {
+  if (plan_rowlen(p, I) == 0) return 0;
   return plan_last_owner(p, I) / p.G - plan_first_owner(p, I) / p.G + 1;
 }
 
-// block row containing cost unit s (binary search)
+// block row containing cost unit s (binary search: the last row starting at
+// or before s, which holds columns when 0 <= s < SC)
 XSYMV_HD int plan_row_of(const Plan& p, long long s) {
   int lo = 0, hi = p.nb - 1;
   while (lo < hi) {
@@ -138,16 +184,12 @@ XSYMV_HD int plan_row_of(const Plan& p, long long s) {
   return lo;
 }
 
-XSYMV_HD long long plan_total_cost(int n, int NB, int upper, int cd, int cg) {
-  if (n <= 0) return 0;
-  Plan p{n, NB, (n + NB - 1) / NB, upper, cd, cg, 0, 1, 1, 1};
-  return plan_rowstart(p, p.nb - 1) + plan_rowcost(p, p.nb - 1);
-}
-
 // Build the plan for n, NB, uplo with at most Wmax warps in blocks of G; a
-// dense column costs cd units and a diagonal-tile column cg units (cd, cg >= 1).
+// dense column costs cd units and a diagonal-tile column cg units (cd, cg >=
+// 1).  Only the stored columns c0 <= j < c1 are streamed (c1 < 0: n); the
+// window must not be empty (0 <= c0 < c1 <= n).
 inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int cg = 1,
-                      int G = 1) {
+                      int G = 1, int c0 = 0, int c1 = -1) {
   Plan p{};
   p.n = n;
   p.NB = NB;
@@ -155,7 +197,9 @@ inline Plan plan_make(int n, int NB, int upper, long long Wmax, int cd = 1, int 
   p.upper = upper;
   p.cd = cd;
   p.cg = cg;
-  p.SC = plan_total_cost(n, NB, upper, cd, cg);
+  p.c0 = c0;
+  p.c1 = c1 < 0 ? n : c1;
+  p.SC = n > 0 ? plan_rowstart(p, p.nb) : 0;
   const long long unit = cd > cg ? cd : cg;
   long long W = Wmax < p.SC / unit ? Wmax : p.SC / unit;
   p.W = (int)(W < 1 ? 1 : W);

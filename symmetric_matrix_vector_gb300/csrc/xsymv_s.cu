@@ -38,6 +38,7 @@ static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv
 
 XSYMV_DEFINE_INTROSPECTION(s, float, kVariants_s)
+XSYMV_DEFINE_SHARDS(xsymv_s_shard, xsymv_s_reduce, 's', float, float, xsymv::kVariants_s)
 
 extern "C" XSYMV_API int xsymv_s(char uplo, int n, float alpha, const float* A, int lda, const float* x,
                                 int incx, float beta, float* y, int incy) {
@@ -145,7 +146,7 @@ int noalloc_scratch(void** out, int* epoch, cudaStream_t stream, size_t* dev_ind
     xsymv::record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  g_noalloc_devices.push_back(NoallocDevice{d, p, 1, xsymv::TablesKey{-1, 0, 0, 0, 0, 0, 0}});
+  g_noalloc_devices.push_back(NoallocDevice{d, p, 1, xsymv::TablesKey{-1, 0, 0, 0, 0, 0, 0, 0, 0}});
   *out = p;
   *epoch = 1;
   *dev_index = g_noalloc_devices.size() - 1;
@@ -231,7 +232,7 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
     TablesKey& have = g_noalloc_devices[dev_index].tables;
     if (memcmp(&have, &key, sizeof(key)) != 0) {
       e = launch_plan_tables(wl.plan, ws + tab_off, st);
-      have = e == cudaSuccess ? key : TablesKey{-1, 0, 0, 0, 0, 0, 0};
+      have = e == cudaSuccess ? key : TablesKey{-1, 0, 0, 0, 0, 0, 0, 0, 0};
       ++launches;
     }
   }

@@ -22,6 +22,7 @@ static_assert(sizeof(dd) == sizeof(xsymv_dd), "C-ABI type layout");
 }  // namespace xsymv
 
 XSYMV_DEFINE_INTROSPECTION(w, xsymv::dd, kVariants_w)
+XSYMV_DEFINE_SHARDS(xsymv_w_shard, xsymv_w_reduce, 'w', xsymv_dd, xsymv::dd, xsymv::kVariants_w)
 
 extern "C" XSYMV_API int xsymv_w(char uplo, int n, xsymv_dd alpha, const xsymv_dd* A, int lda, const xsymv_dd* x,
                                 int incx, xsymv_dd beta, xsymv_dd* y, int incy) {

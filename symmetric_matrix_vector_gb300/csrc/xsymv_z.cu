@@ -22,6 +22,7 @@ static_assert(sizeof(c64) == sizeof(xsymv_c64), "C-ABI type layout");
 }  // namespace xsymv
 
 XSYMV_DEFINE_INTROSPECTION(z, xsymv::c64, kVariants_z)
+XSYMV_DEFINE_SHARDS(xhemv_z_shard, xhemv_z_reduce, 'z', xsymv_c64, xsymv::c64, xsymv::kVariants_z)
 
 extern "C" XSYMV_API int xhemv_z(char uplo, int n, xsymv_c64 alpha, const xsymv_c64* A, int lda, const xsymv_c64* x,
                                 int incx, xsymv_c64 beta, xsymv_c64* y, int incy) {

@@ -4,7 +4,10 @@
 // row-partial slots of each block row have no holes, that the finaliser's
 // block-row ranges are exactly the rows holding each column, and that the
 // ordered-ticket chains visit exactly the contributors of every output chunk,
-// in increasing warp order.
+// in increasing warp order.  The same holds for a column window (the shard
+// of a block-column split): only the window's stored columns are owned, the
+// rows they miss hold nothing, and the closed-form row starts equal the sums
+// of the row costs.
 #include <cstdio>
 #include <algorithm>
 #include <cstdint>
@@ -17,17 +20,68 @@
 using namespace xsymv;
 
 static int g_G = 1;   // warps per block of the case being checked
+static int g_c0 = 0, g_c1 = 0;   // column window of the case being checked
 
 static int fail(const char* what, int n, int NB, int upper, long long W, int cd, int cg) {
-  std::printf("FAIL %s n=%d NB=%d upper=%d W=%lld cd=%d cg=%d G=%d\n", what, n, NB, upper, W, cd,
-              cg, g_G);
+  std::printf("FAIL %s n=%d NB=%d upper=%d W=%lld cd=%d cg=%d G=%d window=[%d,%d)\n", what, n, NB,
+              upper, W, cd, cg, g_G, g_c0, g_c1);
   return 1;
 }
 
-static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
-  const Plan p = plan_make(n, NB, upper, Wmax, cd, cg, g_G);
+// the warp table: rows Ia..Ib, first column ja in row Ia, end jb in row Ib,
+// whole rows between; read this way it gives exactly the owned columns
+static int check_warp_table(const Plan& p, const std::vector<std::vector<int>>& own,
+                            const std::vector<std::vector<int>>& row_warps, long long Wmax, int cd,
+                            int cg) {
+  const int n = p.n, NB = p.NB, upper = p.upper, nb = p.nb;
+  for (int w = 0; w < p.W; ++w) {
+    int Ia, Ib;
+    long long ja, jb;
+    plan_warp_entry(p, w, &Ia, &Ib, &ja, &jb);
+    for (int I = 0; I < nb; ++I) {
+      const long long cb = plan_colbase(p, I), len = plan_rowlen(p, I);
+      const long long a = I == Ia ? ja : cb, b = I == Ib ? jb : cb + len;
+      for (long long c = 0; c < len; ++c) {
+        const bool mine = I >= Ia && I <= Ib && cb + c >= a && cb + c < b;
+        if (mine != (own[I][c] == w)) return fail("warp table", n, NB, upper, Wmax, cd, cg);
+      }
+    }
+    if (ja > INT32_MAX || jb > INT32_MAX) return fail("warp table range", n, NB, upper, Wmax, cd, cg);
+    // a row strictly between the warp's first and last rows is its alone:
+    // the kernel writes that row partial straight to the block's slot
+    for (int I = Ia + 1; I < Ib; ++I)
+      if (row_warps[I].size() != 1 || row_warps[I][0] != w)
+        return fail("middle row shared", n, NB, upper, Wmax, cd, cg);
+  }
+  return 0;
+}
+
+static int check(int n, int NB, int upper, long long Wmax, int cd, int cg, int c0 = 0,
+                 int c1 = -1) {
+  const Plan p = plan_make(n, NB, upper, Wmax, cd, cg, g_G, c0, c1);
+  g_c0 = p.c0;
+  g_c1 = p.c1;
+  const bool full = p.c0 == 0 && p.c1 == n;
   const int G = p.G;
   const int nb = p.nb;
+  // the window's columns of each block row, from the definition
+  long long acc = 0;
+  for (int I = 0; I < nb; ++I) {
+    long long first = -1, count = 0;
+    for (long long j = p.c0; j < p.c1; ++j) {
+      const bool stored = upper ? j >= (long long)I * NB : j < std::min<long long>(n, (long long)(I + 1) * NB);
+      if (!stored) continue;
+      if (first < 0) first = j;
+      if (j != first + count) return fail("row columns not contiguous", n, NB, upper, Wmax, cd, cg);
+      ++count;
+    }
+    if (plan_rowlen(p, I) != count || (count > 0 && plan_colbase(p, I) != first))
+      return fail("row columns", n, NB, upper, Wmax, cd, cg);
+    // closed-form row start = the costs of the rows before
+    if (plan_rowstart(p, I) != acc) return fail("row start", n, NB, upper, Wmax, cd, cg);
+    acc += plan_rowcost(p, I);
+  }
+  if (plan_rowstart(p, nb) != acc || p.SC != acc) return fail("total cost", n, NB, upper, Wmax, cd, cg);
   // owners[I][c] = warp owning column c of block row I, from the kernel loop
   std::vector<std::vector<int>> own(nb);
   for (int I = 0; I < nb; ++I) own[I].assign((size_t)plan_rowlen(p, I), -1);
@@ -63,6 +117,12 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
     for (int o : own[I])
       if (o < 0) return fail("column not owned", n, NB, upper, Wmax, cd, cg);
     total += (long long)own[I].size();
+    if (row_warps[I].empty()) {
+      // a row outside the window: no columns, no slots
+      if (plan_rowlen(p, I) != 0 || plan_nq(p, I) != 0)
+        return fail("empty row", n, NB, upper, Wmax, cd, cg);
+      continue;
+    }
     // the warps of a row are exactly first_owner .. last_owner, each once, so
     // its blocks are exactly first_owner/G .. last_owner/G: the slots have
     // no holes
@@ -74,7 +134,7 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
   }
   // total segments = stored columns per block row, as the report's triangle
   long long want = 0;
-  for (int I = 0; I < nb; ++I) want += upper ? n - (long long)I * NB : std::min<long long>(n, (long long)(I + 1) * NB);
+  for (long long j = p.c0; j < p.c1; ++j) want += upper ? j / NB + 1 : nb - j / NB;
   if (total != want) return fail("segment count", n, NB, upper, Wmax, cd, cg);
   // finaliser: column j gets column partials from block rows I0..I1
   for (int j = 0; j < n; ++j) {
@@ -83,7 +143,9 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
     for (int I = 0; I < nb; ++I) {
       const long long cb = plan_colbase(p, I), len = plan_rowlen(p, I);
       const bool has = j >= cb && j < cb + len;
-      if (has != (I >= I0 && I <= I1)) return fail("finaliser rows", n, NB, upper, Wmax, cd, cg);
+      const bool in_window = j >= p.c0 && j < p.c1;
+      if (has != (in_window && I >= I0 && I <= I1))
+        return fail("finaliser rows", n, NB, upper, Wmax, cd, cg);
     }
   }
   // the diagonal-tile columns are the ones costed cg
@@ -96,8 +158,14 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
       if (next - plan_col_cost(p, I, c) != (diag ? cg : cd))
         return fail("column cost", n, NB, upper, Wmax, cd, cg);
     }
-    if (d != std::min<long long>(NB, n - (long long)I * NB)) return fail("dlen", n, NB, upper, Wmax, cd, cg);
+    const long long ds = std::max<long long>((long long)I * NB, p.c0);
+    const long long de = std::min<long long>({(long long)I * NB + NB, (long long)n, (long long)p.c1});
+    if (d != std::max<long long>(0, de - ds)) return fail("dlen", n, NB, upper, Wmax, cd, cg);
   }
+  if (p.W >= (1 << 24)) return fail("warp bits", n, NB, upper, Wmax, cd, cg);
+  // the warp table (below) holds for any window; the ordered tickets are
+  // used on the whole triangle only
+  if (!full) return check_warp_table(p, own, row_warps, Wmax, cd, cg);
   // ordered tickets: contributors of chunk K = owners of its columns in any
   // row, plus the warps holding row K's partial slots
   std::vector<std::set<int>> contrib(nb);
@@ -133,28 +201,7 @@ static int check(int n, int NB, int upper, long long Wmax, int cd, int cg) {
       pb = wb;
     }
   }
-  if (p.W >= (1 << 24)) return fail("warp bits", n, NB, upper, Wmax, cd, cg);
-  // the warp table: rows Ia..Ib, first column ja in row Ia, end jb in row Ib,
-  // whole rows between; read this way it gives exactly the owned columns
-  for (int w = 0; w < p.W; ++w) {
-    int Ia, Ib;
-    long long ja, jb;
-    plan_warp_entry(p, w, &Ia, &Ib, &ja, &jb);
-    for (int I = 0; I < nb; ++I) {
-      const long long cb = plan_colbase(p, I), len = plan_rowlen(p, I);
-      const long long a = I == Ia ? ja : cb, b = I == Ib ? jb : cb + len;
-      for (long long c = 0; c < len; ++c) {
-        const bool mine = I >= Ia && I <= Ib && cb + c >= a && cb + c < b;
-        if (mine != (own[I][c] == w)) return fail("warp table", n, NB, upper, Wmax, cd, cg);
-      }
-    }
-    if (ja > INT32_MAX || jb > INT32_MAX) return fail("warp table range", n, NB, upper, Wmax, cd, cg);
-    // a row strictly between the warp's first and last rows is its alone:
-    // the kernel writes that row partial straight to the block's slot
-    for (int I = Ia + 1; I < Ib; ++I)
-      if (row_warps[I].size() != 1 || row_warps[I][0] != w)
-        return fail("middle row shared", n, NB, upper, Wmax, cd, cg);
-  }
+  if (check_warp_table(p, own, row_warps, Wmax, cd, cg)) return 1;
   // the same chains between groups of G consecutive warps (thread blocks)
   for (int G : {1, 3, 8}) {
     const int ng = (p.W + G - 1) / G;
@@ -219,6 +266,25 @@ int main() {
               g_G = G;
               bad += check(n, NB, upper, W, c[0], c[1]);
               ++cases;
+            }
+  // column windows (shards of a block-column split), every boundary kind:
+  // at 0 / n, inside a diagonal tile, on a tile edge, a single column
+  const long long wwarps[] = {1, 3, 64, 1000, 7296};
+  for (int n : sizes)
+    for (int NB : edges)
+      for (int upper = 0; upper < 2; ++upper)
+        for (long long W : wwarps)
+          for (auto& c : costs)
+            for (int G : {1, 8}) {
+              const int wins[][2] = {{n / 3, n}, {0, (2 * n + 2) / 3}, {n / 4, (3 * n + 3) / 4},
+                                     {1, n}, {0, n - 1}, {n / 2, n / 2 + 1},
+                                     {std::min(n, NB), n}, {0, std::min(n, 2 * NB)}};
+              for (auto& w : wins) {
+                if (w[0] < 0 || w[0] >= w[1] || w[1] > n) continue;
+                g_G = G;
+                bad += check(n, NB, upper, W, c[0], c[1], w[0], w[1]);
+                ++cases;
+              }
             }
   std::printf("%d cases, %d failures\n", cases, bad);
   return bad ? 1 : 0;

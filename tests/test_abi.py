@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import symmetric_matrix_vector_gb300 as xs
@@ -153,3 +154,55 @@ def test_tuned_table_names_compiled_variants(lib):
             n = min(n_max, 1 << 20)
             got = xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))
             assert got == name, (kind, uplo, n, name, got)
+
+
+@pytest.mark.parametrize("kind", ["s", "d", "c", "z", "w"])
+def test_shard_and_reduce_argument_errors_on_host(lib, kind):
+    """the shard and reduce entry points check their arguments before any
+    CUDA call (positions in their own signatures)"""
+    one = (1.0, 0.0) if kind == "w" else 1.0
+    zero = (0.0, 0.0) if kind == "w" else 0.0
+    bogus = 0x1000
+    sh = lambda *a: xs.symv_shard(kind, *a, stream=0)          # noqa: E731
+    assert sh("X", 10, 0, 5, bogus, 10, bogus, 1, bogus) == 1
+    assert sh("U", -1, 0, 0, bogus, 10, bogus, 1, bogus) == 2
+    assert sh("U", 10, -1, 5, bogus, 10, bogus, 1, bogus) == 3
+    assert sh("U", 10, 11, 11, bogus, 10, bogus, 1, bogus) == 3
+    assert sh("U", 10, 6, 5, bogus, 10, bogus, 1, bogus) == 4
+    assert sh("U", 10, 0, 11, bogus, 10, bogus, 1, bogus) == 4
+    assert sh("U", 10, 2, 8, bogus, 7, bogus, 1, bogus) == 6     # upper panel: 8 rows
+    assert sh("L", 10, 2, 8, bogus, 7, bogus, 1, bogus) == 6     # lower panel: 8 rows
+    assert sh("U", 10, 2, 8, bogus, 8, bogus, 0, bogus) == 8
+    assert sh("U", 0, 0, 0, bogus, 1, bogus, 1, bogus) == 0
+    red = lambda *a: xs.symv_reduce(kind, *a, stream=0)        # noqa: E731
+    assert red(-1, 2, one, bogus, 4, zero, bogus, 1) == 1
+    assert red(4, 0, one, bogus, 4, zero, bogus, 1) == 2
+    assert red(4, 2, one, bogus, 3, zero, bogus, 1) == 5
+    assert red(4, 2, one, bogus, 4, zero, bogus, 0) == 8
+    assert red(0, 2, one, bogus, 1, zero, bogus, 1) == 0
+    assert red(4, 2, zero, bogus, 4, one, bogus, 1) == 0        # alpha 0, beta 1: nothing
+
+
+def test_shard_bounds_split_evenly():
+    """panel boundaries: start at 0, end at n, nondecreasing, inner ones on
+    multiples of 16 columns (or n), and each panel within a few columns' worth of
+    elements of an even share of the stored triangle"""
+    for uplo in "UL":
+        for n in (0, 1, 15, 16, 100, 1000, 4097, 32768, 100003):
+            for N in (1, 2, 3, 5, 8, 64):
+                b = xs.xsymv_shard_bounds(uplo, n, N)
+                assert len(b) == N + 1 and b[0] == 0 and b[-1] == n
+                assert all(b[r] <= b[r + 1] for r in range(N))
+                assert all(v % 16 == 0 or v == n for v in b[1:-1])
+                if n == 0:
+                    continue
+                j = np.arange(n, dtype=np.int64)
+                pref = np.concatenate([[0], np.cumsum(j + 1 if uplo == "U" else n - j)])
+                share = pref[-1] / N
+                for r in range(N):
+                    got = pref[b[r + 1]] - pref[b[r]]
+                    assert abs(got - share) <= 16 * n + 1, (uplo, n, N, r, got, share)
+    with pytest.raises(xs.XsymvError):
+        xs.xsymv_shard_bounds("Q", 10, 2)
+    with pytest.raises(xs.XsymvError):
+        xs.xsymv_shard_bounds("U", 10, 0)
