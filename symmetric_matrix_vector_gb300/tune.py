@@ -25,8 +25,11 @@ import statistics
 
 from . import _build, inputs
 
-DEFAULT_N = {"s": [4096, 8192, 12288, 16384, 20480, 24576, 28672, 32768], "d": [8192, 16384, 24576], "c": [8192, 16384],
-             "z": [8192, 16384], "w": [4096, 8192]}
+# the sizes each kind is tuned at: the small, L2-resident sizes (triangles of
+# at most a few tens of MB) separately from the HBM-bound ones
+DEFAULT_N = {"s": [512, 1024, 2048, 3072, 4096, 8192, 12288, 16384, 20480, 24576, 28672, 32768],
+             "d": [1024, 2048, 4096, 8192, 16384, 24576], "c": [1024, 2048, 4096, 8192, 16384],
+             "z": [1024, 2048, 4096, 8192, 16384], "w": [1024, 2048, 4096, 8192]}
 TUNED_H = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc", "xsymv_tuned.h")
 INT_MAX = 2147483647
 L2_BYTES = 129e6          # GB300's L2

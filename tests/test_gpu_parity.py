@@ -128,8 +128,50 @@ def test_workloads_small_n(o, name):
 
 @pytest.mark.parametrize("n", [4096, 8192])
 def test_sweep_points_all_rows(o, n):
+    """two points of the size sweep, every row against the oracle's row-by-row
+    coding of the definition"""
     p = inputs.workload("ssymv_sweep", n=n)
-    run_and_check(o, p, rows=sample_rows(n, count=512, seed=n))
+    run_and_check(o, p)
+
+
+def all_rows_error(o, p, y_gpu):
+    """Componentwise error of every row against the oracle's three-part
+    algorithm (its binary64 / binary128 accumulator, for all n rows in one
+    streaming pass), normalised by |alpha|(|A||x|)_i + |beta||y_i|: the
+    normaliser is the same algorithm run on the moduli (real symmetric; a
+    Hermitian diagonal counts with its real part only)."""
+    n, k = p.n, p.kind
+    assert p.incx == 1 and p.incy == 1
+    info, _, hi, lo = o.symv(k, p.uplo, n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
+    assert info == 0
+    M = np.abs(p.A[:, :p.lda]).astype(np.float32)
+    idx = np.arange(n)
+    if k in ("c", "z"):
+        M[idx, idx] = np.abs(p.A[idx, idx].real)
+    info, _, den, _ = o.symv("s", p.uplo, n, abs(complex(p.alpha)), M, p.lda,
+                             np.abs(p.x).astype(np.float32), 1, abs(complex(p.beta)),
+                             np.abs(p.y).astype(np.float32), 1)
+    assert info == 0
+    yl = logical(k, y_gpu, n, 1)
+    if k in ("c", "z"):
+        err = np.hypot((yl.real.astype(np.float64) - hi[:, 0]) - lo[:, 0],
+                       (yl.imag.astype(np.float64) - hi[:, 1]) - lo[:, 1])
+    else:
+        err = np.abs((yl.astype(np.float64) - hi) - lo)
+    return err / den
+
+
+@pytest.mark.parametrize("name,n", [("ssymv_sweep", 32768), ("chemv", 16384)])
+def test_workloads_full_size_all_rows(o, name, n):
+    """the largest single-precision workloads, in the benchmark's launch
+    configuration, checked on every row"""
+    p = inputs.workload(name, n=n)
+    dp = DeviceProblem(p)
+    st, yd = dp.run()
+    assert st == 0
+    err = all_rows_error(o, p, from_device(yd, p.y))
+    assert np.all(np.isfinite(err))
+    assert float(np.max(err)) <= TOL[p.kind], (name, float(np.max(err)))
 
 
 FULL = [("ssymv_sweep", 16384), ("ssymv_sweep", 32768), ("dsymv", None), ("chemv", None),
