@@ -10,6 +10,7 @@
 #include <atomic>
 
 #include "../../include/xsymv.h"
+#include "xsymv_fused.cuh"
 #include "xsymv_kernels.cuh"
 #include "xsymv_ticket.cuh"
 #include "xsymv_runtime.h"
@@ -51,12 +52,13 @@ struct MainArgs {
   int epoch;
   bool aligned;    // A and lda*sizeof(T) on the 16-byte grid
   cudaStream_t stream;
-  // ordered-ticket variants only: the final merge happens in the same launch
-  T* v;                       // n running sums (in the workspace, after Wr)
+  // ordered-ticket and one-launch (fused) variants: the final merge happens
+  // in the same launch
+  T* v;                       // n running sums (in the workspace, after Wr; tickets)
   void* tk;                   // ticket buffer (counters, then the tickets)
   unsigned long long call;    // the call's number in the tickets
   T alpha, beta;
-  int mode;                   // kFull or kBetaZero
+  int mode;                   // kFull, kBetaZero (or, fused, kPartial)
   T* y0;                      // logical element 0 of y
   long long incy;
   // the plan's warp and row tables (built before the launch)
@@ -198,13 +200,63 @@ int ctas_per_sm_ticket() {
   });
 }
 
-// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>][_tk],
+// The one-launch kernel (register path): streams, meets at a grid barrier,
+// then every block takes a share of the final merge.  A cooperative launch
+// (every block resident at once) and, like the main kernel, a programmatic
+// dependent of the stream's previous kernel.
+template <class T, int VR, int U, int WARPS, int MB, int R>
+cudaError_t launch_fused(const MainArgs<T>& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.plan.W + WARPS - 1) / WARPS));
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const FinalArgs<T> f{a.alpha, a.beta, a.mode, a.y0, a.incy};
+  unsigned long long* bar =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(a.status) + kBarrierOffset);
+  const unsigned long long limit = wait_limit_ns();
+  const int stall = test_extra_tx() != 0;
+  if (a.aligned)
+    return cudaLaunchKernelEx(&cfg, symv_fused<T, VR, U, WARPS, true, MB, R>, a.plan, a.A, a.lda,
+                              a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, stall,
+                              bar, f);
+  return cudaLaunchKernelEx(&cfg, symv_fused<T, VR, U, WARPS, false, MB, R>, a.plan, a.A, a.lda,
+                            a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, stall,
+                            bar, f);
+}
+
+template <class T, int VR, int U, int WARPS, int MB, int R>
+int ctas_per_sm_fused() {
+  static std::atomic<int> cache[kMaxDevices];
+  return per_device_count(cache, [] {
+    int b = 0;
+    // the smaller of the two instantiations' residencies: the grid must fit
+    // whole whichever one runs
+    int b2 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, symv_fused<T, VR, U, WARPS, true, MB, R>,
+                                                      WARPS * 32, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, symv_fused<T, VR, U, WARPS, false, MB, R>,
+                                                      WARPS * 32, 0) != cudaSuccess)
+      return 0;
+    return b < b2 ? b : b2;
+  });
+}
+
+// Variant names: vr<VR>_u<U>_<pipe><STAGES>_w<WARPS>[_b<MINB>][_x<WAVES>][_g<G>][_c<R>][_tk|_f],
 // pipe r = loads into registers, t = bulk-copy (TMA) ring of STAGES chunks
 // per warp; _b<MINB>: registers capped so that MINB blocks fit on an SM;
 // _x<WAVES>: that many waves of blocks instead of one resident wave;
 // _g<G>: partition cost G of a diagonal-tile column (default DiagCost);
 // _c<R>: column reductions batched over R columns (default U);
-// _tk: ordered tickets instead of the workspace finaliser (symv_ticket).
+// _tk: ordered tickets instead of the workspace finaliser (symv_ticket);
+// _f: the workspace sums in the same launch, after a grid barrier (symv_fused).
 #define XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, G, SUF)                              \
   Variant<T> {                                                                            \
     "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
@@ -237,6 +289,15 @@ int ctas_per_sm_ticket() {
     "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R "_tk", 32 * Ops<T>::VPL * (VR), (W), 0, \
         kPipeRegisters, 1, (G), &launch_ticket<T, VR, U, W, MB, R>,                            \
         &ctas_per_sm_ticket<T, VR, U, W, MB, R>, kAccumTickets                                 \
+  }
+
+// one launch: the main kernel and the final merge after a grid barrier
+// (8 warps per block: one finaliser block's threads)
+#define XSYMV_FUSED(T, VR, U, W, MB, G, R)                                                      \
+  Variant<T> {                                                                                \
+    "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R "_f", 32 * Ops<T>::VPL * (VR), (W), 0,  \
+        kPipeRegisters, 1, (G), &launch_fused<T, VR, U, W, MB, R>,                             \
+        &ctas_per_sm_fused<T, VR, U, W, MB, R>, kAccumFused                                    \
   }
 
 template <class T>
@@ -433,6 +494,25 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
                 st};
   status = ensure_tables(wl.plan, st, &m.wt, &m.rt);
   if (status) return status;
+  if (wl.variant->accum == kAccumFused) {
+    // one launch: the kernel also applies y = alpha*s + beta*y
+    m.alpha = alpha;
+    m.beta = beta;
+    m.mode = bz ? kBetaZero : kFull;
+    m.y0 = y0;
+    m.incy = incy;
+    timing_begin(st);
+    cudaError_t e = wl.variant->launch(m);
+    timing_mid(st);
+    timing_end(st);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return XSYMV_ERR_CUDA;
+    }
+    note_launches(1);
+    note_call_status(st, m.status, epoch);
+    return XSYMV_OK;
+  }
   if (wl.variant->accum == kAccumTickets) {
     // one launch: the kernel also applies y = alpha*s + beta*y
     const long long tk_bytes = kTkHeaderBytes + (long long)wl.plan.nb * kTkStride * 8;
@@ -638,7 +718,7 @@ int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, i
   Workload<T> wl;
   int status = plan_call(table, count, kind, upper, n, &wl, c0, c1, (int)n_pick);
   if (status) return status;
-  if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;   // no ticket shards
+  if (wl.variant->accum == kAccumTickets) return XSYMV_ERR_VALUE;   // no ticket shards
   int epoch = 0;
   char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status, 0, &epoch));
   if (!ws) return status;
@@ -657,19 +737,28 @@ int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, i
                 st};
   status = ensure_tables(wl.plan, st, &m.wt, &m.rt);
   if (status) return status;
+  const bool fused = wl.variant->accum == kAccumFused;
+  if (fused) {   // the partial vector in the same launch
+    m.alpha = one;
+    m.beta = zero;
+    m.mode = kPartial;
+    m.y0 = partial;
+    m.incy = 1;
+  }
   timing_begin(st);
   cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {
     timing_mid(st);
-    e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, one, zero, kPartial, partial, 1, m.status,
-                           epoch, st);
+    if (!fused)
+      e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, one, zero, kPartial, partial, 1,
+                             m.status, epoch, st);
   }
   timing_end(st);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return XSYMV_ERR_CUDA;
   }
-  note_launches(2);
+  note_launches(fused ? 1 : 2);
   note_call_status(st, m.status, epoch);
   return XSYMV_OK;
 }

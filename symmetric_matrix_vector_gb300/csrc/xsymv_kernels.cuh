@@ -47,6 +47,8 @@
 // writes NaN to y and the host can read the status.
 #pragma once
 
+#include <string.h>
+
 #include <type_traits>
 
 #include "xsymv_plan.h"
@@ -776,27 +778,45 @@ constexpr int kFinParts = 8;    // partial sums per output element (the combinat
                                 // below depends on it: changing it changes the rounding)
 constexpr int kFinCols = 32;    // output elements per block
 
-// Block (kFinParts x kFinCols threads) handles 32 consecutive outputs, which
-// lie in one block row K because NB is a multiple of 32.  Thread (part, c)
-// adds, in increasing order, the column partials of block rows I = I0+part,
-// I0+part+kFinParts, ... and the row-partial slots q = part, part+kFinParts,
-// ...; the kFinParts sums are then added in part order.  The order depends
-// only on (n, NB, W), never on timing.
-template <class T>
-__global__ void __launch_bounds__(kFinParts * kFinCols)
-symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
-              const int2* __restrict__ rt, T alpha, T beta, int mode, T* __restrict__ y,
-              long long incy, const int* status, int epoch) {
-  __shared__ T part[kFinParts][kFinCols];
-  // the next call's main kernel, a programmatic dependent, may be scheduled
-  // once every block of this grid runs; it waits for this grid's completion
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // wait until the preceding grid on the stream (the main kernel) has
-  // completed and its writes are visible (no-op without a programmatic launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+// a workspace element written by this kernel's other blocks (COHERENT: read
+// at the L2, never from a possibly stale L1 or the read-only path) or by an
+// earlier kernel
+template <bool COHERENT, class T>
+__device__ __forceinline__ T ld_ws(const T* p) {
+  static_assert(sizeof(T) == 4 || sizeof(T) == 8 || sizeof(T) == 16, "element size");
+  T r;
+  if (sizeof(T) == 4) {
+    const unsigned* q = reinterpret_cast<const unsigned*>(p);
+    const unsigned b = COHERENT ? __ldcg(q) : __ldg(q);
+    memcpy(&r, &b, sizeof(T));
+  } else if (sizeof(T) == 8) {
+    const unsigned long long* q = reinterpret_cast<const unsigned long long*>(p);
+    const unsigned long long b = COHERENT ? __ldcg(q) : __ldg(q);
+    memcpy(&r, &b, sizeof(T));
+  } else {
+    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p);
+    const ulonglong2 b = COHERENT ? __ldcg(q) : __ldg(q);
+    memcpy(&r, &b, sizeof(T));
+  }
+  return r;
+}
+
+// Outputs fb*kFinCols .. fb*kFinCols + kFinCols - 1 (they lie in one block
+// row K because NB is a multiple of 32), computed by threads 0 ..
+// kFinParts*kFinCols - 1 of the block; every one of them must call this.
+// Thread (part, c) adds, in increasing order, the column partials of block
+// rows I = I0+part, I0+part+kFinParts, ... and the row-partial slots q = part,
+// part+kFinParts, ...; the kFinParts sums are then added in part order.  The
+// order depends only on (n, NB, W), never on timing.
+template <class T, bool COHERENT, int LG = 8>
+__device__ __forceinline__ void finalize_outputs(const Plan& p, const T* Wc, const T* Wr,
+                                                 const int2* __restrict__ rt, T alpha, T beta,
+                                                 int mode, T* y, long long incy,
+                                                 const int* status, int epoch, long long fb,
+                                                 T (&part)[kFinParts][kFinCols]) {
   const int c = threadIdx.x % kFinCols;
   const int pp = threadIdx.x / kFinCols;
-  const long long j = (long long)blockIdx.x * kFinCols + c;
+  const long long j = fb * kFinCols + c;
   const bool live = j < p.n;
   T* yj = y + j * incy;
   // y, and the first row-partial slot, are loaded up front so that their
@@ -813,41 +833,63 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
     const int I1 = !in_window ? I0 - 1 : (p.upper ? K : p.nb - 1);
     const int nq = __ldg(&rt[K].y);
     const T* wr = Wr + (long long)K * p.qmax * p.NB + jj;
-    const T wr_first = pp < nq ? wr[(long long)pp * p.NB] : Ops<T>::zero();
+    const T wr_first = pp < nq ? ld_ws<COHERENT>(wr + (long long)pp * p.NB) : Ops<T>::zero();
     const T* wc = Wc + j;
     // column partials I = I0+pp, I0+pp+kFinParts, ... <= I1, then row
     // partials q = pp, pp+kFinParts, ... < nq, added in that order; loads
-    // are issued 8 at a time (the last group predicated), so a thread waits
-    // for about (count / 8) memory round trips
-    for (int I = I0 + pp; I <= I1; I += 8 * kFinParts) {
-      T v[8];
+    // are issued LG at a time (the last group predicated), so a thread waits
+    // for about (count / LG) memory round trips (LG does not change the order
+    // of the additions)
+    for (int I = I0 + pp; I <= I1; I += LG * kFinParts) {
+      T v[LG];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        v[k] = (I + k * kFinParts <= I1) ? wc[(long long)(I + k * kFinParts) * p.n] : Ops<T>::zero();
+      for (int k = 0; k < LG; ++k)
+        v[k] = (I + k * kFinParts <= I1) ? ld_ws<COHERENT>(wc + (long long)(I + k * kFinParts) * p.n)
+                                         : Ops<T>::zero();
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < LG; ++k)
         if (I + k * kFinParts <= I1) s = Ops<T>::add(s, v[k]);
     }
     if (pp < nq) s = Ops<T>::add(s, wr_first);
-    for (int q = pp + kFinParts; q < nq; q += 8 * kFinParts) {
-      T v[8];
+    for (int q = pp + kFinParts; q < nq; q += LG * kFinParts) {
+      T v[LG];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        v[k] = (q + k * kFinParts < nq) ? wr[(long long)(q + k * kFinParts) * p.NB] : Ops<T>::zero();
+      for (int k = 0; k < LG; ++k)
+        v[k] = (q + k * kFinParts < nq) ? ld_ws<COHERENT>(wr + (long long)(q + k * kFinParts) * p.NB)
+                                        : Ops<T>::zero();
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < LG; ++k)
         if (q + k * kFinParts < nq) s = Ops<T>::add(s, v[k]);
     }
   }
   part[pp][c] = s;
   __syncthreads();
-  if (pp != 0 || !live) return;
-  s = part[0][c];
+  if (pp == 0 && live) {
+    s = part[0][c];
 #pragma unroll
-  for (int k = 1; k < kFinParts; ++k) s = Ops<T>::add(s, part[k][c]);
-  T out = final_value(mode, alpha, s, beta, y_old);
-  if (status != nullptr && *status == epoch) out = Ops<T>::nan();   // the main kernel gave up
-  *yj = out;
+    for (int k = 1; k < kFinParts; ++k) s = Ops<T>::add(s, part[k][c]);
+    T out = final_value(mode, alpha, s, beta, y_old);
+    if (status != nullptr && (COHERENT ? __ldcg(status) : *status) == epoch)
+      out = Ops<T>::nan();   // the main kernel (or this kernel's grid barrier) gave up
+    *yj = out;
+  }
+}
+
+// Block (kFinParts x kFinCols threads) fb handles outputs fb*32 .. fb*32+31.
+template <class T>
+__global__ void __launch_bounds__(kFinParts * kFinCols)
+symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
+              const int2* __restrict__ rt, T alpha, T beta, int mode, T* __restrict__ y,
+              long long incy, const int* status, int epoch) {
+  __shared__ T part[kFinParts][kFinCols];
+  // the next call's main kernel, a programmatic dependent, may be scheduled
+  // once every block of this grid runs; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // wait until the preceding grid on the stream (the main kernel) has
+  // completed and its writes are visible (no-op without a programmatic launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  finalize_outputs<T, false>(p, Wc, Wr, rt, alpha, beta, mode, y, incy, status, epoch,
+                             (long long)blockIdx.x, part);
 }
 
 // ----------------------------------------------------------------------------

@@ -33,6 +33,10 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_REG_G(float, 2, 2, 8, 4, 7),
     XSYMV_REG_G(float, 2, 2, 8, 4, 8),
     XSYMV_REG_G(float, 2, 2, 8, 4, 12),
+    XSYMV_FUSED(float, 1, 2, 8, 6, 11, 2),
+    XSYMV_FUSED(float, 2, 2, 8, 4, 12, 2),
+    XSYMV_FUSED(float, 2, 2, 8, 4, 11, 2),
+    XSYMV_FUSED(float, 1, 2, 8, 6, 7, 2),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv
@@ -207,7 +211,7 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
   int status = plan_call<float>(kVariants_s, count, 's', upper, n, &wl);
   if (status) return status;
   // the ordered-ticket kernels keep state in a second, allocated buffer
-  if (wl.variant->accum != kAccumWorkspace) return XSYMV_ERR_VALUE;
+  if (wl.variant->accum == kAccumTickets) return XSYMV_ERR_VALUE;
   // the plan's tables follow the workspace in the same array
   const long long tab_off = align_up(wl.bytes, 256);
   if (tab_off + tables_bytes(wl.plan) > kNoallocScratchBytes) return XSYMV_ERR_TOO_LARGE;
@@ -224,7 +228,15 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
                     st};
   m.wt = reinterpret_cast<const int4*>(ws + tab_off);
   m.rt = reinterpret_cast<const int2*>(ws + tab_off + ((long long)wl.plan.W * 16 + 255) / 256 * 256);
-  int launches = 2;
+  const bool fused = wl.variant->accum == kAccumFused;
+  if (fused) {   // one launch: the kernel also applies y = alpha*s + beta*y
+    m.alpha = alpha;
+    m.beta = beta;
+    m.mode = bz ? kBetaZero : kFull;
+    m.y0 = y0;
+    m.incy = incy;
+  }
+  int launches = fused ? 1 : 2;
   cudaError_t e = cudaSuccess;
   {
     const TablesKey key = tables_key(wl.plan);
@@ -237,7 +249,7 @@ extern "C" XSYMV_API int xsymv_s_noalloc(char uplo, int n, float alpha, const fl
     }
   }
   if (e == cudaSuccess) e = wl.variant->launch(m);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && !fused)
     e = launch_finalize<float>(wl.plan, m.Wc, m.Wr, m.rt, alpha, beta, bz ? kBetaZero : kFull, y0,
                                incy, m.status, epoch, st);
   if (e != cudaSuccess) {

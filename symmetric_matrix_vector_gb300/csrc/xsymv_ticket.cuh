@@ -54,6 +54,7 @@ constexpr int kTkRows = 32;       // block rows of a block kept in shared memory
 enum Accum {
   kAccumWorkspace = 0,   // symv_main + symv_finalize (fixed-order sums of the workspace)
   kAccumTickets = 1,     // symv_ticket (ordered tickets, one launch)
+  kAccumFused = 2,       // symv_fused (the same fixed-order sums after a grid barrier, one launch)
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {

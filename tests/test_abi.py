@@ -80,7 +80,7 @@ def test_variants_introspection(lib):
         cnt = xs.xsymv_variant_count(kind)
         assert cnt >= 1
         for i in range(cnt):
-            assert re.fullmatch(r"vr\d+_u\d+_[rt]\d+_w\d+(_b\d+)?(_x\d+)?(_g\d+)?(_c\d+)?(_tk)?", xs.xsymv_variant_name(kind, i))
+            assert re.fullmatch(r"vr\d+_u\d+_[rt]\d+_w\d+(_b\d+)?(_x\d+)?(_g\d+)?(_c\d+)?(_tk|_f)?", xs.xsymv_variant_name(kind, i))
         assert xs.xsymv_variant_name(kind, cnt) is None
         assert xs.xsymv_set_variant(kind, cnt) == -4
         assert xs.xsymv_set_variant(kind, -1) == 0

@@ -468,3 +468,71 @@ def test_chained_calls_read_previous_result(lib, kind):
     chained = iterate(False)
     waited = iterate(True)
     assert bool((chained == waited).all())
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_one_launch_variants_barrier_timeout(lib, kind):
+    """The one-launch ("_f") variants meet at a grid barrier with a bounded
+    wait.  The test hook makes every block wait for one block more than the
+    grid has (nothing faults): the wait runs out, the host reads
+    XSYMV_ERR_TIMEOUT, the call's y is NaN, and the next normal call on the
+    same context is correct and bit-identical to the one before."""
+    import torch
+
+    fused = [v for v in range(lib.xsymv_variant_count(kind))
+             if lib.xsymv_variant_name(kind, v).endswith("_f")]
+    assert fused
+    al, be = SCAL[kind]
+    p = inputs.make_problem(kind, "U", 900, lda=900, alpha=al, beta=be, seed=12)
+    dp = DeviceProblem(p)
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+    assert lib.xsymv_set_variant(kind, fused[0]) == 0
+    try:
+        st, good = dp.run()
+        assert st == 0 and lib.xsymv_sync_status() == 0
+        assert lib.xsymv_launch_count() > 0
+        lib.xsymv_set_wait_limit(2_000_000)          # 2 ms
+        lib.xsymv_test_stall(True)
+        st, bad = dp.run()
+        assert st == 0
+        assert lib.xsymv_sync_status() == -6
+        assert np.all(np.isnan(from_device(bad, p.y)))
+        lib.xsymv_test_stall(False)
+        lib.xsymv_set_wait_limit(0)
+        st, again = dp.run()
+        assert st == 0 and lib.xsymv_sync_status() == 0
+        assert bool((again == good).all())
+    finally:
+        lib.xsymv_test_stall(False)
+        lib.xsymv_set_wait_limit(0)
+        lib.xsymv_set_variant(kind, -1)
+
+
+@pytest.mark.parametrize("kind", ["s", "c"])
+def test_one_launch_equals_two_kernels_same_plan(o, lib, kind):
+    """A one-launch variant and the two-kernel variant of the same tile shape,
+    register cap and costs (so the same resident warps and the same plan)
+    compute the same partial sums and add them in the same order: the same
+    bytes."""
+    names = [lib.xsymv_variant_name(kind, v) for v in range(lib.xsymv_variant_count(kind))]
+    al, be = SCAL[kind]
+    pairs = [(v, names.index(nm[:-len("_c2_f")])) for v, nm in enumerate(names)
+             if nm.endswith("_c2_f") and nm[:-len("_c2_f")] in names]
+    assert pairs
+    for vf, vt in pairs:
+        for uplo in ("U", "L"):
+            for n in (700, 3001):
+                p = inputs.make_problem(kind, uplo, n, lda=n + 4, alpha=al, beta=be, seed=n + vf)
+                dp = DeviceProblem(p)
+                try:
+                    assert lib.xsymv_set_variant(kind, vf) == 0
+                    st, yf = dp.run()
+                    assert st == 0
+                    assert lib.xsymv_set_variant(kind, vt) == 0
+                    st, yt = dp.run()
+                    assert st == 0
+                finally:
+                    lib.xsymv_set_variant(kind, -1)
+                err, _ = errors(o, p, from_device(yf, p.y))
+                assert np.max(err) <= TOL[kind]
+                assert bool((yf == yt).all()), (names[vf], names[vt], uplo, n)
