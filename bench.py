@@ -250,9 +250,12 @@ def replica_rate(world: int, flops_per_step: float, ms_per_step: float) -> float
     return world * flops_per_step / (ms_per_step * 1e-3) / 1e9
 
 
-# per kind: (workload name, flops per call / n^2, fp64 instructions per stored element)
+# per kind: (workload name, flops per call / n^2, fp64 instructions per stored
+# element: D 2 DFMA; Z 8 DFMA; W 2 double-double multiply-adds of 24 (a
+# 4-operation exact product, the 20-operation accurate addition) + 3 to
+# renormalise the element as it is read)
 KIND_WORKLOADS = {
-    "d": ("dsymv", 2, 2), "c": ("chemv", 8, 0), "z": ("zhemv", 8, 8), "w": ("wsymv", 2, 57),
+    "d": ("dsymv", 2, 2), "c": ("chemv", 8, 0), "z": ("zhemv", 8, 8), "w": ("wsymv", 2, 51),
 }
 
 
@@ -521,9 +524,20 @@ def l2_flush_buffers(torch):
             torch.zeros(64 << 20, dtype=torch.int64, device="cuda"))
 
 
-def time_flushed(torch, stream, fn, flush, reps=20):
-    """median ms of fn() with the L2 flushed before each call (nothing
-    synchronises inside the loop, so the events time the GPU work only)"""
+def trimmed_mean(values, cut=0.1):
+    """mean without the lowest and highest `cut` fraction: CUDA event times
+    are quantised (on GB300 to about 2 us), and over many calls the quantum's
+    phase varies, so a mean resolves what a median cannot"""
+    v = sorted(values)
+    k = int(len(v) * cut)
+    v = v[k:len(v) - k] or v
+    return sum(v) / len(v)
+
+
+def time_flushed(torch, stream, fn, flush, reps=60):
+    """ms of fn() with the L2 flushed before each call: the trimmed mean over
+    `reps` calls (nothing synchronises inside the loop, so the events time the
+    GPU work only)"""
     evs = []
     for _ in range(reps):
         flush[0].fill_(1)
@@ -534,10 +548,27 @@ def time_flushed(torch, stream, fn, flush, reps=20):
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in evs)
+    return trimmed_mean([a.elapsed_time(b) for a, b in evs])
+
+
+def host_us_per_call(torch, fn, calls=50):
+    """the host's cost of issuing one call (Python binding, library, launch)"""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        fn()
+    dt = (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    return dt * 1e6
 
 
 def time_back_to_back(torch, stream, fn, reps):
+    """ms per call of `reps` calls enqueued back to back.  The GPU first
+    spins for longer than the host needs to enqueue them all, so that the
+    calls run back to back on the GPU and the events time the GPU's work,
+    not the host's rate of issuing calls."""
+    host_s = host_us_per_call(torch, fn, 20) * 1e-6 * reps
+    torch.cuda._sleep(int((1.5 * host_s + 2e-4) * NOMINAL_SM_MHZ * 1e6))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
@@ -569,7 +600,8 @@ def measure_sweep(xs, inputs, torch, stream, peak, flush):
         sweep.append({"n": m, "gflops": flops(m) / (t * 1e-3) / 1e9,
                       "gbs": triangle_bytes(m) / (t * 1e-3) / 1e9,
                       "frac": triangle_bytes(m) / (t * 1e-3) / 1e9 / peak,
-                      "l2": "flushed (write 512 MB, read 512 MB) before each call, median of 20"
+                      "l2": "flushed (write 512 MB, read 512 MB) before each call, trimmed mean "
+                            "of 60"
                       if cold else "inputs larger than L2, back-to-back calls",
                       "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
                       "gbs_back_to_back": triangle_bytes(m) / (t_b2b * 1e-3) / 1e9,
@@ -583,7 +615,7 @@ def measure_small(xs, inputs, torch, stream, peak, flush):
     """Small sizes, whose triangle fits the L2 (n <= 4096: at most 34 MB):
     the n = 1024 lower-triangle workload (lda = n, alpha = 1.25, beta = 0.5)
     and upper triangles n = 512 .. 4096 (lda = n + 32), each call's time
-    with the L2 flushed before it (median of 20) and back to back."""
+    with the L2 flushed before it (trimmed mean of 60) and back to back."""
     cases = [("ssymv n=1024 uplo=L lda=n alpha=1.25 beta=0.5 seed=0", "L", 1024, 1024, 1.25, 0.5, 0)]
     cases += [("ssymv n=%d uplo=U lda=n+32 alpha=1 beta=0 seed=%d" % (m, m), "U", m, m + 32, 1.0,
                0.0, m) for m in (512, 1024, 2048, 3072, 4096)]
@@ -599,8 +631,10 @@ def measure_small(xs, inputs, torch, stream, peak, flush):
         torch.cuda.synchronize()
         t_cold = time_flushed(torch, stream, call, flush)
         t_b2b = time_back_to_back(torch, stream, call, 200)
+        host = host_us_per_call(torch, call)
         out.append({"workload": name, "n": m, "uplo": uplo,
                     "us_l2_flushed": t_cold * 1e3, "us_back_to_back": t_b2b * 1e3,
+                    "host_us_per_call": host,
                     "gflops_l2_flushed": flops(m) / (t_cold * 1e-3) / 1e9,
                     "gflops_back_to_back": flops(m) / (t_b2b * 1e-3) / 1e9,
                     "gbs_l2_flushed": triangle_bytes(m) / (t_cold * 1e-3) / 1e9,
@@ -644,7 +678,7 @@ def measure_shards_one_gpu(xs, inputs, torch, stream, n, peak, flush):
 
             for _ in range(3):
                 call()
-            ms = time_flushed(torch, stream, call, flush, reps=10)
+            ms = time_flushed(torch, stream, call, flush, reps=30)
             el = panel_elements("U", n, c0, c1)
             shards.append({"cols": [c0, c1], "ms": ms, "gbs": el * 4 / (ms * 1e-3) / 1e9,
                            "variant": xs.xsymv_variant_name(
@@ -652,7 +686,7 @@ def measure_shards_one_gpu(xs, inputs, torch, stream, n, peak, flush):
             del panel
         red = time_flushed(torch, stream,
                            lambda: xs.check(xs.xsymv_s_reduce(n, N, 1.0, parts, n, 0.0, y, 1)),
-                           flush, reps=10)
+                           flush, reps=30)
         worst = max(sh["ms"] for sh in shards)
         out.append({"ranks": N, "shards": shards, "max_shard_ms": worst, "reduce_ms": red,
                     "step_ms_without_gather": worst + red,

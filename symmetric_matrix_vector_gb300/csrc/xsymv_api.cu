@@ -43,6 +43,7 @@ struct TimedCall {
   cudaEvent_t ev[3];
 };
 bool g_timing = false;
+std::atomic<bool> g_timing_on{false};   // g_timing, readable without the lock
 std::vector<TimedCall> g_timed;      // calls recorded since the last read
 TimedCall g_cur{};                   // call being recorded
 std::vector<cudaEvent_t> g_free_ev;  // event pool
@@ -356,16 +357,19 @@ void note_host_traffic(long long h2d, long long d2h) {
 }
 
 void timing_begin(cudaStream_t s) {
+  if (!g_timing_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_timing) return;
   for (int i = 0; i < 3; ++i) g_cur.ev[i] = take_event();
   if (g_cur.ev[0]) cudaEventRecord(g_cur.ev[0], s);
 }
 void timing_mid(cudaStream_t s) {
+  if (!g_timing_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_timing && g_cur.ev[1]) cudaEventRecord(g_cur.ev[1], s);
 }
 void timing_end(cudaStream_t s) {
+  if (!g_timing_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_timing) return;
   if (g_cur.ev[2]) cudaEventRecord(g_cur.ev[2], s);
@@ -421,6 +425,7 @@ XSYMV_API int xsymv_last_cuda_error(void) { return g_last_error.load(); }
 XSYMV_API int xsymv_timing_enable(int on) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_timing = on != 0;
+  g_timing_on.store(g_timing);
   if (!g_timing) {
     for (TimedCall& t : g_timed)
       for (int i = 0; i < 3; ++i) g_free_ev.push_back(t.ev[i]);

@@ -428,11 +428,47 @@ int pick_variant(const Variant<T>* table, int count, char kind, int upper, int n
 // c0 <= j < c1 (a shard; c1 < 0: n).  The variant is the one tuned for a
 // whole triangle of order n_pick (default n).
 template <class T>
+int plan_call_uncached(const Variant<T>* table, int count, char kind, int upper, int n,
+                       Workload<T>* out, int c0, int c1, int vi);
+
+// The last few plans of this thread, by (table, device, triangle, n, window,
+// variant): a call of a shape seen just before skips the partition
+// arithmetic (its row loop is O(n / NB)) and the device queries.
+template <class T>
 int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, Workload<T>* out,
               int c0 = 0, int c1 = -1, int n_pick = -1) {
+  struct Entry {
+    const Variant<T>* table;
+    int dev, upper, n, c0, c1, vi;
+    Workload<T> wl;
+  };
+  constexpr int kSlots = 4;
+  thread_local Entry cache[kSlots] = {};
+  thread_local int next = 0;
+  const int vi = pick_variant(table, count, kind, upper, n_pick < 0 ? n : n_pick);
+  const int dev = current_device_index();
+  const int cc1 = c1 < 0 ? n : c1;
+  if (dev >= 0)
+    for (Entry& e : cache)
+      if (e.table == table && e.dev == dev && e.upper == upper && e.n == n && e.c0 == c0 &&
+          e.c1 == cc1 && e.vi == vi) {
+        *out = e.wl;
+        return XSYMV_OK;
+      }
+  const int status = plan_call_uncached(table, count, kind, upper, n, out, c0, c1, vi);
+  if (status == XSYMV_OK && dev >= 0) {
+    cache[next] = Entry{table, dev, upper, n, c0, cc1, vi, *out};
+    next = (next + 1) % kSlots;
+  }
+  return status;
+}
+
+template <class T>
+int plan_call_uncached(const Variant<T>* table, int count, char kind, int upper, int n,
+                       Workload<T>* out, int c0, int c1, int vi) {
   int dev = 0, sms = 0;
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
-  const Variant<T>* v = &table[pick_variant(table, count, kind, upper, n_pick < 0 ? n : n_pick)];
+  const Variant<T>* v = &table[vi];
   const long long wmax = (long long)sms * v->ctas_per_sm() * v->warps * v->waves;
   out->plan = plan_make(n, v->NB, upper, wmax, kDenseCost, v->diag_cost, v->warps, c0, c1);
   out->variant = v;

@@ -51,6 +51,19 @@ __device__ __forceinline__ dd dd_mul(dd a, dd b) {
   quick_two_sum(p, e, s, t);
   return dd{s, t};
 }
+// acc + a*b: TwoProd with FMA gives the high parts' product exactly as
+// p + e, the cross terms a.hi*b.lo and a.lo*b.hi are folded into e, and the
+// pair (p, e) goes straight into the accurate addition, whose TwoSum steps
+// absorb an e slightly above half an ulp of p; renormalising the product
+// first (dd_mul's QuickTwoSum) would cost three more operations and change
+// nothing the addition does not already do.
+__device__ __forceinline__ dd dd_madd(dd acc, dd a, dd b) {
+  const double p = __dmul_rn(a.hi, b.hi);
+  double e = __fma_rn(a.hi, b.hi, -p);
+  e = __fma_rn(a.hi, b.lo, e);
+  e = __fma_rn(a.lo, b.hi, e);
+  return dd_add(acc, dd{p, e});
+}
 __device__ __forceinline__ dd dd_renorm(dd a) {
   dd r;
   quick_two_sum(a.hi, a.lo, r.hi, r.lo);
@@ -173,8 +186,8 @@ template <> struct Ops<dd> {
   __device__ __forceinline__ static dd nan() { return dd{Ops<double>::nan(), Ops<double>::nan()}; }
   __device__ __forceinline__ static dd add(dd a, dd b) { return dd_add(a, b); }
   __device__ __forceinline__ static dd mul(dd a, dd b) { return dd_mul(a, b); }
-  __device__ __forceinline__ static dd madd(dd acc, dd a, dd b) { return dd_add(acc, dd_mul(a, b)); }
-  __device__ __forceinline__ static dd maddc(dd acc, dd a, dd b) { return dd_add(acc, dd_mul(a, b)); }
+  __device__ __forceinline__ static dd madd(dd acc, dd a, dd b) { return dd_madd(acc, a, b); }
+  __device__ __forceinline__ static dd maddc(dd acc, dd a, dd b) { return dd_madd(acc, a, b); }
   __device__ __forceinline__ static dd diag(dd a) { return a; }
   // inputs are renormalised (QuickTwoSum) as they are read
   __device__ __forceinline__ static dd load(const dd* p) {

@@ -36,11 +36,22 @@ L2_BYTES = 129e6          # GB300's L2
 COLD_BELOW = 4 * L2_BYTES  # smaller stored triangles are timed with L2 flushed before each call
 
 
+def trimmed_mean(values, cut=0.1):
+    """mean of the values without the lowest and highest `cut` fraction.
+    CUDA event times are quantised (on GB300 to about 2 us); over many calls
+    the quantum's phase varies, so a mean resolves what a median cannot."""
+    v = sorted(values)
+    k = int(len(v) * cut)
+    v = v[k:len(v) - k] or v
+    return sum(v) / len(v)
+
+
 def measure(xs, kind, uplo, n, variant, reps, prob, cold=False):
-    """median ms of one call.  Back-to-back calls, or, with cold=True, each
-    call after writing a 512 MB buffer and reading another (nothing of the
-    problem left in L2, and no dirty lines left to write back during the
-    call) -- the protocol the benchmark uses for triangles near L2's size."""
+    """ms of one call.  Back-to-back calls (median of three runs), or, with
+    cold=True, each call after writing a 512 MB buffer and reading another
+    (nothing of the problem left in L2, and no dirty lines left to write back
+    during the call; the trimmed mean of many such calls) -- the protocol the
+    benchmark uses for triangles near L2's size."""
     import torch
 
     assert xs.xsymv_set_variant(kind, variant) == 0
@@ -55,7 +66,7 @@ def measure(xs, kind, uplo, n, variant, reps, prob, cold=False):
             flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
             clean = torch.zeros(64 << 20, dtype=torch.int64, device="cuda")
             evs = []
-            for _ in range(max(20, min(reps, 60))):
+            for _ in range(max(60, min(reps, 120))):
                 flush.fill_(1)
                 clean.sum()
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -65,7 +76,7 @@ def measure(xs, kind, uplo, n, variant, reps, prob, cold=False):
                 e1.record()
                 evs.append((e0, e1))
             torch.cuda.synchronize()
-            return statistics.median(a.elapsed_time(b) for a, b in evs)
+            return trimmed_mean([a.elapsed_time(b) for a, b in evs])
         times = []
         for _ in range(3):
             e0 = torch.cuda.Event(enable_timing=True)
