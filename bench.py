@@ -233,6 +233,40 @@ def host_link_gbs(torch, nbytes=1 << 30, reps=5):
     return nbytes / (best * 1e-3) / 1e9
 
 
+def parse_cpulist(text: str):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_host_placement(dev: int):
+    """The GPU's PCI address, its NUMA node and the host CPUs local to it
+    (from sysfs), and the CPUs this process may run on; None where unknown."""
+    info = {"gpu_pci": None, "gpu_numa_node": None, "local_cpus": None,
+            "process_cpus": len(os.sched_getaffinity(0))}
+    try:
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", str(dev)], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        path = "/sys/bus/pci/devices/%s:%s" % (dom[-4:].lower(), rest.lower())
+        info["gpu_pci"] = bus
+        with open(path + "/numa_node") as f:
+            info["gpu_numa_node"] = int(f.read())
+        with open(path + "/local_cpulist") as f:
+            info["local_cpus"] = sorted(parse_cpulist(f.read()))
+    except Exception:
+        pass
+    return info
+
+
 def max_over_ranks(value: float, dist, device="cuda") -> float:
     """The largest value over all ranks (for times: the slowest rank)."""
     if dist is None:
@@ -937,6 +971,19 @@ def run_ours(args):
     e2e = None
     hA = hx = hy = None
     if not args.no_e2e:
+        # the host link's rate as the process starts, then with the process
+        # (and so its page-locked buffers, placed where they are first
+        # touched) on the CPUs local to the GPU, when sysfs names a proper
+        # subset of them
+        placement = gpu_host_placement(dev)
+        placement["link_gbs_default"] = host_link_gbs(torch)
+        local = set(placement["local_cpus"] or [])
+        allowed = os.sched_getaffinity(0)
+        if local and (local & allowed) and (local & allowed) != allowed:
+            os.sched_setaffinity(0, local & allowed)
+            placement["bound_to_local_cpus"] = True
+        else:
+            placement["bound_to_local_cpus"] = False
         hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
         hA.copy_(A)
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -968,6 +1015,7 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
                "steps": esteps,
                "api": "xsymv_s_host on pinned host buffers (read in place over the host link)",
+               "host_placement": placement,
                "roofline": {"bound": "host link", "achieved": moved, "peak": link, "unit": "GB/s",
                             "frac": moved / link,
                             "peak_source": "pinned host -> device copy of 1 GiB, same run"}}

@@ -162,10 +162,8 @@ def _ptr(a) -> int:
 
 
 def _scalar(kind: str, v):
-    if kind == "s":
-        return ctypes.c_float(float(v))
-    if kind == "d":
-        return ctypes.c_double(float(v))
+    if kind == "s" or kind == "d":     # ctypes converts a float to the declared type
+        return float(v)
     if kind == "c":
         v = complex(v)
         return C32(v.real, v.imag)
@@ -183,11 +181,36 @@ def _uplo(u) -> bytes:
     return str(u).encode()[:1] or b"?"
 
 
+_cuda_ok = None          # torch's CUDA availability, asked once
+
+
 def _torch_stream():
+    """torch's current CUDA stream on the current device, as an address
+    (None when torch is not loaded or has no GPU)"""
+    global _cuda_ok
     torch = sys.modules.get("torch")
-    if torch is None or not torch.cuda.is_available():
+    if torch is None:
         return None
+    if _cuda_ok is None:
+        _cuda_ok = bool(torch.cuda.is_available())
+    if not _cuda_ok:
+        return None
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch._C._cuda_getDevice())
     return torch.cuda.current_stream().cuda_stream
+
+
+_stream_set = [None]    # the stream last handed to xsymv_set_stream from here
+
+
+def _use_stream(lib, stream):
+    s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
+                                                getattr(stream, "cuda_stream", stream))
+    s = s or 0
+    if s != _stream_set[0]:
+        lib.xsymv_set_stream(s)
+        _stream_set[0] = s
 
 
 def _host_ptr(a) -> int:
@@ -203,15 +226,12 @@ def _host_ptr(a) -> int:
 
 
 def _call(kind, uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream, host=False):
-    lib = load()
-    s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
-                                                getattr(stream, "cuda_stream", stream))
-    lib.xsymv_set_stream(ctypes.c_void_p(s or 0))
+    lib = _lib if _lib is not None else load()
+    _use_stream(lib, stream)
     fn = getattr(lib, ENTRY_POINTS[kind] + ("_host" if host else ""))
     cv = _host_ptr if host else _ptr
-    return fn(_uplo(uplo), int(n), _scalar(kind, alpha), ctypes.c_void_p(cv(A)), int(lda),
-              ctypes.c_void_p(cv(x)), int(incx), _scalar(kind, beta), ctypes.c_void_p(cv(y)),
-              int(incy))
+    return fn(_uplo(uplo), int(n), _scalar(kind, alpha), cv(A), int(lda), cv(x), int(incx),
+              _scalar(kind, beta), cv(y), int(incy))
 
 
 def xsymv_s(uplo, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
@@ -355,7 +375,9 @@ def xsymv_probe_peaks():
 
 
 def xsymv_set_stream(stream) -> int:
-    return load().xsymv_set_stream(ctypes.c_void_p(int(stream or 0)))
+    s = int(stream or 0)
+    _stream_set[0] = s
+    return load().xsymv_set_stream(s)
 
 
 def xsymv_get_stream() -> int:
@@ -415,9 +437,7 @@ def xsymv_workspace_bytes(kind: str, uplo: str, n: int) -> int:
 # ------------------------------------------- the general product (GEMV) --
 
 def _set_stream(lib, stream):
-    s = _torch_stream() if stream is None else (stream if isinstance(stream, int) else
-                                                getattr(stream, "cuda_stream", stream))
-    lib.xsymv_set_stream(ctypes.c_void_p(s or 0))
+    _use_stream(lib, stream)
 
 
 def gemv(kind, n, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
