@@ -78,6 +78,9 @@ def parse_args():
     ap.add_argument("--no-shards", action="store_true",
                     help="skip the block-column split run shard by shard on one GPU")
     ap.add_argument("--no-small", action="store_true", help="skip the small sizes n = 512 .. 4096")
+    ap.add_argument("--gemv-n", type=int, default=0,
+                    help="order of the SYMV-versus-GEMV comparison (default: 32768 for S, "
+                         "24576 for D)")
     return ap.parse_args()
 
 
@@ -413,12 +416,13 @@ def measure_tickets(xs, inputs, torch, reps=10):
     return out
 
 
-def measure_gemv(xs, inputs, torch, reps=20):
+def measure_gemv(xs, inputs, torch, reps=20, n_over=0):
     """SYMV against the general product GEMV on the same loader (the
     report's §1 expects SYMV at about twice GEMV's speed when memory-bound),
     with cuBLAS's GEMV (torch.mv) beside it as an outside reference."""
     out = []
     for kind, n, uplo, lda_pad in (("s", 32768, "U", 32), ("d", 24576, "L", 0)):
+        n = n_over or n
         lda = n + lda_pad
         es = 4 if kind == "s" else 8
         g = inputs.device_general(kind, n, lda=lda, alpha=1.0, beta=0.0, seed=n)
@@ -1027,7 +1031,7 @@ def run_ours(args):
 
     gemv_cmp = []
     if rank == 0 and not args.no_gemv:
-        gemv_cmp = measure_gemv(xs, inputs, torch)
+        gemv_cmp = measure_gemv(xs, inputs, torch, n_over=args.gemv_n)
 
     tickets = []
     if rank == 0 and not args.no_tickets:
