@@ -144,16 +144,24 @@ def all_rows_error(o, p, y_gpu):
     assert p.incx == 1 and p.incy == 1
     info, _, hi, lo = o.symv(k, p.uplo, n, p.alpha, p.A, p.lda, p.x, 1, p.beta, p.y, 1)
     assert info == 0
-    M = np.abs(p.A[:, :p.lda]).astype(np.float32)
     idx = np.arange(n)
-    if k in ("c", "z"):
-        M[idx, idx] = np.abs(p.A[idx, idx].real)
-    info, _, den, _ = o.symv("s", p.uplo, n, abs(complex(p.alpha)), M, p.lda,
-                             np.abs(p.x).astype(np.float32), 1, abs(complex(p.beta)),
-                             np.abs(p.y).astype(np.float32), 1)
+    if k == "w":      # moduli of the high words (the low words change them by 2^-53 at most)
+        M = np.abs(p.A[:, :p.lda, 0]).astype(np.float32)
+        ax, ay = np.abs(p.x[:, 0]), np.abs(p.y[:, 0])
+        al, be = abs(p.alpha[0]), abs(p.beta[0])
+    else:
+        M = np.abs(p.A[:, :p.lda]).astype(np.float32)
+        if k in ("c", "z"):
+            M[idx, idx] = np.abs(p.A[idx, idx].real)
+        ax, ay = np.abs(p.x), np.abs(p.y)
+        al, be = abs(complex(p.alpha)), abs(complex(p.beta))
+    info, _, den, _ = o.symv("s", p.uplo, n, al, M, p.lda, ax.astype(np.float32), 1, be,
+                             ay.astype(np.float32), 1)
     assert info == 0
     yl = logical(k, y_gpu, n, 1)
-    if k in ("c", "z"):
+    if k == "w":
+        err = np.abs((yl[:, 0] - hi) + (yl[:, 1] - lo))
+    elif k in ("c", "z"):
         err = np.hypot((yl.real.astype(np.float64) - hi[:, 0]) - lo[:, 0],
                        (yl.imag.astype(np.float64) - hi[:, 1]) - lo[:, 1])
     else:
@@ -161,10 +169,10 @@ def all_rows_error(o, p, y_gpu):
     return err / den
 
 
-@pytest.mark.parametrize("name,n", [("ssymv_sweep", 32768), ("chemv", 16384)])
+@pytest.mark.parametrize("name,n", [("ssymv_sweep", 32768), ("chemv", 16384), ("wsymv", 8192)])
 def test_workloads_full_size_all_rows(o, name, n):
-    """the largest single-precision workloads, in the benchmark's launch
-    configuration, checked on every row"""
+    """the largest single-precision workloads and the double-double one, in
+    the benchmark's launch configuration, checked on every row"""
     p = inputs.workload(name, n=n)
     dp = DeviceProblem(p)
     st, yd = dp.run()
