@@ -281,6 +281,17 @@ def max_over_ranks(value: float, dist, device="cuda") -> float:
     return float(t.item())
 
 
+def sum_over_ranks(value: float, dist, device="cuda") -> float:
+    """The sum of value over all ranks."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def replica_rate(world: int, flops_per_step: float, ms_per_step: float) -> float:
     """Whole-job GFLOP/s when each of `world` ranks runs its own replica and
     the slowest rank takes ms_per_step per step."""
@@ -798,7 +809,7 @@ def run_sharded(args, xs, inputs, torch, dist, world, rank, dev):
     ms = max_over_ranks(ev0.elapsed_time(ev1), dist)
     ms_per_step = ms / args.steps
     value = flops(n) / (ms_per_step * 1e-3) / 1e9
-    launches_all = int(max_over_ranks(float(launches), dist) * world)
+    launches_all = int(sum_over_ranks(float(launches), dist))
 
     # this rank's shard kernel (library events), the slowest rank's figure
     xs.xsymv_timing_enable(True)
@@ -840,7 +851,7 @@ def run_sharded(args, xs, inputs, torch, dist, world, rank, dev):
     torch.cuda.synchronize()
     dist.barrier()
     ems = max_over_ranks(e0.elapsed_time(e1) / esteps, dist)
-    h2d = max_over_ranks(float(hp.numel() * hp.element_size() + hx.numel() * 4), dist) * world
+    h2d = sum_over_ranks(float(hp.numel() * hp.element_size() + hx.numel() * 4), dist)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

@@ -728,13 +728,13 @@ int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, i
   if (n == 0) return XSYMV_OK;
   const int upper = (uplo == 'U' || uplo == 'u');
   cudaStream_t st = current_stream();
-  const T one = T{}, zero = T{};   // unused by the partial and zero modes
+  const T unused = T{};   // alpha and beta: the partial and zero modes read neither
   if (c0 == c1) {  // an empty panel: its partial vector is zero
     int dev = 0, sms = 0;
     if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
     Plan p = plan_make(n, 32, upper, 1);
-    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, nullptr, one, zero, kZero, partial, 1,
-                                       nullptr, 0, st);
+    cudaError_t e = launch_finalize<T>(p, nullptr, nullptr, nullptr, unused, unused, kZero,
+                                       partial, 1, nullptr, 0, st);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       return XSYMV_ERR_CUDA;
@@ -775,8 +775,8 @@ int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, i
   if (status) return status;
   const bool fused = wl.variant->accum == kAccumFused;
   if (fused) {   // the partial vector in the same launch
-    m.alpha = one;
-    m.beta = zero;
+    m.alpha = unused;
+    m.beta = unused;
     m.mode = kPartial;
     m.y0 = partial;
     m.incy = 1;
@@ -786,7 +786,7 @@ int symv_shard_entry(const Variant<T>* table, int count, char kind, char uplo, i
   if (e == cudaSuccess) {
     timing_mid(st);
     if (!fused)
-      e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, one, zero, kPartial, partial, 1,
+      e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, unused, unused, kPartial, partial, 1,
                              m.status, epoch, st);
   }
   timing_end(st);

@@ -75,12 +75,12 @@ static const TunedEntry kTuned[] = {
     {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1105.4 GB/s at n=16384
     {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.5 GB/s at n=1024
     {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 112.2 GB/s at n=2048
-    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 133.0 GB/s at n=4096
-    {'w', 1, 2147483647, "vr8_u1_r0_w4_b0_g6_c8"},   // 147.4 GB/s at n=8192
+    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 132.8 GB/s at n=4096
+    {'w', 1, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 149.6 GB/s at n=8192
     {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.5 GB/s at n=1024
     {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 111.4 GB/s at n=2048
-    {'w', 0, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 131.8 GB/s at n=4096
-    {'w', 0, 2147483647, "vr8_u1_r0_w4_b0_g6_c8"},   // 147.3 GB/s at n=8192
+    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 132.5 GB/s at n=4096
+    {'w', 0, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 149.6 GB/s at n=8192
 };
 // END TUNED TABLE
 

@@ -126,3 +126,26 @@ def test_two_gloo_ranks_split_columns_and_reduce_in_rank_order():
     for rank in range(world):
         for uplo, n, err in out[rank]:
             assert err <= 5e-5, (rank, uplo, n, err)
+
+
+def _sum_worker(rank, world, port, out):
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = bench.sum_over_ranks(float(rank + 1), dist, device="cpu")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_sum_bytes_and_launches():
+    """per-rank counts (bytes copied, kernels launched) add up over ranks"""
+    world = 2
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_sum_worker, args=(world, _free_port(), out), nprocs=world, join=True,
+                       start_method="spawn")
+    assert out[0] == out[1] == 3.0
