@@ -544,3 +544,50 @@ def test_one_launch_equals_two_kernels_same_plan(o, lib, kind):
                 err, _ = errors(o, p, from_device(yf, p.y))
                 assert np.max(err) <= TOL[kind]
                 assert bool((yf == yt).all()), (names[vf], names[vt], uplo, n)
+
+
+@pytest.mark.parametrize("kind", ["s", "d"])
+def test_one_launch_calls_on_two_streams(o, lib, kind):
+    """One-launch calls issued on two streams at once, each with its own
+    problem and workspace: their grids are cooperative (the driver starts a
+    grid only when all of its blocks fit), so neither waits at its barrier for
+    blocks the other holds; both results stay correct and bit-identical to the
+    same calls made one at a time."""
+    import torch
+
+    fused = [v for v in range(lib.xsymv_variant_count(kind))
+             if lib.xsymv_variant_name(kind, v).endswith("_f")]
+    al, be = SCAL[kind]
+    probs = [inputs.make_problem(kind, u, 2500 + 300 * i, lda=2600 + 300 * i, alpha=al, beta=be,
+                                 seed=90 + i) for i, u in enumerate("UL")]
+    dps = [DeviceProblem(p) for p in probs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    assert lib.xsymv_set_variant(kind, fused[0]) == 0
+    try:
+        torch.cuda.synchronize()
+        ref = []
+        for dp, s in zip(dps, streams):
+            with torch.cuda.stream(s):          # y's copy and the call on the same stream
+                st, y = dp.run(stream=s)
+            assert st == 0
+            s.synchronize()
+            ref.append(y)
+        outs = [[], []]
+        for _ in range(10):
+            for i, (dp, s) in enumerate(zip(dps, streams)):
+                with torch.cuda.stream(s):
+                    st, y = dp.run(stream=s)
+                assert st == 0
+                outs[i].append(y)
+        torch.cuda.synchronize()
+        for i, s in enumerate(streams):
+            assert lib.xsymv_set_stream(s.cuda_stream) == 0
+            assert lib.xsymv_sync_status() == 0
+            for y in outs[i]:
+                assert bool((y == ref[i]).all())
+        for p, y in zip(probs, ref):
+            err, _ = errors(o, p, from_device(y, p.y))
+            assert np.max(err) <= TOL[kind]
+    finally:
+        lib.xsymv_set_variant(kind, -1)
+        lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream)

@@ -106,6 +106,24 @@ def test_noalloc_largest_accepted_size(lib):
     _check_case(lib, fn, "U", n, n, 1.0, 0.0, 1, rows=sample_rows(n, count=128, seed=n))
 
 
+def test_noalloc_one_launch_variant(lib):
+    """the allocation-free entry with a one-launch variant forced (its grid
+    barrier's word lives in the array's header): against the oracle and, bit
+    for bit, against xsymv_s with the same variant, two calls in a row"""
+    fn = _noalloc(lib)
+    fused = [v for v in range(lib.xsymv_variant_count("s"))
+             if lib.xsymv_variant_name("s", v).endswith("_f")]
+    assert fused
+    try:
+        for v in fused[:2]:
+            assert lib.xsymv_set_variant("s", v) == 0
+            _check_case(lib, fn, "U", 8192, 8192 + 4, 1.25, 0.5, 1,
+                        rows=sample_rows(8192, count=128, seed=v))
+            _check_case(lib, fn, "L", 3001, 3001, 1.0, 0.0, -1)
+    finally:
+        lib.xsymv_set_variant("s", -1)
+
+
 def test_noalloc_alpha_zero(lib):
     """alpha = 0: y := beta*y, neither A nor x read (NaN bytes there are
     harmless), equal to xsymv_s's result"""
