@@ -121,7 +121,8 @@ std::atomic<long long> g_h2d{0}, g_d2h{0};
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};
 std::atomic<uint32_t> g_extra_tx{0};
 
-void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch) {
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch,
+                size_t* capacity) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) {
@@ -186,6 +187,7 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
     }
     *epoch = ++w->epoch;
   }
+  if (capacity != nullptr) *capacity = w->bytes;
   return w->ptr;
 }
 
@@ -195,11 +197,13 @@ struct CallStatus {
   cudaStream_t stream;
   const int* status;   // nullptr: the latest call has no status word
   int epoch;
+  uintptr_t y_lo, y_hi;   // bytes its finaliser writes (empty: it did not end with one)
 };
 std::vector<CallStatus> g_call_status;
 }  // namespace
 
-void note_call_status(cudaStream_t stream, const int* status, int epoch) {
+void note_call_status(cudaStream_t stream, const int* status, int epoch, uintptr_t y_lo,
+                      uintptr_t y_hi) {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess) {
     cudaGetLastError();
@@ -210,9 +214,29 @@ void note_call_status(cudaStream_t stream, const int* status, int epoch) {
     if (c.device == d && c.stream == stream) {
       c.status = status;
       c.epoch = epoch;
+      c.y_lo = y_lo;
+      c.y_hi = y_hi;
       return;
     }
-  g_call_status.push_back(CallStatus{d, stream, status, epoch});
+  g_call_status.push_back(CallStatus{d, stream, status, epoch, y_lo, y_hi});
+}
+
+bool may_start_early(cudaStream_t stream, uintptr_t a_lo, uintptr_t a_hi, uintptr_t x_lo,
+                     uintptr_t x_hi) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const CallStatus& c : g_call_status)
+    if (c.device == d && c.stream == stream) {
+      if (c.y_lo >= c.y_hi) return false;
+      const bool hits_a = a_lo < c.y_hi && c.y_lo < a_hi;
+      const bool hits_x = x_lo < c.y_hi && c.y_lo < x_hi;
+      return !hits_a && !hits_x;
+    }
+  return false;
 }
 
 namespace {

@@ -64,6 +64,9 @@ struct MainArgs {
   // the plan's warp and row tables (built before the launch)
   const int4* wt;
   const int2* rt;
+  // the main kernel may stream before the stream's previous kernel (the
+  // previous call's finaliser) completes; it waits for it at its end
+  int early;
 };
 
 // One compiled configuration of the main kernel.
@@ -118,10 +121,10 @@ cudaError_t launch_main(const MainArgs<T>& a) {
   if (a.aligned)
     return cudaLaunchKernelEx(&cfg, symv_main<T, VR, U, S, P, WARPS, true, MB, R>, a.plan, a.A,
                               a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch,
-                              limit, extra);
+                              limit, extra, a.early);
   return cudaLaunchKernelEx(&cfg, symv_main<T, VR, U, S, P, WARPS, false, MB, R>, a.plan, a.A,
                             a.lda, a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit,
-                            extra);
+                            extra, a.early);
 }
 
 // resident blocks per SM of one kernel on the current device, computed once
@@ -521,10 +524,21 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   int status = plan_call(table, count, kind, upper, n, &wl);
   if (status) return status;
   int epoch = 0;
-  char* ws = static_cast<char*>(workspace((size_t)wl.bytes, st, &status, 0, &epoch));
+  size_t cap = 0;
+  // two sets of partial sums: calls of even number use the one after the
+  // header, odd ones the one ending (256-byte aligned) at the end of the
+  // buffer, so a call's main kernel never writes what the previous call's
+  // finaliser may still read, whatever the two calls' sizes (the buffer
+  // holds both calls' two sets and 256 bytes more)
+  const long long set = wl.bytes - kHeaderBytes;
+  char* ws = static_cast<char*>(workspace((size_t)(kHeaderBytes + 2 * set + 256), st, &status, 0,
+                                          &epoch, &cap));
   if (!ws) return status;
-  MainArgs<T> m{wl.plan, A, lda, x0, incx, reinterpret_cast<T*>(ws + wl.wc_off),
-                reinterpret_cast<T*>(ws + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
+  const long long odd_start = ((long long)cap - set) / 256 * 256;
+  char* sb = ws + ((epoch & 1) ? odd_start - kHeaderBytes : 0);   // this call's set (offsets
+                                                                  // wc_off.. count the header)
+  MainArgs<T> m{wl.plan, A, lda, x0, incx, reinterpret_cast<T*>(sb + wl.wc_off),
+                reinterpret_cast<T*>(sb + wl.wr_off), reinterpret_cast<int*>(ws), epoch,
                 (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
                     (((long long)lda * (long long)sizeof(T)) % 16 == 0),
                 st};
@@ -554,7 +568,7 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     const long long tk_bytes = kTkHeaderBytes + (long long)wl.plan.nb * kTkStride * 8;
     m.tk = ticket_buffer((size_t)tk_bytes, st, &status, &m.call);
     if (!m.tk) return status;
-    m.v = reinterpret_cast<T*>(ws + wl.v_off);
+    m.v = reinterpret_cast<T*>(sb + wl.v_off);
     m.alpha = alpha;
     m.beta = beta;
     m.mode = bz ? kBetaZero : kFull;
@@ -572,6 +586,15 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     note_call_status(st, m.status, epoch);
     return XSYMV_OK;
   }
+  // the bytes this call reads (A, x) and its finaliser writes (y)
+  const uintptr_t es = sizeof(T);
+  const uintptr_t a_lo = reinterpret_cast<uintptr_t>(A);
+  const uintptr_t a_hi = a_lo + ((uintptr_t)(n - 1) * (uintptr_t)lda + (uintptr_t)n) * es;
+  const uintptr_t x_lo = reinterpret_cast<uintptr_t>(x);
+  const uintptr_t x_hi = x_lo + ((uintptr_t)(n - 1) * (uintptr_t)(incx < 0 ? -incx : incx) + 1) * es;
+  const uintptr_t y_lo = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t y_hi = y_lo + ((uintptr_t)(n - 1) * (uintptr_t)(incy < 0 ? -incy : incy) + 1) * es;
+  m.early = may_start_early(st, a_lo, a_hi, x_lo, x_hi) ? 1 : 0;
   timing_begin(st);
   cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {
@@ -585,7 +608,7 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
     return XSYMV_ERR_CUDA;
   }
   note_launches(2);
-  note_call_status(st, m.status, epoch);
+  note_call_status(st, m.status, epoch, y_lo, y_hi);
   return XSYMV_OK;
 }
 

@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
           T* __restrict__ Wc, T* __restrict__ Wr, const int4* __restrict__ wt,
           const int2* __restrict__ rt, int* status, int epoch, unsigned long long limit_ns,
-          uint32_t extra_tx) {
+          uint32_t extra_tx, int early) {
   using Lay = RingLayout<T, VR, U, STAGES, PIPE>;
   constexpr bool RING = (PIPE == kPipeBulk) && ALIGNED;
   __shared__ RowBuffers<T, WarpTile<T, VR, U>::NB, WARPS> rb;
@@ -743,8 +743,13 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
   }
   // launched as a programmatic dependent of the stream's previous kernel
   // (the previous call's finaliser lets it start early): nothing of global
-  // memory is touched before that kernel has completed
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // memory is touched before that kernel has completed -- unless `early`:
+  // the host has checked that the previous kernel is a finaliser whose
+  // writes (its y) miss A and x, and this call's partial sums go to the other
+  // half of the workspace, so the stream can start at once; the wait then
+  // comes at the end, so that this grid completes only after that finaliser
+  // (the next kernels' ordering rests on it)
+  if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
   bool ok = true;
   if (w < p.W)
     ok = stream_warp<T, VR, U, STAGES, RING, ALIGNED, R, WARPS>(p, w, wl, blockIdx.x, lane, rg, A,
@@ -753,6 +758,7 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
   if (!ok && lane == 0) atomicMax(status, epoch);   // (its row buffers are incomplete: y is NaN)
   __syncthreads();
   row_partials_combine<T, WarpTile<T, VR, U>::NB, WARPS>(p, Wr, rt, blockIdx.x, rb);
+  if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ----------------------------------------------------------------------------

@@ -28,13 +28,25 @@ bool current_device(int* dev, int* sm_count);
 // For slot 0 the first 256 bytes (the status header) are zeroed when the
 // buffer is allocated, and *epoch receives a fresh call number (> 0) that the
 // kernels write to the status word if they give up on a wait.
-void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch);
+// *capacity (if given) receives the buffer's allocated size (>= bytes).
+void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* epoch,
+                size_t* capacity = nullptr);
 
 // Record where the latest call on (current device, stream) keeps its
 // status word and the call number its kernels write there if a bounded wait
 // runs out; xsymv_sync_status reads it.  status == nullptr: the call has no
-// status word (it launched no kernel that waits).
-void note_call_status(cudaStream_t stream, const int* status, int epoch);
+// status word (it launched no kernel that waits).  y_lo < y_hi: the call
+// ended with the two-kernel path's finaliser, which writes (at most) the
+// bytes [y_lo, y_hi) and reads the workspace half of its call number's
+// parity; the next call's main kernel may then stream before it finishes
+// (may_start_early).
+void note_call_status(cudaStream_t stream, const int* status, int epoch, uintptr_t y_lo = 0,
+                      uintptr_t y_hi = 0);
+
+// true if the latest call on (current device, stream) ended with a
+// finaliser whose writes miss both byte ranges [a_lo, a_hi) and [x_lo, x_hi)
+bool may_start_early(cudaStream_t stream, uintptr_t a_lo, uintptr_t a_hi, uintptr_t x_lo,
+                     uintptr_t x_hi);
 
 // Set the last call number of the allocation-free entry point on the current
 // device (defined beside it); false if that entry point has not been called

@@ -591,3 +591,64 @@ def test_one_launch_calls_on_two_streams(o, lib, kind):
     finally:
         lib.xsymv_set_variant(kind, -1)
         lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("kind", ["s", "c", "d"])
+def test_back_to_back_calls_overlap_safely(lib, kind):
+    """A call's main kernel may start streaming while the previous call's
+    finaliser still runs, when the host sees that the finaliser's y misses
+    the new call's A and x (the two calls' partial sums sit in different
+    halves of the workspace).  Calls of two different sizes alternating on one
+    stream with no host wait, and calls whose x or A overlaps the previous
+    call's y (which must wait), give the bytes of the same calls made one at a
+    time."""
+    import torch
+
+    al, be = SCAL[kind]
+    sizes = (1500, 4100) if kind != "d" else (1200, 2900)
+    probs = [inputs.make_problem(kind, u, n, lda=n + 2, alpha=al, beta=be, seed=n)
+             for u, n in zip("UL", sizes)]
+    dps = [DeviceProblem(p) for p in probs]
+    order = [0, 1, 1, 0, 1, 0, 0, 1]
+
+    def run_all(sync):
+        outs = []
+        for i in order:
+            st, y = dps[i].run()
+            assert st == 0
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(y)
+        torch.cuda.synchronize()
+        return outs
+
+    waited = run_all(True)
+    chained = run_all(False)
+    for a, b in zip(waited, chained):
+        assert bool((a == b).all())
+    # the next call reads as its A a buffer the previous call's finaliser is
+    # writing (y): the host must not let it start early
+    n = 512
+    p = inputs.make_problem(kind, "U", n, lda=n, alpha=al, beta=0.0, seed=5)
+    dp = DeviceProblem(p)
+    big = torch.zeros(dp.A.numel(), dtype=torch.uint8, device="cuda")
+    big.copy_(dp.A)
+    es = inputs.ELEM_BYTES[kind]
+
+    def pair(sync):
+        y1 = big[: n * es]                          # call 1 writes the first column of A2
+        st, _ = dp.run(y=y1)
+        assert st == 0
+        if sync:
+            torch.cuda.synchronize()
+        y2 = dp.y0.clone()
+        st, _ = dp.run(A=big, y=y2)                 # call 2 reads it as A
+        assert st == 0
+        torch.cuda.synchronize()
+        return y2.clone(), big.clone()
+
+    big.copy_(dp.A)
+    ref = pair(True)
+    big.copy_(dp.A)
+    got = pair(False)
+    assert bool((ref[0] == got[0]).all()) and bool((ref[1] == got[1]).all())
