@@ -46,7 +46,9 @@
  * Ownership: the caller owns A, x and y (device memory, not freed or kept).
  * The library owns a workspace per (device, stream), allocated with
  * cudaMalloc on first use and grown on demand; it lives until the process
- * exits.  The ordered-ticket variants ("_tk", below) also keep a small
+ * exits.  It holds two sets of partial sums (consecutive calls use
+ * different ones), so that a call whose A and x do not overlap the previous
+ * call's y can start streaming while that call's last kernel still runs.  The ordered-ticket variants ("_tk", below) also keep a small
  * ticket buffer per (device, stream), zeroed when it is allocated.  Work is
  * enqueued on the stream set by xsymv_set_stream (default: the legacy
  * default stream) and runs asynchronously: when a call returns XSYMV_OK the
@@ -331,8 +333,11 @@ XSYMV_API int xsymv_set_variant(char kind, int index);
 XSYMV_API int xsymv_selected_variant(char kind, char uplo, int n);
 
 /* Workspace bytes a call of this kind, uplo and n needs on the current
- * device (< 0: XSYMV_ERR_*); a "_tk" variant's ticket buffer (256 bytes
- * + 32 bytes per chunk of NB outputs) is not included. */
+ * device: the 256-byte header and one set of partial sums (what
+ * xsymv_s_noalloc needs; the stream workspaces of the other entry points
+ * hold two sets and 256 bytes more).  < 0: XSYMV_ERR_*.  A "_tk"
+ * variant's ticket buffer (256 bytes + 32 bytes per chunk of NB outputs) is
+ * not included. */
 XSYMV_API long long xsymv_workspace_bytes(char kind, char uplo, int n);
 
 /* ---- the general product, for comparison ------------------------------

@@ -221,6 +221,44 @@ void note_call_status(cudaStream_t stream, const int* status, int epoch, uintptr
   g_call_status.push_back(CallStatus{d, stream, status, epoch, y_lo, y_hi});
 }
 
+namespace {
+struct OverlapFlag {
+  int device;
+  cudaStream_t stream;
+  int* host;   // page-locked, mapped
+  int* dev;
+};
+std::vector<OverlapFlag> g_overlap;
+}  // namespace
+
+const volatile int* overlap_flag(cudaStream_t stream, int** dev) {
+  *dev = nullptr;
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const OverlapFlag& f : g_overlap)
+    if (f.device == d && f.stream == stream) {
+      *dev = f.dev;
+      return f.host;
+    }
+  void* h = nullptr;
+  void* dp = nullptr;
+  if (cudaHostAlloc(&h, sizeof(int), cudaHostAllocMapped) != cudaSuccess ||
+      cudaHostGetDevicePointer(&dp, h, 0) != cudaSuccess) {
+    cudaGetLastError();
+    if (h != nullptr) cudaFreeHost(h);
+    g_overlap.push_back(OverlapFlag{d, stream, nullptr, nullptr});   // do not try again
+    return nullptr;
+  }
+  *static_cast<int*>(h) = 0;
+  g_overlap.push_back(OverlapFlag{d, stream, static_cast<int*>(h), static_cast<int*>(dp)});
+  *dev = static_cast<int*>(dp);
+  return static_cast<int*>(h);
+}
+
 bool may_start_early(cudaStream_t stream, uintptr_t a_lo, uintptr_t a_hi, uintptr_t x_lo,
                      uintptr_t x_hi) {
   int d = 0;

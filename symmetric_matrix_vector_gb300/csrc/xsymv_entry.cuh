@@ -19,8 +19,11 @@
 namespace xsymv {
 
 // Workspace layout: a 256-byte header (word 0: the status word the main
-// kernel sets to the call's epoch when a bounded wait runs out), then the
-// column partials Wc, then the row partials Wr.
+// kernel sets to the call's epoch when a bounded wait runs out; bytes 8-15:
+// the one-launch kernels' grid barrier; bytes 16-47: the finalisers' end
+// times and the early main kernels' start times, one per call parity), then
+// the column partials Wc, then the row partials Wr (two such sets in the
+// stream workspaces).
 constexpr long long kHeaderBytes = 256;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // 2 s
 
@@ -65,7 +68,8 @@ struct MainArgs {
   const int4* wt;
   const int2* rt;
   // the main kernel may stream before the stream's previous kernel (the
-  // previous call's finaliser) completes; it waits for it at its end
+  // previous call's finaliser) completes; it waits for it at its end, and
+  // notes its start time in the workspace header
   int early;
 };
 
@@ -303,14 +307,29 @@ int ctas_per_sm_fused() {
         &ctas_per_sm_fused<T, VR, U, W, MB, R>, kAccumFused                                    \
   }
 
+// The finaliser's grid: one block per group of kFinCols outputs, or, when
+// `compact`, at most one block per SM, each taking the groups g, g + grid,
+// ... in turn.  The compact grid is slower on its own (its blocks add their
+// groups one after another), but it becomes resident, and so lets the next
+// call's main kernel launch, while this call's main kernel still has blocks
+// running: back-to-back calls then fill each other's tails.  It is used
+// while calls on the stream really overlap (each main kernel that started
+// early reports whether it began before the previous finaliser ended);
+// isolated calls, calls with other work between them and calls that read
+// the previous result keep the full grid.  The sums, hence the results, are
+// the same either way.  ow: see OverlapWords (all null: not used).
 template <class T>
 cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, const int2* rt, T alpha,
                             T beta, int mode, T* y0, long long incy, const int* status, int epoch,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool compact = false,
+                            OverlapWords ow = OverlapWords{nullptr, nullptr, nullptr, nullptr}) {
   // programmatic dependent launch: the launch overlaps the tail of the main
   // kernel, whose completion the finaliser awaits with griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((p.n + kFinCols - 1) / kFinCols));
+  long long groups = (p.n + kFinCols - 1) / kFinCols;
+  int dev = 0, sms = 0;
+  if (compact && current_device(&dev, &sms) && groups > (long long)sms) groups = sms;
+  cfg.gridDim = dim3((unsigned)groups);
   cfg.blockDim = dim3(kFinParts * kFinCols);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
@@ -320,7 +339,7 @@ cudaError_t launch_finalize(const Plan& p, const T* Wc, const T* Wr, const int2*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, symv_finalize<T>, p, Wc, Wr, rt, alpha, beta, mode, y0, incy,
-                            status, epoch);
+                            status, epoch, ow);
 }
 
 // ----------------------------------------------------------- plan tables --
@@ -595,12 +614,20 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   const uintptr_t y_lo = reinterpret_cast<uintptr_t>(y);
   const uintptr_t y_hi = y_lo + ((uintptr_t)(n - 1) * (uintptr_t)(incy < 0 ? -incy : incy) + 1) * es;
   m.early = may_start_early(st, a_lo, a_hi, x_lo, x_hi) ? 1 : 0;
+  // overlap bookkeeping in the header: finaliser end times and main-kernel
+  // start times, one word each per call parity
+  unsigned long long* hw = reinterpret_cast<unsigned long long*>(ws + kOverlapOffset);
+  const int q = epoch & 1;
+  int* report = nullptr;
+  const volatile int* seen = overlap_flag(st, &report);   // null if unavailable
+  OverlapWords ow{hw + q, hw + 2 + q, hw + (1 - q), m.early ? report : nullptr};
+  const bool compact = m.early && seen != nullptr && *seen == 1;
   timing_begin(st);
   cudaError_t e = wl.variant->launch(m);
   if (e == cudaSuccess) {
     timing_mid(st);
     e = launch_finalize<T>(wl.plan, m.Wc, m.Wr, m.rt, alpha, beta, bz ? kBetaZero : kFull, y0,
-                           incy, m.status, epoch, st);
+                           incy, m.status, epoch, st, compact, ow);
   }
   timing_end(st);
   if (e != cudaSuccess) {

@@ -56,6 +56,11 @@
 
 namespace xsymv {
 
+// Bytes into the workspace header of the overlap bookkeeping of
+// back-to-back calls: four 64-bit words, the finalisers' end times and the
+// early main kernels' start times, one of each per call parity.
+constexpr long long kOverlapOffset = 16;
+
 template <int U> struct Log2;
 template <> struct Log2<1> { static constexpr int v = 0; };
 template <> struct Log2<2> { static constexpr int v = 1; };
@@ -113,6 +118,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// store the global timer at p (a 64-bit word), one instruction pair
+__device__ __forceinline__ void note_time(void* p) {
+  asm volatile("{\n\t.reg .u64 t;\n\tmov.u64 t, %%globaltimer;\n\tst.global.u64 [%0], t;\n\t}" ::"l"(p)
+               : "memory");
 }
 
 // Wait for phase `parity` of the mbarrier, giving up once limit_ns have
@@ -750,6 +761,10 @@ symv_main(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ 
   // comes at the end, so that this grid completes only after that finaliser
   // (the next kernels' ordering rests on it)
   if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // an early grid notes when it began, in the header word of its call's
+  // parity (the finaliser compares it with the previous finaliser's end)
+  if (early && blockIdx.x == 0 && threadIdx.x == 0)
+    note_time(reinterpret_cast<char*>(status) + kOverlapOffset + 8 * (2 + (epoch & 1)));
   bool ok = true;
   if (w < p.W)
     ok = stream_warp<T, VR, U, STAGES, RING, ALIGNED, R, WARPS>(p, w, wl, blockIdx.x, lane, rg, A,
@@ -881,12 +896,25 @@ __device__ __forceinline__ void finalize_outputs(const Plan& p, const T* Wc, con
   }
 }
 
-// Block (kFinParts x kFinCols threads) fb handles outputs fb*32 .. fb*32+31.
+// Words of the stream workspace's header through which back-to-back calls
+// learn whether they overlap (all null: not used): `end` receives this
+// finaliser's end time; when `report` is set, this call's main kernel
+// started early, `start` holds its start time and `prev_end` the previous
+// finaliser's end time, and *report (host-mapped) gets 1 if they overlapped.
+struct OverlapWords {
+  unsigned long long* end;
+  const unsigned long long* start;
+  const unsigned long long* prev_end;
+  int* report;
+};
+
+// Block (kFinParts x kFinCols threads) b handles the groups of outputs
+// fb*32 .. fb*32+31 for fb = b, b + grid, ...
 template <class T>
 __global__ void __launch_bounds__(kFinParts * kFinCols)
 symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
               const int2* __restrict__ rt, T alpha, T beta, int mode, T* __restrict__ y,
-              long long incy, const int* status, int epoch) {
+              long long incy, const int* status, int epoch, OverlapWords ow) {
   __shared__ T part[kFinParts][kFinCols];
   // the next call's main kernel, a programmatic dependent, may be scheduled
   // once every block of this grid runs; it waits for this grid's completion
@@ -894,8 +922,23 @@ symv_finalize(Plan p, const T* __restrict__ Wc, const T* __restrict__ Wr,
   // wait until the preceding grid on the stream (the main kernel) has
   // completed and its writes are visible (no-op without a programmatic launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  finalize_outputs<T, false>(p, Wc, Wr, rt, alpha, beta, mode, y, incy, status, epoch,
-                             (long long)blockIdx.x, part);
+  // after an early main kernel: did it start before the previous finaliser
+  // ended (nothing else ran between the two calls)?  The host reads the
+  // answer when it enqueues later calls, and gives their finalisers the
+  // compact grid while the answer is yes
+  if (ow.report != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    const unsigned long long began = *reinterpret_cast<const volatile unsigned long long*>(ow.start);
+    const unsigned long long ended = *reinterpret_cast<const volatile unsigned long long*>(ow.prev_end);
+    *reinterpret_cast<volatile int*>(ow.report) = began < ended ? 1 : 0;
+  }
+  const long long nfb = (p.n + kFinCols - 1) / kFinCols;
+  for (long long fb = blockIdx.x; fb < nfb; fb += gridDim.x) {
+    finalize_outputs<T, false>(p, Wc, Wr, rt, alpha, beta, mode, y, incy, status, epoch, fb, part);
+    __syncthreads();   // (part is reused by the next group)
+  }
+  // the time the grid's last block ends (a reduction nobody waits for): the
+  // next call's finaliser compares it with the start of that call's main kernel
+  if (ow.end != nullptr && threadIdx.x == 0) atomicMax(ow.end, global_ns());
 }
 
 // ----------------------------------------------------------------------------

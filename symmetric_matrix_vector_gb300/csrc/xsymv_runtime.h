@@ -43,6 +43,13 @@ void* workspace(size_t bytes, cudaStream_t stream, int* status, int slot, int* e
 void note_call_status(cudaStream_t stream, const int* status, int epoch, uintptr_t y_lo = 0,
                       uintptr_t y_hi = 0);
 
+// A host-mapped word per (current device, stream) in which the main
+// kernels of early-started calls report whether they overlapped the previous
+// finaliser: returns its host address (read it to see the latest report)
+// and sets *dev to its device address; nullptr (and *dev = nullptr) if it
+// could not be allocated.
+const volatile int* overlap_flag(cudaStream_t stream, int** dev);
+
 // true if the latest call on (current device, stream) ended with a
 // finaliser whose writes miss both byte ranges [a_lo, a_hi) and [x_lo, x_hi)
 bool may_start_early(cudaStream_t stream, uintptr_t a_lo, uintptr_t a_hi, uintptr_t x_lo,
