@@ -36,3 +36,13 @@ def test_render_table_fills_missing_kinds():
     assert "{'z', 1, %d, \"x\"}" % tune.INT_MAX in text
     for k in "sdcw":
         assert "{'%s', -1, %d, \"\"}," % (k, tune.INT_MAX) in text
+
+
+def test_choose_breaks_near_ties_by_back_to_back_time():
+    done = {}
+    for r in (dict(rec("s", "U", 8192, 0, "a", 1.000), ms_b2b=0.95),
+              dict(rec("s", "U", 8192, 1, "b", 1.005), ms_b2b=0.80),
+              dict(rec("s", "U", 8192, 2, "c", 1.100), ms_b2b=0.50)):
+        done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
+    (entry,) = tune.choose(done)
+    assert entry[3]["variant_name"] == "b"      # c is fastest back to back but 10 % slower alone
