@@ -17,70 +17,70 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 768, "vr1_u2_r0_w8_b0_g9"},   // 50.4 GB/s at n=512
-    {'s', 1, 1536, "vr2_u2_r0_w8_b4_g8"},   // 174.9 GB/s at n=1024
-    {'s', 1, 2560, "vr1_u2_r0_w8"},   // 613.9 GB/s at n=2048
-    {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1274.2 GB/s at n=3072
-    {'s', 1, 6144, "vr2_u2_r0_w8_b4_g8"},   // 1899.0 GB/s at n=4096
-    {'s', 1, 10240, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 4093.3 GB/s at n=8192
-    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 5443.9 GB/s at n=12288
-    {'s', 1, 18432, "vr2_u2_r0_w8_b4_g11"},   // 6282.1 GB/s at n=16384
-    {'s', 1, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6516.5 GB/s at n=20480
-    {'s', 1, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6617.4 GB/s at n=24576
-    {'s', 1, 30720, "vr2_u2_r0_w8_b4_g11"},   // 6752.6 GB/s at n=28672
-    {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6863.5 GB/s at n=32768
-    {'s', 0, 768, "vr1_u8_r0_w8"},   // 50.9 GB/s at n=512
-    {'s', 0, 1536, "vr1_u2_r0_w8_b0_g9"},   // 191.1 GB/s at n=1024
-    {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 671.5 GB/s at n=2048
-    {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1312.6 GB/s at n=3072
-    {'s', 0, 6144, "vr2_u2_r0_w8_b4_g13"},   // 1990.7 GB/s at n=4096
-    {'s', 0, 10240, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 4060.5 GB/s at n=8192
-    {'s', 0, 14336, "vr2_u2_r0_w8_b4_g11"},   // 5429.0 GB/s at n=12288
-    {'s', 0, 18432, "vr2_u2_r0_w8_b4_g11"},   // 6323.2 GB/s at n=16384
-    {'s', 0, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6480.1 GB/s at n=20480
-    {'s', 0, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6686.4 GB/s at n=24576
-    {'s', 0, 30720, "vr2_u2_r0_w8_b4_g11"},   // 6789.4 GB/s at n=28672
-    {'s', 0, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6879.8 GB/s at n=32768
-    {'d', 1, 1536, "vr4_u2_r0_w8"},   // 255.4 GB/s at n=1024
-    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 740.4 GB/s at n=2048
-    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1338.8 GB/s at n=4096
-    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1889.3 GB/s at n=8192
-    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2124.7 GB/s at n=16384
-    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2174.6 GB/s at n=24576
-    {'d', 0, 1536, "vr4_u2_r0_w8"},   // 253.0 GB/s at n=1024
-    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c16"},   // 734.6 GB/s at n=2048
-    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1342.5 GB/s at n=4096
-    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1896.1 GB/s at n=8192
-    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2120.8 GB/s at n=16384
-    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2180.5 GB/s at n=24576
-    {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13"},   // 339.5 GB/s at n=1024
-    {'c', 1, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1136.7 GB/s at n=2048
-    {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2964.7 GB/s at n=4096
-    {'c', 1, 12288, "vr2_u2_r0_w8_b4_g10"},   // 5249.5 GB/s at n=8192
-    {'c', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6461.3 GB/s at n=16384
-    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 338.1 GB/s at n=1024
-    {'c', 0, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1151.6 GB/s at n=2048
-    {'c', 0, 6144, "vr2_u2_r0_w8_b4_g13"},   // 2973.7 GB/s at n=4096
-    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g11"},   // 5239.4 GB/s at n=8192
-    {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6590.4 GB/s at n=16384
-    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 331.4 GB/s at n=1024
-    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.8 GB/s at n=2048
-    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 907.0 GB/s at n=4096
-    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1062.2 GB/s at n=8192
-    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1100.2 GB/s at n=16384
-    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 343.0 GB/s at n=1024
-    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.5 GB/s at n=2048
-    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 918.2 GB/s at n=4096
-    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1062.9 GB/s at n=8192
-    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1105.4 GB/s at n=16384
-    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.5 GB/s at n=1024
-    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 112.2 GB/s at n=2048
-    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 132.8 GB/s at n=4096
-    {'w', 1, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 149.6 GB/s at n=8192
-    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.5 GB/s at n=1024
-    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 111.4 GB/s at n=2048
-    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 132.5 GB/s at n=4096
-    {'w', 0, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 149.6 GB/s at n=8192
+    {'s', 1, 768, "vr1_u2_r0_w8_b6_g7_c2_f"},   // 48.8 GB/s at n=512
+    {'s', 1, 1536, "vr1_u2_r0_w8_b6_g14"},   // 165.0 GB/s at n=1024
+    {'s', 1, 2560, "vr2_u2_r0_w8_b4_g13"},   // 566.6 GB/s at n=2048
+    {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1199.7 GB/s at n=3072
+    {'s', 1, 6144, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 1820.8 GB/s at n=4096
+    {'s', 1, 10240, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 4075.3 GB/s at n=8192
+    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5388.6 GB/s at n=12288
+    {'s', 1, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6850.1 GB/s at n=16384
+    {'s', 1, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6867.7 GB/s at n=20480
+    {'s', 1, 26624, "vr2_u2_r0_w8_b4_g13"},   // 6874.7 GB/s at n=24576
+    {'s', 1, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6911.6 GB/s at n=28672
+    {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6946.3 GB/s at n=32768
+    {'s', 0, 768, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 49.7 GB/s at n=512
+    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 170.1 GB/s at n=1024
+    {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 616.2 GB/s at n=2048
+    {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1255.2 GB/s at n=3072
+    {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1836.3 GB/s at n=4096
+    {'s', 0, 10240, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 4075.1 GB/s at n=8192
+    {'s', 0, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5407.4 GB/s at n=12288
+    {'s', 0, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6818.0 GB/s at n=16384
+    {'s', 0, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6835.9 GB/s at n=20480
+    {'s', 0, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6888.1 GB/s at n=24576
+    {'s', 0, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6923.5 GB/s at n=28672
+    {'s', 0, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6946.1 GB/s at n=32768
+    {'d', 1, 1536, "vr4_u2_r0_w8_b0_g5_c16"},   // 221.3 GB/s at n=1024
+    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 745.0 GB/s at n=2048
+    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1344.9 GB/s at n=4096
+    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1893.2 GB/s at n=8192
+    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2159.2 GB/s at n=16384
+    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c16"},   // 2197.8 GB/s at n=24576
+    {'d', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 227.4 GB/s at n=1024
+    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 742.5 GB/s at n=2048
+    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1340.2 GB/s at n=4096
+    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1890.7 GB/s at n=8192
+    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2160.5 GB/s at n=16384
+    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 2193.7 GB/s at n=24576
+    {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 337.8 GB/s at n=1024
+    {'c', 1, 3072, "vr2_u2_r0_w8_b4_g10"},   // 1041.8 GB/s at n=2048
+    {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2965.1 GB/s at n=4096
+    {'c', 1, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5203.0 GB/s at n=8192
+    {'c', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6824.6 GB/s at n=16384
+    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g13"},   // 327.8 GB/s at n=1024
+    {'c', 0, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1070.1 GB/s at n=2048
+    {'c', 0, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2960.3 GB/s at n=4096
+    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g13"},   // 5125.4 GB/s at n=8192
+    {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6824.6 GB/s at n=16384
+    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 333.3 GB/s at n=1024
+    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 631.1 GB/s at n=2048
+    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 908.7 GB/s at n=4096
+    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1091.0 GB/s at n=8192
+    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1111.1 GB/s at n=16384
+    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 344.3 GB/s at n=1024
+    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.7 GB/s at n=2048
+    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 918.7 GB/s at n=4096
+    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1092.8 GB/s at n=8192
+    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1113.8 GB/s at n=16384
+    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 78.3 GB/s at n=1024
+    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 112.3 GB/s at n=2048
+    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 133.0 GB/s at n=4096
+    {'w', 1, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 146.0 GB/s at n=8192
+    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.4 GB/s at n=1024
+    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 111.5 GB/s at n=2048
+    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 133.3 GB/s at n=4096
+    {'w', 0, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 146.0 GB/s at n=8192
 };
 // END TUNED TABLE
 

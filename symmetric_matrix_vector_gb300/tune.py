@@ -106,7 +106,11 @@ def measure(xs, kind, uplo, n, variant, reps, prob, cold=False):
 
 
 def load_results(path):
-    done = {}
+    """(kind, uplo, n, variant name) -> record.  A file may hold several
+    measurements of one key (runs on different GPUs of the same model,
+    appended one after another): their times are averaged, so that the
+    choice does not follow one GPU's quirks."""
+    groups = {}
     if path and os.path.exists(path):
         with open(path) as f:
             for line in f:
@@ -114,7 +118,18 @@ def load_results(path):
                     r = json.loads(line)
                 except ValueError:
                     continue
-                done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
+                groups.setdefault((r["kind"], r["uplo"], r["n"], r["variant_name"]), []).append(r)
+    done = {}
+    for key, rs in groups.items():
+        r = dict(rs[-1])
+        r["ms"] = sum(x["ms"] for x in rs) / len(rs)
+        b2b = [x["ms_b2b"] for x in rs if "ms_b2b" in x]
+        if b2b:
+            r["ms_b2b"] = sum(b2b) / len(b2b)
+        r["runs"] = len(rs)
+        tri = r["gbs"] * rs[-1]["ms"]   # stored bytes / 1e6, from the record's own figures
+        r["gbs"] = tri / r["ms"]
+        done[key] = r
     return done
 
 

@@ -46,3 +46,15 @@ def test_choose_breaks_near_ties_by_back_to_back_time():
         done[(r["kind"], r["uplo"], r["n"], r["variant_name"])] = r
     (entry,) = tune.choose(done)
     assert entry[3]["variant_name"] == "b"      # c is fastest back to back but 10 % slower alone
+
+
+def test_results_of_several_runs_are_averaged(tmp_path):
+    import json
+
+    path = tmp_path / "r.jsonl"
+    rows = [rec("w", "L", 8192, 0, "a", 3.6), rec("w", "L", 8192, 1, "b", 3.7),
+            rec("w", "L", 8192, 0, "a", 3.8), rec("w", "L", 8192, 1, "b", 3.7)]
+    path.write_text("".join(json.dumps(r) + "\n" for r in rows))
+    done = tune.load_results(str(path))
+    assert abs(done[("w", "L", 8192, "a")]["ms"] - 3.7) < 1e-12
+    assert done[("w", "L", 8192, "a")]["runs"] == 2
