@@ -308,9 +308,9 @@ KIND_WORKLOADS = {
 
 
 # FP64 issue rate of GB300: the nominal 1.25 TFLOP/s over 152 SMs x 2 flops x
-# 2.07 GHz is 1.99, i.e. 2 FP64 FMAs per clock per SM.  (A loop of nothing but
-# FP64 FMAs reaches 1.68 per clock; the general product on the same loader
-# reaches 1.88, so the unit itself is faster than the plain FMA loop shows.)
+# 2.07 GHz is 1.99, i.e. 2 FP64 FMAs per clock per SM.  A loop of FMAs with
+# register operands reaches it (the same-run probe); DADD, DMUL and FMAs with
+# an immediate operand issue at about 1.68 per clock.
 FP64_PER_CLK_PER_SM = 2
 NOMINAL_SM_MHZ = 2070.0
 
@@ -350,13 +350,13 @@ def measure_kinds(xs, inputs, torch, peaks, reps=10):
                "variant": xs.xsymv_variant_name(kind, xs.xsymv_selected_variant(kind, uplo, n))}
         if f64:
             issue = fp64_issue_peak(torch, peaks.get("sm_max_mhz"))
-            probe = peaks["fp64_tflops"] * 1e12 / 2          # pure-FMA loop, a lower bound
+            probe = peaks["fp64_tflops"] * 1e12 / 2          # register-operand FMA loop, same run
             ach = elems * f64 / (ms * 1e-3)
             rec["roofline"] = {"bound": "alu", "unit": "FP64 inst/s", "achieved": ach,
                                "peak": issue, "frac": ach / issue, "per_element": f64,
                                "peak_source": "%d FP64 FMA/clock/SM x SMs x max SM clock"
                                               % FP64_PER_CLK_PER_SM,
-                               "probe_pure_fma": probe, "frac_of_probe": ach / probe}
+                               "probe_fma": probe, "frac_of_probe": ach / probe}
         else:
             rec["roofline"] = {"bound": "hbm", "unit": "GB/s", "achieved": gbs,
                                "peak": peaks["hbm"], "frac": gbs / peaks["hbm"]}

@@ -293,13 +293,26 @@ XSYMV_API int xsymv_timing_read(int *calls, double *main_ms, double *call_ms);
 /* Roofline denominators measured now on the current device and stream:
  * HBM copy bandwidth (bytes read + written per second, 1 GiB buffers), HBM
  * read bandwidth, and FP64 / FP32 FMA throughput (2 flops per FMA) of a loop
- * of nothing but FMAs, each the best of a few timed runs.  On GB300 the FP64
- * figure is a lower bound: such a loop issues about 1.68 FP64 FMAs per clock
- * per SM, while streaming kernels that mix loads and FP64 FMAs sustain more.
- * Allocates and frees two 1 GiB buffers; synchronises the stream.  Any
- * output pointer may be NULL. */
+ * of nothing but FMAs with register operands, each the best of a few timed
+ * runs.  Allocates and frees two 1 GiB buffers; synchronises the stream.
+ * Any output pointer may be NULL. */
 XSYMV_API int xsymv_probe_peaks(double *copy_gbs, double *read_gbs, double *fp64_tflops,
                                 double *fp32_tflops);
+
+/* The double-double kernels issue every rounded sum, difference and
+ * product of two doubles as a fused multiply-add with a unit operand
+ * (a + b = fma(a, 1, b), a - b = fma(b, -1, a), a * b = fma(a, b, -0)),
+ * which IEEE 754 makes bit-identical to the plain operations and which
+ * GB300 issues faster.  This entry checks that on the current device: for
+ * i < n it writes out[6i .. 6i+5] = a[i]+b[i], a[i]-b[i], a[i]*b[i] by the
+ * plain instructions, then the same three in the kernels' form.  a, b: n
+ * doubles; out: 6n doubles; all device memory, not overlapping.  Enqueued
+ * on the current stream (no synchronisation).  Returns 0, XSYMV_ERR_VALUE
+ * (n < 0, or a NULL pointer with n > 0), XSYMV_ERR_DEVICE or
+ * XSYMV_ERR_CUDA.
+ * No counterpart in the report: it backs the GB300 form of the DD steps. */
+XSYMV_API int xsymv_probe_unit_forms(const double *a, const double *b, double *out,
+                                     long long n);
 
 /* Number of kernels this library has launched since it was loaded. */
 XSYMV_API long long xsymv_launch_count(void);

@@ -31,7 +31,7 @@ __all__ = [
     "xsymv_s_host", "xsymv_d_host", "xhemv_c_host", "xhemv_z_host", "xsymv_w_host", "symv_host",
     "xsymv_host_traffic", "xsymv_sync_status", "xsymv_set_wait_limit", "xsymv_test_stall",
     "xsymv_test_set_call_number",
-    "xsymv_probe_peaks", "xgemv_s", "xgemv_d", "gemv", "xgemv_variant_count",
+    "xsymv_probe_peaks", "xsymv_probe_unit_forms", "xgemv_s", "xgemv_d", "gemv", "xgemv_variant_count",
     "xgemv_variant_name", "xgemv_set_variant", "xgemv_selected_variant",
     "ELEM_BYTES_BY_KIND", "SHARD_ENTRY_POINTS", "REDUCE_ENTRY_POINTS", "symv_shard", "symv_reduce", "xsymv_shard_bounds",
     "xsymv_s_shard", "xsymv_d_shard", "xhemv_c_shard", "xhemv_z_shard", "xsymv_w_shard",
@@ -103,6 +103,8 @@ def load():
         lib.xsymv_sync_status.restype = c_int
         lib.xsymv_probe_peaks.argtypes = [ctypes.POINTER(ctypes.c_double)] * 4
         lib.xsymv_probe_peaks.restype = c_int
+        lib.xsymv_probe_unit_forms.argtypes = [vp, vp, vp, ctypes.c_longlong]
+        lib.xsymv_probe_unit_forms.restype = c_int
         lib.xsymv_set_wait_limit.argtypes = [ctypes.c_ulonglong]
         lib.xsymv_set_wait_limit.restype = c_int
         lib.xsymv_test_stall.argtypes = [c_int]
@@ -372,6 +374,14 @@ def xsymv_probe_peaks():
     v = [ctypes.c_double(0) for _ in range(4)]
     check(load().xsymv_probe_peaks(*[ctypes.byref(x) for x in v]))
     return dict(zip(("copy_gbs", "read_gbs", "fp64_tflops", "fp32_tflops"), (x.value for x in v)))
+
+
+def xsymv_probe_unit_forms(a, b, out, n: int, stream=None) -> int:
+    """out[6i:6i+6] = a+b, a-b, a*b (plain instructions), then the same in the
+    fused multiply-add form the DD kernels use; device tensors of doubles."""
+    lib = load()
+    _use_stream(lib, stream)
+    return lib.xsymv_probe_unit_forms(_ptr(a), _ptr(b), _ptr(out), int(n))
 
 
 def xsymv_set_stream(stream) -> int:

@@ -9,6 +9,7 @@
 
 #include "../../include/xsymv.h"
 #include "xsymv_runtime.h"
+#include "xsymv_scalar.cuh"
 
 namespace xsymv {
 namespace {
@@ -39,16 +40,34 @@ __global__ void probe_read(const uint4* __restrict__ src, size_t n, unsigned* si
   if (acc == 0x9e3779b9u) sink[0] = acc;   // practically never; keeps the loads
 }
 
-// 8 independent FMA chains per thread.  On GB300 a loop of nothing but
-// FP64 FMAs issues at about 1.68 per clock per SM whatever its parallelism,
-// while a memory-streaming FP64 kernel (the general product) sustains 1.88:
-// this is a lower bound of the FP64 rate, not the unit's peak.
+// The multiplier and addend of the FMA probe, read by an opaque load so
+// that they sit in registers: on GB300 an FP64 FMA with an immediate or
+// constant-bank operand (as a compile-time constant becomes) issues at
+// about 1.68 per clock per SM, one with register operands at 2.0, the
+// unit's rate.
+static __device__ double g_probe_bc64[2] = {0.999999, 1e-9};
+static __device__ float g_probe_bc32[2] = {0.999999f, 1e-9f};
+__device__ __forceinline__ double opaque_load(const double* p) {
+  double v;
+  asm("ld.global.nc.f64 %0, [%1];" : "=d"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float opaque_load(const float* p) {
+  float v;
+  asm("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+template <class F> struct ProbeBC;
+template <> struct ProbeBC<double> { __device__ static const double* p() { return g_probe_bc64; } };
+template <> struct ProbeBC<float> { __device__ static const float* p() { return g_probe_bc32; } };
+
+// 8 independent FMA chains per thread, all operands in registers.
 template <class F>
 __global__ void probe_fma(F* out, int iters) {
   F a[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) a[k] = (F)(threadIdx.x + k) * (F)1e-7;
-  const F b = (F)0.999999, c = (F)1e-9;
+  const F b = opaque_load(ProbeBC<F>::p()), c = opaque_load(ProbeBC<F>::p() + 1);
 #pragma unroll 1
   for (int i = 0; i < iters; ++i)
 #pragma unroll
@@ -57,6 +76,23 @@ __global__ void probe_fma(F* out, int iters) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) s += a[k];
   if (s == (F)12345.678) out[0] = s;
+}
+
+// out[6i .. 6i+5] = a+b, a-b, a*b with the plain instructions, then the
+// same three as the DD code issues them (see d_add, d_sub, d_mul)
+__global__ void probe_unit_forms(const double* __restrict__ a, const double* __restrict__ b,
+                                 double* __restrict__ out, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const double x = a[i], y = b[i];
+    double* o = out + 6 * i;
+    o[0] = __dadd_rn(x, y);
+    o[1] = __dsub_rn(x, y);
+    o[2] = __dmul_rn(x, y);
+    o[3] = d_add(x, y);
+    o[4] = d_sub(x, y);
+    o[5] = d_mul(x, y);
+  }
 }
 
 float elapsed(cudaEvent_t a, cudaEvent_t b) {
@@ -136,5 +172,25 @@ extern "C" XSYMV_API int xsymv_probe_peaks(double* copy_gbs, double* read_gbs,
   if (fp64_tflops) *fp64_tflops = best64;
   if (fp32_tflops) *fp32_tflops = best32;
   note_launches(21);
+  return XSYMV_OK;
+}
+
+extern "C" XSYMV_API int xsymv_probe_unit_forms(const double* a, const double* b, double* out,
+                                               long long n) {
+  if (n < 0) return XSYMV_ERR_VALUE;
+  if (n == 0) return XSYMV_OK;
+  if (!a || !b || !out) return XSYMV_ERR_VALUE;
+  int dev = 0, sms = 0;
+  if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
+  cudaStream_t st = current_stream();
+  long long blocks = (n + 255) / 256;
+  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+  probe_unit_forms<<<(unsigned)blocks, 256, 0, st>>>(a, b, out, n);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return XSYMV_ERR_CUDA;
+  }
+  note_launches(1);
   return XSYMV_OK;
 }

@@ -29,8 +29,8 @@ static const TunedEntry kTuned[] = {
     {'s', 1, 26624, "vr2_u2_r0_w8_b4_g13"},   // 6874.7 GB/s at n=24576
     {'s', 1, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6911.6 GB/s at n=28672
     {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6946.3 GB/s at n=32768
-    {'s', 0, 768, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 49.7 GB/s at n=512
-    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 170.1 GB/s at n=1024
+    {'s', 0, 768, "vr1_u2_r0_w8_b6_g5"},   // 48.7 GB/s at n=512
+    {'s', 0, 1536, "vr1_u2_r0_w8_b0_g9"},   // 167.7 GB/s at n=1024
     {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 616.2 GB/s at n=2048
     {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1255.2 GB/s at n=3072
     {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1836.3 GB/s at n=4096
@@ -73,14 +73,14 @@ static const TunedEntry kTuned[] = {
     {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 918.7 GB/s at n=4096
     {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1092.8 GB/s at n=8192
     {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1113.8 GB/s at n=16384
-    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 78.3 GB/s at n=1024
-    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 112.3 GB/s at n=2048
-    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 133.0 GB/s at n=4096
-    {'w', 1, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 146.0 GB/s at n=8192
-    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 77.4 GB/s at n=1024
-    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 111.5 GB/s at n=2048
-    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 133.3 GB/s at n=4096
-    {'w', 0, 2147483647, "vr8_u1_r0_w4_b0_g5_c8"},   // 146.0 GB/s at n=8192
+    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.7 GB/s at n=1024
+    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 126.2 GB/s at n=2048
+    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 152.6 GB/s at n=4096
+    {'w', 1, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.0 GB/s at n=8192
+    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.6 GB/s at n=1024
+    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 125.1 GB/s at n=2048
+    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 154.5 GB/s at n=4096
+    {'w', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.5 GB/s at n=8192
 };
 // END TUNED TABLE
 

@@ -181,7 +181,9 @@ def sweep(kinds, sizes, uplos, results_path, reps_bytes=8e9, only=None):
     return done
 
 
-TIE = 0.01   # variants within 1 % of the fastest isolated call count as equal
+TIE = 0.01        # variants within 1 % of the fastest isolated call count as equal,
+TIE_MS = 0.00025  # or within 0.25 us of it: an eighth of the event timer's ~2 us tick,
+                  # about the spread of a trimmed mean of 60 flushed calls
 
 
 def choose(done, index_of=None):
@@ -189,7 +191,8 @@ def choose(done, index_of=None):
 
     The fastest call decides (an isolated call with the L2 flushed for the
     small triangles, back to back for the large ones); among small-triangle
-    variants within TIE of the fastest, the one fastest back to back wins.
+    variants within TIE (relative) or TIE_MS (absolute) of the fastest, the
+    one fastest back to back wins.
 
     ``index_of`` maps (kind, variant name) to the variant's index in the
     library being tuned; results for names it does not know (variants since
@@ -205,7 +208,7 @@ def choose(done, index_of=None):
     best = {}
     for key, rs in groups.items():
         fastest = min(r["ms"] for r in rs)
-        near = [r for r in rs if r["ms"] <= fastest * (1 + TIE)]
+        near = [r for r in rs if r["ms"] <= max(fastest * (1 + TIE), fastest + TIE_MS)]
         if all("ms_b2b" in r for r in near):
             best[key] = min(near, key=lambda r: (r["ms_b2b"], r["ms"]))
         else:

@@ -206,3 +206,13 @@ def test_shard_bounds_split_evenly():
         xs.xsymv_shard_bounds("Q", 10, 2)
     with pytest.raises(xs.XsymvError):
         xs.xsymv_shard_bounds("U", 10, 0)
+
+
+def test_unit_forms_probe_argument_errors_on_host(lib):
+    """checked before any device work: an empty call succeeds, a negative
+    count or a missing buffer is refused"""
+    import symmetric_matrix_vector_gb300 as xs
+
+    assert xs.xsymv_probe_unit_forms(0, 0, 0, 0) == 0
+    assert xs.xsymv_probe_unit_forms(0, 0, 0, -1) == -4
+    assert xs.xsymv_probe_unit_forms(0, 0, 0, 5) == -4
