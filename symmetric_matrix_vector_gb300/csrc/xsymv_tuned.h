@@ -41,18 +41,18 @@ static const TunedEntry kTuned[] = {
     {'s', 0, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6888.1 GB/s at n=24576
     {'s', 0, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6923.5 GB/s at n=28672
     {'s', 0, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6946.1 GB/s at n=32768
-    {'d', 1, 1536, "vr4_u2_r0_w8_b0_g5_c16"},   // 221.3 GB/s at n=1024
-    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 745.0 GB/s at n=2048
-    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1344.9 GB/s at n=4096
+    {'d', 1, 1536, "vr4_u2_r0_w8_b0_g6"},   // 247.8 GB/s at n=1024
+    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c16"},   // 669.7 GB/s at n=2048
+    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1328.8 GB/s at n=4096
     {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1893.2 GB/s at n=8192
-    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2159.2 GB/s at n=16384
-    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c16"},   // 2197.8 GB/s at n=24576
-    {'d', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 227.4 GB/s at n=1024
-    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 742.5 GB/s at n=2048
-    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1340.2 GB/s at n=4096
-    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1890.7 GB/s at n=8192
-    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2160.5 GB/s at n=16384
-    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 2193.7 GB/s at n=24576
+    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2178.4 GB/s at n=16384
+    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2213.9 GB/s at n=24576
+    {'d', 0, 1536, "vr4_u2_r0_w8"},   // 248.8 GB/s at n=1024
+    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 689.5 GB/s at n=2048
+    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1319.9 GB/s at n=4096
+    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1871.7 GB/s at n=8192
+    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2177.2 GB/s at n=16384
+    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2214.3 GB/s at n=24576
     {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 337.8 GB/s at n=1024
     {'c', 1, 3072, "vr2_u2_r0_w8_b4_g10"},   // 1041.8 GB/s at n=2048
     {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2965.1 GB/s at n=4096
@@ -63,16 +63,16 @@ static const TunedEntry kTuned[] = {
     {'c', 0, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2960.3 GB/s at n=4096
     {'c', 0, 12288, "vr2_u2_r0_w8_b4_g13"},   // 5125.4 GB/s at n=8192
     {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6824.6 GB/s at n=16384
-    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 333.3 GB/s at n=1024
-    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 631.1 GB/s at n=2048
-    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 908.7 GB/s at n=4096
-    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1091.0 GB/s at n=8192
-    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1111.1 GB/s at n=16384
-    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 344.3 GB/s at n=1024
-    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.7 GB/s at n=2048
-    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 918.7 GB/s at n=4096
-    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1092.8 GB/s at n=8192
-    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1113.8 GB/s at n=16384
+    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 327.9 GB/s at n=1024
+    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.2 GB/s at n=2048
+    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 916.3 GB/s at n=4096
+    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1099.0 GB/s at n=8192
+    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1119.8 GB/s at n=16384
+    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 335.9 GB/s at n=1024
+    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 630.0 GB/s at n=2048
+    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8"},   // 923.0 GB/s at n=4096
+    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1101.0 GB/s at n=8192
+    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1121.9 GB/s at n=16384
     {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.7 GB/s at n=1024
     {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 126.2 GB/s at n=2048
     {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 152.6 GB/s at n=4096
