@@ -478,6 +478,46 @@ def test_chained_calls_read_previous_result(lib, kind):
     assert bool((chained == waited).all())
 
 
+@pytest.mark.parametrize("kind", ["s", "d", "c", "w"])
+def test_caller_kernels_between_calls_are_ordered(lib, kind):
+    """An iterative method: each step's x is rebuilt from the previous
+    product by the caller's own kernels on the same stream (a slow one on a
+    large buffer, then the write of x), and the next call reads it.  A main
+    kernel that starts streaming early must still see every byte those
+    kernels wrote: the loop enqueued without host waits gives the bytes of
+    the same loop with the host waiting after every step."""
+    import torch
+
+    n = 3000 if kind != "w" else 900
+    al, _ = SCAL[kind]
+    p = inputs.make_problem(kind, "U", n, lda=n + 4, alpha=al, beta=0.0, seed=99)
+    dp = DeviceProblem(p)
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+    big = torch.ones(64 << 20, dtype=torch.float32, device="cuda")   # 256 MB
+    es = inputs.ELEM_BYTES[kind]
+    dt = torch.float32 if kind in "sc" else torch.float64
+
+    def iterate(sync):
+        x = dp.x.clone()
+        y = torch.zeros_like(x)
+        for k in range(6):
+            st = lib.symv(kind, "U", n, al, dp.A, p.lda, x, 1, 0.0, y, 1)
+            assert st == 0
+            # the caller's kernels: a slow pass over 256 MB, then x := y / 4 + 1 + k,
+            # written element by element as the real components of the kind
+            s = (big * 1.0000001).sum() * 0.0
+            xv, yv = x.view(dt), y.view(dt)
+            xv.copy_(yv * 0.25 + s.to(dt) + (1.0 + k))
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return x.clone(), y.clone()
+
+    waited = iterate(True)
+    chained = iterate(False)
+    assert bool((waited[0] == chained[0]).all()) and bool((waited[1] == chained[1]).all())
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_one_launch_variants_barrier_timeout(lib, kind):
     """The one-launch ("_f") variants meet at a grid barrier with a bounded
