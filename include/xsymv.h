@@ -321,7 +321,7 @@ XSYMV_API long long xsymv_launch_count(void);
 
 /* kind: 's', 'd', 'c', 'z' or 'w'.  Number of compiled variants (0 for an
  * unknown kind) and the name of variant index: "vr<VR>_u<U>_<p><S>_w<W>"
- * with optional suffixes "_b<B>", "_x<X>", "_g<G>", "_c<R>", "_tk" =
+ * with optional suffixes "_b<B>", "_x<X>", "_g<G>", "_c<R>", "_tk", "_f" =
  * 16-byte vectors per lane (the tile edge is 32 lanes x VR vectors),
  * columns per load step, how off-diagonal columns reach the arithmetic
  * (p = r: 16-byte loads into registers; t: a per-warp shared-memory ring of
@@ -332,8 +332,15 @@ XSYMV_API long long xsymv_launch_count(void);
  * tickets in the same launch (the report's mechanism, §2.1, figures
  * "kernel" and "Atomic": dynamic block IDs, one ticket per chunk of NB
  * outputs passed from contributor to contributor in a fixed order) instead
- * of by a second, fixed-order reduction kernel.  Both are bit-identical from
- * run to run; their results differ from each other only in rounding. */
+ * of by a second, fixed-order reduction kernel, and "_f": the fixed-order
+ * sums in the same launch, after a grid-wide barrier (one launch per call,
+ * the same sums as the two-kernel path of the same plan).  A tuned "_f"
+ * variant gives way to its two-kernel twin (the same name without "_f")
+ * while calls on a stream run back to back, since two-kernel calls fill
+ * each other's tails; the twin runs the same plan, so the results are the
+ * same bytes.  A forced variant (xsymv_set_variant) is always used as is.
+ * All are bit-identical from run to run; "_tk" results differ from the
+ * others only in rounding. */
 XSYMV_API int xsymv_variant_count(char kind);
 XSYMV_API const char *xsymv_variant_name(char kind, int index);
 

@@ -71,6 +71,9 @@ struct MainArgs {
   // previous call's finaliser) completes; it waits for it at its end, and
   // notes its start time in the workspace header
   int early;
+  // one-launch variants: the header words of the back-to-back bookkeeping
+  // (all null: none)
+  OverlapWords ow;
 };
 
 // One compiled configuration of the main kernel.
@@ -233,10 +236,10 @@ cudaError_t launch_fused(const MainArgs<T>& a) {
   if (a.aligned)
     return cudaLaunchKernelEx(&cfg, symv_fused<T, VR, U, WARPS, true, MB, R>, a.plan, a.A, a.lda,
                               a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, stall,
-                              bar, f);
+                              bar, f, a.ow);
   return cudaLaunchKernelEx(&cfg, symv_fused<T, VR, U, WARPS, false, MB, R>, a.plan, a.A, a.lda,
                             a.x, a.incx, a.Wc, a.Wr, a.wt, a.rt, a.status, a.epoch, limit, stall,
-                            bar, f);
+                            bar, f, a.ow);
 }
 
 template <class T, int VR, int U, int WARPS, int MB, int R>
@@ -420,7 +423,36 @@ struct Workload {
   long long wr_off;     // byte offset of Wr
   long long v_off;      // byte offset of v (ordered-ticket variants)
   long long bytes;      // total workspace bytes
+  int twin;             // one-launch variant: its two-kernel twin (the same kernel code
+                        // without the final merge), which runs this plan in one wave,
+                        // else -1
 };
+
+// The two-kernel variant of a one-launch variant: the same name without
+// "_f" (and without "_c<R>" when R is U, the default), -1 if there is none.
+template <class T>
+int twin_index(const Variant<T>* table, int count, int vi) {
+  const char* nm = table[vi].name;
+  const size_t len = strlen(nm);
+  char buf[96];
+  if (table[vi].accum != kAccumFused || len < 3 || len - 2 >= sizeof(buf) ||
+      strcmp(nm + len - 2, "_f") != 0)
+    return -1;
+  memcpy(buf, nm, len - 2);
+  buf[len - 2] = '\0';
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int i = 0; i < count; ++i)
+      if (table[i].accum == kAccumWorkspace && strcmp(table[i].name, buf) == 0) return i;
+    // "_c<R>" with R = U names the default reduction: the twin omits it
+    const char* u = strstr(buf, "_u");
+    char* c = strrchr(buf, '_');
+    if (pass == 0 && u != nullptr && c != nullptr && c[1] == 'c' && atoi(c + 2) == atoi(u + 2))
+      *c = '\0';
+    else
+      break;
+  }
+  return -1;
+}
 
 // The variant a call uses: the forced one, else the tuned entry's variant,
 // looked up by name in this kind's table (once per entry, then cached); 0 if
@@ -498,9 +530,14 @@ int plan_call_uncached(const Variant<T>* table, int count, char kind, int upper,
   out->wr_off = out->wc_off + align_up(plan_wc_elems(out->plan) * (long long)sizeof(T), 256);
   out->v_off = out->wr_off + align_up(plan_wr_elems(out->plan) * (long long)sizeof(T), 256);
   out->bytes = out->v_off;
+  out->twin = -1;
   if (v->accum == kAccumTickets) {
     if (out->plan.W >= (1 << kTkIdBits)) return XSYMV_ERR_VALUE;
     out->bytes += align_up((long long)n * (long long)sizeof(T), 256);
+  }
+  if (v->accum == kAccumFused) {
+    const int t = twin_index(table, count, vi);
+    if (t >= 0 && table[t].ctas_per_sm() >= v->ctas_per_sm()) out->twin = t;
   }
   return XSYMV_OK;
 }
@@ -542,6 +579,14 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   Workload<T> wl;
   int status = plan_call(table, count, kind, upper, n, &wl);
   if (status) return status;
+  // back-to-back calls (the stream's flag, see OverlapWords): a tuned
+  // one-launch variant gives way to its two-kernel twin, whose calls fill
+  // each other's tails.  The twin runs this very plan (its main kernel takes
+  // any grid), so the partial sums, their order and the results are the same.
+  int* report = nullptr;
+  const volatile int* seen = overlap_flag(st, &report);   // null if unavailable
+  if (wl.twin >= 0 && forced_variant(kind) < 0 && seen != nullptr && *seen == 1)
+    wl.variant = &table[wl.twin];
   int epoch = 0;
   size_t cap = 0;
   // two sets of partial sums: calls of even number use the one after the
@@ -563,8 +608,13 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
                 st};
   status = ensure_tables(wl.plan, st, &m.wt, &m.rt);
   if (status) return status;
+  // overlap bookkeeping in the header: end times of the calls' last kernels
+  // and main-kernel start times, one word each per call parity
+  unsigned long long* hw = reinterpret_cast<unsigned long long*>(ws + kOverlapOffset);
+  const int q = epoch & 1;
   if (wl.variant->accum == kAccumFused) {
     // one launch: the kernel also applies y = alpha*s + beta*y
+    m.ow = OverlapWords{hw + q, nullptr, hw + (1 - q), report};
     m.alpha = alpha;
     m.beta = beta;
     m.mode = bz ? kBetaZero : kFull;
@@ -614,12 +664,6 @@ int symv_entry(const Variant<T>* table, int count, char kind, char uplo, int n, 
   const uintptr_t y_lo = reinterpret_cast<uintptr_t>(y);
   const uintptr_t y_hi = y_lo + ((uintptr_t)(n - 1) * (uintptr_t)(incy < 0 ? -incy : incy) + 1) * es;
   m.early = may_start_early(st, a_lo, a_hi, x_lo, x_hi) ? 1 : 0;
-  // overlap bookkeeping in the header: finaliser end times and main-kernel
-  // start times, one word each per call parity
-  unsigned long long* hw = reinterpret_cast<unsigned long long*>(ws + kOverlapOffset);
-  const int q = epoch & 1;
-  int* report = nullptr;
-  const volatile int* seen = overlap_flag(st, &report);   // null if unavailable
   OverlapWords ow{hw + q, hw + 2 + q, hw + (1 - q), m.early ? report : nullptr};
   const bool compact = m.early && seen != nullptr && *seen == 1;
   timing_begin(st);

@@ -41,6 +41,15 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, int epoch,
   }
 }
 
+// A one-launch kernel that begins less than this after the previous call
+// on its stream ended ran back to back with it: the two calls were queued
+// together, with no other kernel between them.  (Measured on GB300: a
+// cooperative grid queued behind another begins 2.4-4.7 us after the last
+// block of the one before it ends; a kernel of the caller in between adds
+// its own two launch gaps and its run time.  A wrong answer costs only
+// speed, and the next call's report corrects it.)
+constexpr unsigned long long kBackToBackNs = 6000;
+
 // the final merge's arguments (as for symv_finalize)
 template <class T>
 struct FinalArgs {
@@ -55,7 +64,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB)
 symv_fused(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__ x, int incx,
            T* __restrict__ Wc, T* __restrict__ Wr, const int4* __restrict__ wt,
            const int2* __restrict__ rt, int* status, int epoch, unsigned long long limit_ns,
-           int stall, unsigned long long* bar, FinalArgs<T> f) {
+           int stall, unsigned long long* bar, FinalArgs<T> f, OverlapWords ow) {
   static_assert(WARPS * 32 == kFinParts * kFinCols, "one finaliser block per thread block");
   constexpr int NB = WarpTile<T, VR, U>::NB;
   __shared__ RowBuffers<T, NB, WARPS> rb;
@@ -65,11 +74,20 @@ symv_fused(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__
   const int w = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   if (lane < 2) rb.row[wl][lane] = -1;
   __syncwarp();
+  const bool reporter = ow.report != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+  const unsigned long long began = reporter ? global_ns() : 0;
   // launched as a programmatic dependent of the stream's previous kernel:
   // nothing of global memory is touched before that kernel has completed.
   // (This grid lets its own dependents start only after the barrier below,
   // so that their blocks cannot take the places this grid's blocks need.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // did this call follow the previous one back to back?  (The host reads the
+  // answer when it enqueues later calls, and then prefers the two-kernel
+  // twin of this variant, whose calls fill each other's tails.)
+  if (reporter) {
+    const unsigned long long prev = *reinterpret_cast<const volatile unsigned long long*>(ow.prev_end);
+    *reinterpret_cast<volatile int*>(ow.report) = began < prev + kBackToBackNs ? 1 : 0;
+  }
   if (w < p.W) {
     Ring rg{0u, 0u, 0, 0u, 0u};
     stream_warp<T, VR, U, 1, false, ALIGNED, R, WARPS>(p, w, wl, blockIdx.x, lane, rg, A, lda, x,
@@ -96,6 +114,8 @@ symv_fused(Plan p, const T* __restrict__ A, long long lda, const T* __restrict__
                                  epoch, fb, part);
     __syncthreads();
   }
+  // the time the grid's last block ends (a reduction nobody waits for)
+  if (ow.end != nullptr && threadIdx.x == 0) atomicMax(ow.end, global_ns());
 }
 
 }  // namespace xsymv

@@ -897,10 +897,13 @@ __device__ __forceinline__ void finalize_outputs(const Plan& p, const T* Wc, con
 }
 
 // Words of the stream workspace's header through which back-to-back calls
-// learn whether they overlap (all null: not used): `end` receives this
-// finaliser's end time; when `report` is set, this call's main kernel
-// started early, `start` holds its start time and `prev_end` the previous
-// finaliser's end time, and *report (host-mapped) gets 1 if they overlapped.
+// learn whether they overlap (all null: not used): `end` receives the end
+// time of this call's last kernel (finaliser, or one-launch kernel); when
+// `report` is set, `prev_end` holds the previous call's end time and
+// *report (host-mapped) gets 1 if this call ran back to back with it: for a
+// finaliser, its call's main kernel started early and `start` holds that
+// start time, which must precede `prev_end`; a one-launch kernel compares
+// its own start with `prev_end` (kBackToBackNs).
 struct OverlapWords {
   unsigned long long* end;
   const unsigned long long* start;

@@ -478,6 +478,55 @@ def test_chained_calls_read_previous_result(lib, kind):
     assert bool((chained == waited).all())
 
 
+@pytest.mark.parametrize("kind,n", [("s", 8192), ("d", 4096), ("z", 2048), ("w", 2048)])
+def test_one_launch_gives_way_to_its_twin_back_to_back(lib, kind, n):
+    """At sizes where the tuned variant is a one-launch kernel, isolated
+    calls run in one launch each; calls that run back to back (the GPU never
+    idle between them) switch to the variant's two-kernel twin, whose calls
+    fill each other's tails, and isolated calls switch back.  Both compute the
+    same plan's sums in the same order: every call gives the same bytes."""
+    import torch
+
+    name = lib.xsymv_variant_name(kind, lib.xsymv_selected_variant(kind, "U", n))
+    if not name.endswith("_f"):
+        pytest.skip("the tuned variant at this size is not a one-launch one: " + name)
+    al, _ = SCAL[kind]
+    p = inputs.make_problem(kind, "U", n, lda=n, alpha=al, beta=0.0, seed=n)
+    dp = DeviceProblem(p)
+    es = inputs.ELEM_BYTES[kind]
+    assert lib.xsymv_set_stream(torch.cuda.current_stream().cuda_stream) == 0
+    ref = torch.zeros(n * es, dtype=torch.uint8, device="cuda")
+    assert lib.symv(kind, "U", n, al, dp.A, n, dp.x, 1, 0.0, ref, 1) == 0
+    torch.cuda.synchronize()
+
+    def isolated(k):
+        c0 = lib.xsymv_launch_count()
+        for _ in range(k):
+            y = torch.zeros_like(ref)
+            assert lib.symv(kind, "U", n, al, dp.A, n, dp.x, 1, 0.0, y, 1) == 0
+            torch.cuda.synchronize()
+            assert bool((y == ref).all())
+        return lib.xsymv_launch_count() - c0
+
+    isolated(2)
+    assert isolated(4) == 4                       # one launch per isolated call
+    calls = 40
+    ys = torch.zeros((calls, n * es), dtype=torch.uint8, device="cuda")
+    ev = [torch.cuda.Event() for _ in range(calls)]
+    c0 = lib.xsymv_launch_count()
+    for i in range(calls):
+        if i >= 4:
+            ev[i - 4].synchronize()               # four calls queued: the GPU is never idle
+        assert lib.symv(kind, "U", n, al, dp.A, n, dp.x, 1, 0.0, ys[i], 1) == 0
+        ev[i].record()
+    torch.cuda.synchronize()
+    launched = lib.xsymv_launch_count() - c0
+    assert launched >= calls + calls // 2, launched   # most calls ran as two kernels
+    assert bool((ys == ref.unsqueeze(0)).all())
+    isolated(2)                                   # (the first may still be a twin)
+    assert isolated(4) == 4
+
+
 @pytest.mark.parametrize("kind", ["s", "d", "c", "w"])
 def test_caller_kernels_between_calls_are_ordered(lib, kind):
     """An iterative method: each step's x is rebuilt from the previous
