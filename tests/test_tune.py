@@ -58,3 +58,16 @@ def test_results_of_several_runs_are_averaged(tmp_path):
     done = tune.load_results(str(path))
     assert abs(done[("w", "L", 8192, "a")]["ms"] - 3.7) < 1e-12
     assert done[("w", "L", 8192, "a")]["runs"] == 2
+
+
+def test_choose_counts_sub_quarter_microsecond_gaps_as_ties():
+    """small calls: 12.34 against 12.52 us is 1.5 % apart but under 0.25 us
+    (below the event timer's resolution): back to back decides; 0.3 us
+    apart is a real difference"""
+    a = dict(rec("s", "L", 1024, 0, "one_launch", 0.01234), ms_b2b=0.0100)
+    b = dict(rec("s", "L", 1024, 1, "two_kernels", 0.01252), ms_b2b=0.0045)
+    best = tune.choose({("s", "L", 1024, r["variant_name"]): r for r in (a, b)})
+    assert best[0][3]["variant_name"] == "two_kernels"
+    c = dict(rec("s", "L", 1024, 1, "two_kernels", 0.01264), ms_b2b=0.0045)
+    best = tune.choose({("s", "L", 1024, r["variant_name"]): r for r in (a, c)})
+    assert best[0][3]["variant_name"] == "one_launch"
