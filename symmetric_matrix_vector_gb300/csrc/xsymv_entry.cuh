@@ -57,23 +57,23 @@ struct MainArgs {
   cudaStream_t stream;
   // ordered-ticket and one-launch (fused) variants: the final merge happens
   // in the same launch
-  T* v;                       // n running sums (in the workspace, after Wr; tickets)
-  void* tk;                   // ticket buffer (counters, then the tickets)
-  unsigned long long call;    // the call's number in the tickets
-  T alpha, beta;
-  int mode;                   // kFull, kBetaZero (or, fused, kPartial)
-  T* y0;                      // logical element 0 of y
-  long long incy;
+  T* v = nullptr;                  // n running sums (in the workspace, after Wr; tickets)
+  void* tk = nullptr;              // ticket buffer (counters, then the tickets)
+  unsigned long long call = 0;     // the call's number in the tickets
+  T alpha{}, beta{};
+  int mode = 0;                    // kFull, kBetaZero (or, fused, kPartial)
+  T* y0 = nullptr;                 // logical element 0 of y
+  long long incy = 0;
   // the plan's warp and row tables (built before the launch)
-  const int4* wt;
-  const int2* rt;
+  const int4* wt = nullptr;
+  const int2* rt = nullptr;
   // the main kernel may stream before the stream's previous kernel (the
   // previous call's finaliser) completes; it waits for it at its end, and
   // notes its start time in the workspace header
-  int early;
+  int early = 0;
   // one-launch variants: the header words of the back-to-back bookkeeping
   // (all null: none)
-  OverlapWords ow;
+  OverlapWords ow{nullptr, nullptr, nullptr, nullptr};
 };
 
 // One compiled configuration of the main kernel.
@@ -270,7 +270,8 @@ int ctas_per_sm_fused() {
 #define XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, G, SUF)                              \
   Variant<T> {                                                                            \
     "vr" #VR "_u" #U "_" L #S "_w" #W SUF, 32 * Ops<T>::VPL * (VR), (W), (S), (P), (X),  \
-        (G), &launch_main<T, VR, U, S, P, W, MB>, &ctas_per_sm<T, VR, U, S, P, W, MB>     \
+        (G), &launch_main<T, VR, U, S, P, W, MB>, &ctas_per_sm<T, VR, U, S, P, W, MB>,    \
+        kAccumWorkspace                                                                   \
   }
 #define XSYMV_VARIANT_P(T, VR, U, S, P, L, W, MB, X, SUF) \
   XSYMV_VARIANT_G(T, VR, U, S, P, L, W, MB, X, DiagCost<T>::v, SUF)
@@ -290,7 +291,7 @@ int ctas_per_sm_fused() {
   Variant<T> {                                                                              \
     "vr" #VR "_u" #U "_r0_w" #W "_b" #MB "_g" #G "_c" #R, 32 * Ops<T>::VPL * (VR), (W), 0,    \
         kPipeRegisters, 1, (G), &launch_main<T, VR, U, 0, kPipeRegisters, W, MB, R>,           \
-        &ctas_per_sm<T, VR, U, 0, kPipeRegisters, W, MB, R>                                   \
+        &ctas_per_sm<T, VR, U, 0, kPipeRegisters, W, MB, R>, kAccumWorkspace                  \
   }
 
 // ordered tickets (register path): diagonal cost G, batched reductions R
@@ -482,7 +483,7 @@ int pick_variant(const Variant<T>* table, int count, char kind, int upper, int n
 // c0 <= j < c1 (a shard; c1 < 0: n).  The variant is the one tuned for a
 // whole triangle of order n_pick (default n).
 template <class T>
-int plan_call_uncached(const Variant<T>* table, int count, char kind, int upper, int n,
+int plan_call_uncached(const Variant<T>* table, int count, int upper, int n,
                        Workload<T>* out, int c0, int c1, int vi);
 
 // The last few plans of this thread, by (table, device, triangle, n, window,
@@ -509,7 +510,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
         *out = e.wl;
         return XSYMV_OK;
       }
-  const int status = plan_call_uncached(table, count, kind, upper, n, out, c0, c1, vi);
+  const int status = plan_call_uncached(table, count, upper, n, out, c0, c1, vi);
   if (status == XSYMV_OK && dev >= 0) {
     cache[next] = Entry{table, dev, upper, n, c0, cc1, vi, *out};
     next = (next + 1) % kSlots;
@@ -518,7 +519,7 @@ int plan_call(const Variant<T>* table, int count, char kind, int upper, int n, W
 }
 
 template <class T>
-int plan_call_uncached(const Variant<T>* table, int count, char kind, int upper, int n,
+int plan_call_uncached(const Variant<T>* table, int count, int upper, int n,
                        Workload<T>* out, int c0, int c1, int vi) {
   int dev = 0, sms = 0;
   if (!current_device(&dev, &sms)) return XSYMV_ERR_DEVICE;
