@@ -23,14 +23,14 @@ static const TunedEntry kTuned[] = {
     {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1199.7 GB/s at n=3072
     {'s', 1, 6144, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 1820.8 GB/s at n=4096
     {'s', 1, 10240, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 4075.3 GB/s at n=8192
-    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5388.6 GB/s at n=12288
+    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 5354.7 GB/s at n=12288
     {'s', 1, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6850.1 GB/s at n=16384
     {'s', 1, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6867.7 GB/s at n=20480
     {'s', 1, 26624, "vr2_u2_r0_w8_b4_g13"},   // 6874.7 GB/s at n=24576
     {'s', 1, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6911.6 GB/s at n=28672
     {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6946.3 GB/s at n=32768
-    {'s', 0, 768, "vr1_u2_r0_w8_b6_g5"},   // 48.7 GB/s at n=512
-    {'s', 0, 1536, "vr1_u2_r0_w8_b0_g9"},   // 167.7 GB/s at n=1024
+    {'s', 0, 768, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 49.7 GB/s at n=512
+    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 170.1 GB/s at n=1024
     {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 616.2 GB/s at n=2048
     {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1255.2 GB/s at n=3072
     {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1836.3 GB/s at n=4096
@@ -50,7 +50,7 @@ static const TunedEntry kTuned[] = {
     {'d', 0, 1536, "vr4_u2_r0_w8"},   // 248.8 GB/s at n=1024
     {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 689.5 GB/s at n=2048
     {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1319.9 GB/s at n=4096
-    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1871.7 GB/s at n=8192
+    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1889.1 GB/s at n=8192
     {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2177.2 GB/s at n=16384
     {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2214.3 GB/s at n=24576
     {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 337.8 GB/s at n=1024
@@ -58,10 +58,10 @@ static const TunedEntry kTuned[] = {
     {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2965.1 GB/s at n=4096
     {'c', 1, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5203.0 GB/s at n=8192
     {'c', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6824.6 GB/s at n=16384
-    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g13"},   // 327.8 GB/s at n=1024
+    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 329.8 GB/s at n=1024
     {'c', 0, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1070.1 GB/s at n=2048
     {'c', 0, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2960.3 GB/s at n=4096
-    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g13"},   // 5125.4 GB/s at n=8192
+    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5168.5 GB/s at n=8192
     {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6824.6 GB/s at n=16384
     {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 327.9 GB/s at n=1024
     {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 632.2 GB/s at n=2048

@@ -186,13 +186,27 @@ TIE_MS = 0.00025  # or within 0.25 us of it: an eighth of the event timer's ~2 u
                   # about the spread of a trimmed mean of 60 flushed calls
 
 
+def twin_name(name):
+    """the two-kernel twin of a one-launch variant name ("..._f"): the name
+    without "_f", and without "_c<R>" when R is U (the default); the
+    library runs it for back-to-back calls.  None for other names."""
+    if not name.endswith("_f"):
+        return None
+    base = name[:-2]
+    m = re.match(r"vr\d+_u(\d+)_.*_c(\d+)$", base)
+    if m and m.group(1) == m.group(2):
+        return [base, base[: base.rindex("_c")]]
+    return [base]
+
+
 def choose(done, index_of=None):
     """best variant per (kind, uplo, n) -> table entries with n_max buckets.
 
     The fastest call decides (an isolated call with the L2 flushed for the
     small triangles, back to back for the large ones); among small-triangle
     variants within TIE (relative) or TIE_MS (absolute) of the fastest, the
-    one fastest back to back wins.
+    one fastest back to back wins, a one-launch variant counting its
+    two-kernel twin's time there (the library runs the twin back to back).
 
     ``index_of`` maps (kind, variant name) to the variant's index in the
     library being tuned; results for names it does not know (variants since
@@ -207,6 +221,17 @@ def choose(done, index_of=None):
         groups.setdefault((kind, uplo, n), []).append(r)
     best = {}
     for key, rs in groups.items():
+        # back to back, a one-launch variant runs as its two-kernel twin
+        by_name = {r["variant_name"]: r for r in rs}
+
+        def effective(r):
+            for t in twin_name(r["variant_name"]) or []:
+                tr = by_name.get(t)
+                if tr is not None and "ms_b2b" in tr and "ms_b2b" in r:
+                    return dict(r, ms_b2b=min(r["ms_b2b"], tr["ms_b2b"]))
+            return r
+
+        rs = [effective(r) for r in rs]
         fastest = min(r["ms"] for r in rs)
         near = [r for r in rs if r["ms"] <= max(fastest * (1 + TIE), fastest + TIE_MS)]
         if all("ms_b2b" in r for r in near):

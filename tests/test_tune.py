@@ -71,3 +71,19 @@ def test_choose_counts_sub_quarter_microsecond_gaps_as_ties():
     c = dict(rec("s", "L", 1024, 1, "two_kernels", 0.01264), ms_b2b=0.0045)
     best = tune.choose({("s", "L", 1024, r["variant_name"]): r for r in (a, c)})
     assert best[0][3]["variant_name"] == "one_launch"
+
+
+def test_one_launch_variant_counts_its_twin_back_to_back():
+    """the library runs a one-launch variant's two-kernel twin for
+    back-to-back calls, so the tie-break charges it the twin's time"""
+    assert tune.twin_name("vr2_u2_r0_w8_b4_g12_c2_f") == ["vr2_u2_r0_w8_b4_g12_c2",
+                                                          "vr2_u2_r0_w8_b4_g12"]
+    assert tune.twin_name("vr4_u2_r0_w8_b0_g5_c8_f") == ["vr4_u2_r0_w8_b0_g5_c8"]
+    assert tune.twin_name("vr4_u2_r0_w8_b0_g5_c8") is None
+    one = dict(rec("s", "L", 1024, 0, "vr1_u2_r0_w8_b6_g11_c2_f", 0.01234), ms_b2b=0.0100)
+    twin = dict(rec("s", "L", 1024, 1, "vr1_u2_r0_w8_b6_g11", 0.01270), ms_b2b=0.0044)
+    other = dict(rec("s", "L", 1024, 2, "vr1_u2_r0_w8_b0_g9", 0.01252), ms_b2b=0.0045)
+    done = {("s", "L", 1024, r["variant_name"]): r for r in (one, twin, other)}
+    (entry,) = tune.choose(done)
+    assert entry[3]["variant_name"] == "vr1_u2_r0_w8_b6_g11_c2_f"
+    assert one["ms_b2b"] == 0.0100          # the caller's records are not changed
