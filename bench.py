@@ -544,11 +544,12 @@ def run_reference(args):
         oracle_block_call(o, p.A, p.lda, p.x, p.y, ns)
     el = time.perf_counter() - t0
     value = flops(ns) * args.steps / el / 1e9
-    what = ("the whole matrix" if ns == n else
-            "its leading %d-by-%d principal block (a bounded sample)" % (ns, ns))
+    what = ("the workload's whole matrix" if ns == n else
+            "the leading %d-by-%d principal block of the workload's matrix (a bounded sample)"
+            % (ns, ns))
     sample = ("each step: the oracle's three-part SSYMV (binary64 accumulator), single-threaded, "
-              "on %s of the workload's matrix (host recipe: numpy PCG64, seed n; generated in "
-              "%.1f s before the timed steps)" % (what, t_gen))
+              "on %s (host recipe: numpy PCG64, seed n; generated in %.1f s before the timed "
+              "steps)" % (what, t_gen))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
