@@ -478,7 +478,7 @@ def test_chained_calls_read_previous_result(lib, kind):
     assert bool((chained == waited).all())
 
 
-@pytest.mark.parametrize("kind,n", [("s", 8192), ("d", 4096), ("z", 2048), ("w", 2048)])
+@pytest.mark.parametrize("kind,n", [("s", 8192), ("d", 4096), ("z", 2048), ("w", 1024)])
 def test_one_launch_gives_way_to_its_twin_back_to_back(lib, kind, n):
     """At sizes where the tuned variant is a one-launch kernel, isolated
     calls run in one launch each; calls that run back to back (the GPU never
