@@ -17,70 +17,70 @@ struct TunedEntry {
 
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
-    {'s', 1, 768, "vr1_u2_r0_w8_b6_g7"},   // 47.2 GB/s at n=512
-    {'s', 1, 1536, "vr1_u2_r0_w8_b6_g14"},   // 164.6 GB/s at n=1024
-    {'s', 1, 2560, "vr2_u2_r0_w8_b4_g13"},   // 565.8 GB/s at n=2048
-    {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1173.7 GB/s at n=3072
-    {'s', 1, 6144, "vr1_u2_r0_w8_b6_g14"},   // 1778.6 GB/s at n=4096
-    {'s', 1, 10240, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 4019.0 GB/s at n=8192
-    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5403.0 GB/s at n=12288
-    {'s', 1, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6891.8 GB/s at n=16384
-    {'s', 1, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6903.0 GB/s at n=20480
-    {'s', 1, 26624, "vr2_u2_r0_w8_b4_g13"},   // 6918.3 GB/s at n=24576
-    {'s', 1, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6959.4 GB/s at n=28672
-    {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6992.5 GB/s at n=32768
-    {'s', 0, 768, "vr1_u2_r0_w8"},   // 48.6 GB/s at n=512
-    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 167.7 GB/s at n=1024
-    {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 625.0 GB/s at n=2048
-    {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1260.6 GB/s at n=3072
-    {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1853.6 GB/s at n=4096
-    {'s', 0, 10240, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 4030.1 GB/s at n=8192
-    {'s', 0, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5401.2 GB/s at n=12288
-    {'s', 0, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6853.1 GB/s at n=16384
-    {'s', 0, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6874.0 GB/s at n=20480
-    {'s', 0, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6935.2 GB/s at n=24576
-    {'s', 0, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6965.4 GB/s at n=28672
-    {'s', 0, 2147483647, "vr2_u2_r0_w8_b4_g11"},   // 6987.8 GB/s at n=32768
-    {'d', 1, 1536, "vr4_u2_r0_w8_b0_g6"},   // 245.8 GB/s at n=1024
-    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 679.9 GB/s at n=2048
-    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1322.5 GB/s at n=4096
-    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1886.3 GB/s at n=8192
-    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2179.1 GB/s at n=16384
-    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2215.1 GB/s at n=24576
+    {'s', 1, 768, "vr1_u2_r0_w8_b6_g7"},   // 47.6 GB/s at n=512
+    {'s', 1, 1536, "vr1_u2_r0_w8_b6_g14"},   // 164.3 GB/s at n=1024
+    {'s', 1, 2560, "vr2_u2_r0_w8_b4_g13"},   // 565.9 GB/s at n=2048
+    {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1179.8 GB/s at n=3072
+    {'s', 1, 6144, "vr1_u2_r0_w8_b6_g14"},   // 1776.0 GB/s at n=4096
+    {'s', 1, 10240, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 4016.5 GB/s at n=8192
+    {'s', 1, 14336, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 5329.5 GB/s at n=12288
+    {'s', 1, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6877.7 GB/s at n=16384
+    {'s', 1, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6891.1 GB/s at n=20480
+    {'s', 1, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6905.8 GB/s at n=24576
+    {'s', 1, 30720, "vr2_u2_r0_w8_b4_g11"},   // 6941.3 GB/s at n=28672
+    {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6975.5 GB/s at n=32768
+    {'s', 0, 768, "vr1_u2_r0_w8"},   // 48.5 GB/s at n=512
+    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 166.7 GB/s at n=1024
+    {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 628.4 GB/s at n=2048
+    {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1260.0 GB/s at n=3072
+    {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1844.0 GB/s at n=4096
+    {'s', 0, 10240, "vr2_u2_r0_w8_b4_g12_c2_f"},   // 4005.0 GB/s at n=8192
+    {'s', 0, 14336, "vr2_u2_r0_w8_b4_g11_c2_f"},   // 5376.3 GB/s at n=12288
+    {'s', 0, 18432, "vr2_u2_r0_w8_b4_g13"},   // 6843.5 GB/s at n=16384
+    {'s', 0, 22528, "vr2_u2_r0_w8_b4_g12"},   // 6863.3 GB/s at n=20480
+    {'s', 0, 26624, "vr2_u2_r0_w8_b4_g12"},   // 6923.8 GB/s at n=24576
+    {'s', 0, 30720, "vr2_u2_r0_w8_b4_g12"},   // 6951.2 GB/s at n=28672
+    {'s', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6975.4 GB/s at n=32768
+    {'d', 1, 1536, "vr4_u2_r0_w8_b0_g6"},   // 245.6 GB/s at n=1024
+    {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 680.6 GB/s at n=2048
+    {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1320.2 GB/s at n=4096
+    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1885.4 GB/s at n=8192
+    {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2179.7 GB/s at n=16384
+    {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2214.4 GB/s at n=24576
     {'d', 0, 1536, "vr4_u2_r0_w8"},   // 248.6 GB/s at n=1024
-    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 688.7 GB/s at n=2048
-    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1317.8 GB/s at n=4096
-    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1889.7 GB/s at n=8192
-    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2177.8 GB/s at n=16384
-    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2213.9 GB/s at n=24576
-    {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 323.8 GB/s at n=1024
-    {'c', 1, 3072, "vr2_u2_r0_w8_b4_g10"},   // 1022.3 GB/s at n=2048
-    {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2944.3 GB/s at n=4096
-    {'c', 1, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5174.3 GB/s at n=8192
-    {'c', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6869.2 GB/s at n=16384
-    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g13"},   // 328.3 GB/s at n=1024
-    {'c', 0, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1057.0 GB/s at n=2048
-    {'c', 0, 6144, "vr2_u2_r0_w8_b4_g11"},   // 2903.5 GB/s at n=4096
-    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5185.8 GB/s at n=8192
-    {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6875.6 GB/s at n=16384
-    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 332.9 GB/s at n=1024
-    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 631.5 GB/s at n=2048
-    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 916.6 GB/s at n=4096
-    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1099.5 GB/s at n=8192
-    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1120.0 GB/s at n=16384
-    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 338.8 GB/s at n=1024
-    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 630.1 GB/s at n=2048
-    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 924.8 GB/s at n=4096
-    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1101.3 GB/s at n=8192
-    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1122.5 GB/s at n=16384
+    {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 687.7 GB/s at n=2048
+    {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1315.8 GB/s at n=4096
+    {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1889.4 GB/s at n=8192
+    {'d', 0, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2178.4 GB/s at n=16384
+    {'d', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2214.4 GB/s at n=24576
+    {'c', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 321.2 GB/s at n=1024
+    {'c', 1, 3072, "vr2_u2_r0_w8_b4_g10"},   // 1015.3 GB/s at n=2048
+    {'c', 1, 6144, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 2929.4 GB/s at n=4096
+    {'c', 1, 12288, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 5151.3 GB/s at n=8192
+    {'c', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6854.2 GB/s at n=16384
+    {'c', 0, 1536, "vr2_u2_r0_w8_b4_g13"},   // 328.4 GB/s at n=1024
+    {'c', 0, 3072, "vr2_u2_r0_w8_b0_g7"},   // 1054.5 GB/s at n=2048
+    {'c', 0, 6144, "vr2_u2_r0_w8_b4_g11"},   // 2899.9 GB/s at n=4096
+    {'c', 0, 12288, "vr2_u2_r0_w8_b4_g10"},   // 5130.6 GB/s at n=8192
+    {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6858.4 GB/s at n=16384
+    {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 333.4 GB/s at n=1024
+    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 631.2 GB/s at n=2048
+    {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 920.2 GB/s at n=4096
+    {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1099.4 GB/s at n=8192
+    {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1119.9 GB/s at n=16384
+    {'z', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 338.7 GB/s at n=1024
+    {'z', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 630.2 GB/s at n=2048
+    {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 927.4 GB/s at n=4096
+    {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1101.4 GB/s at n=8192
+    {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1122.8 GB/s at n=16384
     {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.6 GB/s at n=1024
     {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 125.8 GB/s at n=2048
     {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 152.6 GB/s at n=4096
     {'w', 1, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.2 GB/s at n=8192
     {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.3 GB/s at n=1024
-    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 124.8 GB/s at n=2048
+    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 124.7 GB/s at n=2048
     {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 154.6 GB/s at n=4096
-    {'w', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.4 GB/s at n=8192
+    {'w', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.3 GB/s at n=8192
 };
 // END TUNED TABLE
 
