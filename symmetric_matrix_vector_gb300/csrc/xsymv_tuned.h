@@ -73,14 +73,14 @@ static const TunedEntry kTuned[] = {
     {'z', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 927.4 GB/s at n=4096
     {'z', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1101.4 GB/s at n=8192
     {'z', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8"},   // 1122.8 GB/s at n=16384
-    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.6 GB/s at n=1024
-    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 125.8 GB/s at n=2048
-    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 152.6 GB/s at n=4096
-    {'w', 1, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.2 GB/s at n=8192
-    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 85.3 GB/s at n=1024
-    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g4_c4"},   // 124.7 GB/s at n=2048
-    {'w', 0, 6144, "vr8_u1_r0_w4_b0_g5_c8"},   // 154.6 GB/s at n=4096
-    {'w', 0, 2147483647, "vr4_u2_r0_w8_b0_g4_c8_f"},   // 167.3 GB/s at n=8192
+    {'w', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 89.0 GB/s at n=1024
+    {'w', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 132.3 GB/s at n=2048
+    {'w', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 160.6 GB/s at n=4096
+    {'w', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 168.9 GB/s at n=8192
+    {'w', 0, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 88.3 GB/s at n=1024
+    {'w', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 132.4 GB/s at n=2048
+    {'w', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 160.6 GB/s at n=4096
+    {'w', 0, 2147483647, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 168.8 GB/s at n=8192
 };
 // END TUNED TABLE
 

@@ -22,6 +22,10 @@ static const Variant<dd> kVariants_w[] = {
     XSYMV_REG_GC(dd, 8, 1, 4, 0, 5, 8),
     XSYMV_REG_GC(dd, 8, 1, 4, 0, 7, 8),
     XSYMV_REG_GC(dd, 8, 1, 4, 0, 8, 8),
+    XSYMV_FUSED(dd, 4, 2, 8, 0, 5, 8),
+    XSYMV_FUSED(dd, 4, 2, 8, 0, 6, 8),
+    XSYMV_REG_GC(dd, 4, 2, 8, 0, 5, 8),
+    XSYMV_REG_GC(dd, 4, 2, 8, 0, 6, 8),
 };
 static_assert(sizeof(dd) == sizeof(xsymv_dd), "C-ABI type layout");
 }  // namespace xsymv
