@@ -26,6 +26,7 @@ static const Variant<c32> kVariants_c[] = {
     XSYMV_REG_G(c32, 2, 2, 8, 4, 13),
     XSYMV_FUSED(c32, 2, 2, 8, 4, 13, 2),
     XSYMV_FUSED(c32, 2, 2, 8, 4, 11, 2),
+    XSYMV_FUSED(c32, 2, 2, 8, 4, 9, 2),
 };
 static_assert(sizeof(c32) == sizeof(xsymv_c32), "C-ABI type layout");
 }  // namespace xsymv

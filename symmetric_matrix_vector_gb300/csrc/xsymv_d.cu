@@ -22,6 +22,9 @@ static const Variant<double> kVariants_d[] = {
     XSYMV_TICKET(double, 4, 2, 8, 0, 5, 8),
     XSYMV_REG_GC(double, 8, 1, 4, 0, 8, 8),
     XSYMV_FUSED(double, 4, 2, 8, 0, 5, 8),
+    XSYMV_FUSED(double, 4, 2, 8, 0, 4, 8),
+    XSYMV_FUSED(double, 4, 2, 8, 0, 6, 8),
+    XSYMV_REG_GC(double, 4, 2, 8, 0, 6, 8),
 };
 static_assert(sizeof(double) == sizeof(double), "C-ABI type layout");
 }  // namespace xsymv

@@ -37,6 +37,10 @@ static const Variant<float> kVariants_s[] = {
     XSYMV_FUSED(float, 2, 2, 8, 4, 12, 2),
     XSYMV_FUSED(float, 2, 2, 8, 4, 11, 2),
     XSYMV_FUSED(float, 1, 2, 8, 6, 7, 2),
+    XSYMV_FUSED(float, 2, 2, 8, 4, 13, 2),
+    XSYMV_FUSED(float, 2, 2, 8, 4, 9, 2),
+    XSYMV_FUSED(float, 1, 2, 8, 6, 9, 2),
+    XSYMV_FUSED(float, 1, 2, 8, 6, 14, 2),
 };
 static_assert(sizeof(float) == sizeof(float), "C-ABI type layout");
 }  // namespace xsymv

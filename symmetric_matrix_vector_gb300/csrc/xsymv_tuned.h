@@ -18,7 +18,7 @@ struct TunedEntry {
 // BEGIN TUNED TABLE
 static const TunedEntry kTuned[] = {
     {'s', 1, 768, "vr1_u2_r0_w8_b6_g7"},   // 47.6 GB/s at n=512
-    {'s', 1, 1536, "vr1_u2_r0_w8_b6_g14"},   // 164.3 GB/s at n=1024
+    {'s', 1, 1536, "vr2_u2_r0_w8_b4_g13_c2_f"},   // 171.6 GB/s at n=1024
     {'s', 1, 2560, "vr2_u2_r0_w8_b4_g13"},   // 565.9 GB/s at n=2048
     {'s', 1, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1179.8 GB/s at n=3072
     {'s', 1, 6144, "vr1_u2_r0_w8_b6_g14"},   // 1776.0 GB/s at n=4096
@@ -30,7 +30,7 @@ static const TunedEntry kTuned[] = {
     {'s', 1, 30720, "vr2_u2_r0_w8_b4_g11"},   // 6941.3 GB/s at n=28672
     {'s', 1, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6975.5 GB/s at n=32768
     {'s', 0, 768, "vr1_u2_r0_w8"},   // 48.5 GB/s at n=512
-    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g11_c2_f"},   // 166.7 GB/s at n=1024
+    {'s', 0, 1536, "vr1_u2_r0_w8_b6_g14_c2_f"},   // 173.3 GB/s at n=1024
     {'s', 0, 2560, "vr1_u2_r0_w8_b0_g9"},   // 628.4 GB/s at n=2048
     {'s', 0, 3584, "vr1_u2_r0_w8_b0_g9"},   // 1260.0 GB/s at n=3072
     {'s', 0, 6144, "vr1_u2_r0_w8_b6_g11"},   // 1844.0 GB/s at n=4096
@@ -44,10 +44,10 @@ static const TunedEntry kTuned[] = {
     {'d', 1, 1536, "vr4_u2_r0_w8_b0_g6"},   // 245.6 GB/s at n=1024
     {'d', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 680.6 GB/s at n=2048
     {'d', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1320.2 GB/s at n=4096
-    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1885.4 GB/s at n=8192
+    {'d', 1, 12288, "vr4_u2_r0_w8_b0_g6_c8_f"},   // 1871.8 GB/s at n=8192
     {'d', 1, 20480, "vr4_u2_r0_w8_b0_g5_c8"},   // 2179.7 GB/s at n=16384
     {'d', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 2214.4 GB/s at n=24576
-    {'d', 0, 1536, "vr4_u2_r0_w8"},   // 248.6 GB/s at n=1024
+    {'d', 0, 1536, "vr4_u2_r0_w8_b0_g6_c8"},   // 248.3 GB/s at n=1024
     {'d', 0, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 687.7 GB/s at n=2048
     {'d', 0, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1315.8 GB/s at n=4096
     {'d', 0, 12288, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 1889.4 GB/s at n=8192
@@ -64,7 +64,7 @@ static const TunedEntry kTuned[] = {
     {'c', 0, 12288, "vr2_u2_r0_w8_b4_g10"},   // 5130.6 GB/s at n=8192
     {'c', 0, 2147483647, "vr2_u2_r0_w8_b4_g13"},   // 6858.4 GB/s at n=16384
     {'z', 1, 1536, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 333.4 GB/s at n=1024
-    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 631.2 GB/s at n=2048
+    {'z', 1, 3072, "vr4_u2_r0_w8_b0_g6_c8_f"},   // 630.5 GB/s at n=2048
     {'z', 1, 6144, "vr4_u2_r0_w8_b0_g5_c8_f"},   // 920.2 GB/s at n=4096
     {'z', 1, 12288, "vr4_u2_r0_w8_b0_g5_c8"},   // 1099.4 GB/s at n=8192
     {'z', 1, 2147483647, "vr4_u2_r0_w8_b0_g5_c8"},   // 1119.9 GB/s at n=16384

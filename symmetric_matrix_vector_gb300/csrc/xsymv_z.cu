@@ -18,6 +18,9 @@ static const Variant<c64> kVariants_z[] = {
     XSYMV_REG_GC(c64, 2, 2, 8, 0, 4, 8),
     XSYMV_TICKET(c64, 4, 2, 8, 0, 5, 8),
     XSYMV_FUSED(c64, 4, 2, 8, 0, 5, 8),
+    XSYMV_FUSED(c64, 4, 2, 8, 0, 4, 8),
+    XSYMV_FUSED(c64, 4, 2, 8, 0, 6, 8),
+    XSYMV_REG_GC(c64, 4, 2, 8, 0, 6, 8),
 };
 static_assert(sizeof(c64) == sizeof(xsymv_c64), "C-ABI type layout");
 }  // namespace xsymv
