@@ -616,8 +616,15 @@ def time_back_to_back(torch, stream, fn, reps):
     """ms per call of `reps` calls enqueued back to back.  The GPU first
     spins for longer than the host needs to enqueue them all, so that the
     calls run back to back on the GPU and the events time the GPU's work,
-    not the host's rate of issuing calls."""
-    host_s = host_us_per_call(torch, fn, 20) * 1e-6 * reps
+    not the host's rate of issuing calls.  A few calls queued the same way
+    beforehand leave the library in the state it keeps for back-to-back
+    calls (it learns it from the calls it has run on the stream)."""
+    per_call_s = host_us_per_call(torch, fn, 20) * 1e-6
+    torch.cuda._sleep(int((1.5 * per_call_s * 10 + 2e-4) * NOMINAL_SM_MHZ * 1e6))
+    for _ in range(10):
+        fn()
+    torch.cuda.synchronize()
+    host_s = per_call_s * reps
     torch.cuda._sleep(int((1.5 * host_s + 2e-4) * NOMINAL_SM_MHZ * 1e6))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)

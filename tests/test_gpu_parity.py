@@ -308,22 +308,31 @@ def test_non_default_stream(o):
     assert np.max(err) <= TOL["s"]
 
 
-def test_launch_count_and_timing(lib):
-    """every call launches exactly the main kernel and the finaliser (plus,
-    on the first call of a plan, the kernel that builds its tables)"""
-    p = inputs.make_problem("s", "U", 1000, alpha=1.0, beta=0.5, seed=1)
-    dp = DeviceProblem(p)
-    st, _ = dp.run()    # a new plan: its warp and row tables are built once (one more launch)
-    assert st == 0
-    c0 = lib.xsymv_launch_count()
-    lib.xsymv_timing_enable(True)
-    for _ in range(5):
-        st, _ = dp.run()
+@pytest.mark.parametrize("variant,per_call", [("vr2_u2_r0_w8_b4_g13", 2),
+                                               ("vr2_u2_r0_w8_b4_g13_c2_f", 1)])
+def test_launch_count_and_timing(lib, variant, per_call):
+    """every call of a two-kernel variant launches exactly the main kernel and
+    the finaliser, a one-launch variant one kernel (plus, on the first call of
+    a plan, the kernel that builds its tables); a forced variant is used as
+    is, even back to back"""
+    names = [lib.xsymv_variant_name("s", i) for i in range(lib.xsymv_variant_count("s"))]
+    assert lib.xsymv_set_variant("s", names.index(variant)) == 0
+    try:
+        p = inputs.make_problem("s", "U", 1000, alpha=1.0, beta=0.5, seed=1)
+        dp = DeviceProblem(p)
+        st, _ = dp.run()    # a new plan: its warp and row tables are built once (one more launch)
         assert st == 0
-    calls, main_ms, call_ms = lib.xsymv_timing_read()
-    lib.xsymv_timing_enable(False)
-    assert lib.xsymv_launch_count() - c0 == 10
-    assert calls == 5 and 0 < main_ms <= call_ms
+        c0 = lib.xsymv_launch_count()
+        lib.xsymv_timing_enable(True)
+        for _ in range(5):
+            st, _ = dp.run()
+            assert st == 0
+        calls, main_ms, call_ms = lib.xsymv_timing_read()
+        lib.xsymv_timing_enable(False)
+        assert lib.xsymv_launch_count() - c0 == 5 * per_call
+        assert calls == 5 and 0 < main_ms <= call_ms
+    finally:
+        lib.xsymv_set_variant("s", -1)
 
 
 @pytest.mark.parametrize("kind", KINDS)
